@@ -1,0 +1,403 @@
+#!/usr/bin/env python3
+"""Benchmark of the W4A8 block-64 prefill linear on GB300 (one JSON line on rank 0).
+
+A step is one pass of the whole hot path over one batch: for every linear of the
+workload, the fused call w4a8_prefill_linear (activation pre-pass + tensor-core
+contraction + epilogue), inputs resident in HBM.  L2 is flushed (256 MiB written)
+before every timed step, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c1] [--impl ours|reference]
+
+Multi-GPU runs are replicas: each rank runs the whole workload on its own GPU with no
+data exchange (weak scaling); value = units of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "W4A8 block64 prefill linear: effective TOPS & tok/s at M=512; % of INT8 peak"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--workload", default="c1", choices=["c0", "c1", "c2", "c3", "c4"])
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ distributed (replicas)
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    """Max over ranks (the timed region's slowest rank)."""
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Units processed by all ranks divided by the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            ident = str(device_index)
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "50", "-i", ident]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ peaks
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ workload
+def load_workload(key, device):
+    from w4a8_block_quantized_gb300 import binding, synth
+    title, specs = synth.workload(key)
+    lin = []
+    for spec in specs:
+        d = synth.make_linear(spec)
+        t = {k: (torch.from_numpy(v).to(device) if isinstance(v, np.ndarray) else v) for k, v in d.items()}
+        t["ws"] = binding.workspace(binding.prefill_workspace_bytes(spec.M, spec.N, spec.K), device)
+        t["y"] = torch.empty((spec.M, spec.N), dtype=torch.float32, device=device)
+        t["spec"] = spec
+        t["host"] = d
+        lin.append(t)
+    return title, specs, lin
+
+
+def run_bench(args):
+    from w4a8_block_quantized_gb300 import binding
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    binding.load()
+    title, specs, lin = load_workload(args.workload, device)
+    M = specs[0].M
+    ops_per_step = sum(s.ops for s in specs)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def step():
+        for t in lin:
+            binding.prefill_linear(t["x"], t["wq"], t["s_w"], t["z_w"], t["bias"], y=t["y"], ws=t["ws"],
+                                   stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    if binding.sync_status(stream) != 0:
+        raise RuntimeError("device status reported a timeout during warm-up")
+
+    # ---------------- timed region: K fused steps, L2 flushed before each
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    dist_barrier(world)
+    torch.cuda.synchronize(device)
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(device)
+    dist_barrier(world)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_s = reduce_max(sum(step_ms) / 1e3, world, device)
+    if binding.sync_status(stream) != 0:
+        raise RuntimeError("device status reported a timeout in the timed region")
+    ms_per_step = total_s * 1e3 / args.steps
+    value_tops = whole_job_rate(ops_per_step * args.steps, world, total_s) / 1e12
+    tok_s = whole_job_rate(M * args.steps, world, total_s)
+
+    # ---------------- kernel-level timing (same stream, CUDA events): the GEMM alone
+    # through the split calls, and the pre-pass alone, each after an L2 flush.
+    gemm_ms, prep_ms = [], []
+    prepared = []
+    for t in lin:
+        s = t["spec"]
+        act = binding.prepare_activations(t["x"], stream=stream)
+        wsc = binding.prepare_weights(t["s_w"], t["z_w"], s.K, stream=stream)
+        prepared.append((act, wsc))
+    kreps = max(20, min(args.steps, 200))
+    for _ in range(kreps):
+        g_ms = p_ms = 0.0
+        for t, (act, wsc) in zip(lin, prepared):
+            s = t["spec"]
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            flush.zero_()
+            e0.record(stream)
+            binding.prepare_activations(t["x"], act=act, stream=stream)
+            e1.record(stream)
+            binding.linear_prepared(act, t["wq"], wsc, s.M, s.K, bias=t["bias"], y=t["y"], stream=stream)
+            e2.record(stream)
+            e2.synchronize()
+            p_ms += e0.elapsed_time(e1)
+            g_ms += e1.elapsed_time(e2)
+        gemm_ms.append(g_ms)
+        prep_ms.append(p_ms)
+    gemm_avg = statistics.fmean(gemm_ms) / len(lin)   # per launch
+    prep_avg = statistics.fmean(prep_ms) / len(lin)
+
+    hbm_gbs, bf16_tf, peak_src = measured_peaks()
+    # Contraction peak in effective int8-equivalent ops: fp8 = 2x bf16 (nominal ratio),
+    # and each int8 x u4 MAC costs two e4m3 MACs (the two nibble planes).
+    tensor_peak = bf16_tf * 2.0 / 2.0
+    gemm_ops = ops_per_step / len(lin)
+    gemm_tops = gemm_ops / (gemm_avg * 1e-3) / 1e12
+    prep_bytes = sum(s.M * s.K * 4 + s.M * s.K * 2 + s.M * 4 + s.M * (s.K // 64) * 4 for s in specs) / len(lin)
+    prep_gbs = prep_bytes / (prep_avg * 1e-3) / 1e9
+
+    # ---------------- end to end through the C ABI with host buffers
+    x_host = [torch.from_numpy(t["host"]["x"]).pin_memory() for t in lin]
+    y_host = [torch.empty(t["y"].shape, dtype=torch.float32).pin_memory() for t in lin]
+    e2e_steps = max(5, min(args.steps, 200))
+    e2e_ms = []
+    for i in range(e2e_steps + 3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for t, xh, yh in zip(lin, x_host, y_host):
+            t["x"].copy_(xh, non_blocking=True)
+            binding.prefill_linear(t["x"], t["wq"], t["s_w"], t["z_w"], t["bias"], y=t["y"], ws=t["ws"],
+                                   stream=stream)
+            yh.copy_(t["y"], non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 3:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_s = reduce_max(sum(e2e_ms) / 1e3, world, device)
+    h2d = sum(s.M * s.K * 4 for s in specs)
+    d2h = sum(s.M * s.N * 4 for s in specs)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(lin, specs, args.cpu_seconds)
+
+    clocks = clk.summary()
+    out = {
+        "metric": METRIC,
+        "value": round(value_tops, 3),
+        "unit": "TOPS",
+        "tok_s": round(tok_s, 1),
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3xe4m3->f32 (exact int8 x u4 blocks), f32 epilogue",
+        "data": "synthetic (seeded Philox; no model weights)",
+        "config": {"workload": f"{args.workload}: {title}",
+                   "linears": [{"name": s.name, "M": s.M, "K": s.K, "N": s.N, "bias": s.bias} for s in specs],
+                   "tokens_per_step": M, "ops_per_step": ops_per_step,
+                   "l2": "flushed before every timed step (256 MiB memset, outside the timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "gemm_kernel (tcgen05 kind::f8f6f4 + epilogue)",
+                     "achieved": round(gemm_tops, 2), "peak": round(tensor_peak, 1), "unit": "TOPS",
+                     "frac": round(gemm_tops / tensor_peak, 4), "traffic": None,
+                     "peak_source": f"{peak_src} bf16 burst x2 (fp8 nominal ratio) /2 (two e4m3 MACs per int8 MAC)",
+                     "gemm_us_per_launch": round(gemm_avg * 1e3, 3)},
+        "prepass": {"bound": "hbm", "achieved": round(prep_gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
+                    "frac": round(prep_gbs / hbm_gbs, 4), "us_per_launch": round(prep_avg * 1e3, 3),
+                    "peak_source": peak_src},
+        "e2e": {"value": round(whole_job_rate(ops_per_step * e2e_steps, world, e2e_s) / 1e12, 3), "unit": "TOPS",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_s * 1e3 / e2e_steps, 4)},
+        "gpu_launches": args.steps * 2 * len(lin),
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+def oracle_rows_for(spec, seconds, x, host):
+    """Rows of the workload the oracle processes in about `seconds` (calibrated on 4 rows)."""
+    import oracle
+    rows = np.arange(min(4, spec.M), dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.prefill_linear(x, host["wq"], host["s_w"], host["z_w"], host["bias"], rows=rows)
+    dt = max(time.perf_counter() - t0, 1e-4) / len(rows)
+    return int(max(4, min(spec.M, seconds / dt)))
+
+
+def cpu_baseline(lin, specs, seconds):
+    import oracle
+    oracle.build()
+    total_ops, total_s, parts = 0, 0.0, []
+    for t, s in zip(lin, specs):
+        h = t["host"]
+        n = oracle_rows_for(s, seconds / len(specs), h["x"], h)
+        rows = np.linspace(0, s.M - 1, n).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.prefill_linear(h["x"], h["wq"], h["s_w"], h["z_w"], h["bias"], rows=rows)
+        dt = time.perf_counter() - t0
+        total_ops += 2 * n * s.N * s.K
+        total_s += dt
+        parts.append(f"{s.name}: {n}/{s.M} rows")
+    return {"value": round(total_ops / total_s / 1e12, 6), "unit": "TOPS", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": "evenly spaced rows of the workload, all outputs: " + "; ".join(parts),
+            "seconds": round(total_s, 2)}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from w4a8_block_quantized_gb300 import synth
+    oracle.build()
+    title, specs = synth.workload(args.workload)
+    hosts = [synth.make_linear(s) for s in specs]
+    per_step = max(0.5, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
+    rows = [np.linspace(0, s.M - 1, oracle_rows_for(s, per_step / len(specs), h["x"], h)).astype(np.int64)
+            for s, h in zip(specs, hosts)]
+
+    def step():
+        for s, h, r in zip(specs, hosts, rows):
+            oracle.prefill_linear(h["x"], h["wq"], h["s_w"], h["z_w"], h["bias"], rows=r)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    ops = args.steps * sum(2 * len(r) * s.N * s.K for s, r in zip(specs, rows))
+    value = ops / dt / 1e12
+    toks = args.steps * sum(len(r) for r in rows) / len(rows) / dt
+    sample = "; ".join(f"{s.name}: {len(r)}/{s.M} evenly spaced rows" for s, r in zip(specs, rows))
+    out = {
+        "metric": METRIC, "value": round(value, 6), "unit": "TOPS", "tok_s": round(toks, 2), "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int32/int64 blocks, f64 output", "data": "synthetic (seeded Philox)",
+        "config": {"workload": f"{args.workload}: {title}",
+                   "linears": [{"name": s.name, "M": s.M, "K": s.K, "N": s.N, "bias": s.bias} for s in specs]},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TOPS", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_bench(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,140 @@
+/*
+ * w4a8.h -- C ABI of the GB300 (sm_103a) W4A8 block-64 quantized prefill linear.
+ *
+ * The operation ("MNN LLM inference on the SpacemiT K3", section 3 eqs. (1)-(3),
+ * section 4 steps 1-3):
+ *
+ *   weights   w[n,k] ~= s_w[n,b] * (q[n,k] - z_w[n,b]),   b = k / 64            (eq. 1)
+ *   act.      s_a[m] = max_k |x[m,k]| / 127 (fp32), a_q[m,k] = clamp(round_half_away(x[m,k] / s_a[m]), +-127)
+ *   row sums  rs[m,b] = sum_{k in block b} a_q[m,k]            ("srcKernelSum", section 4)
+ *   output    y[m,n] = s_a[m] * sum_b s_w[n,b] * (acc[m,n,b] - z_w[n,b] * rs[m,b]) + bias[n]   (eq. 2)
+ *             acc[m,n,b] = sum_{k in block b} a_q[m,k] * q[n,k]   (exact int32)
+ *
+ * Layouts (all row-major, no padding):
+ *   x       fp32  [M][K]            activations
+ *   a_q     int8  [M][K]            INT8 codes
+ *   a_scale fp32  [M]               s_a
+ *   rowsum  int32 [M][K/64]         rs
+ *   wq      uint8 [N][K/2]          u4 codes, k even in the low nibble, k odd in the high nibble
+ *   w_scale fp16  [N][K/64]         s_w, passed as raw IEEE binary16 bit patterns (uint16_t)
+ *   w_zero  fp16  [N][K/64]         z_w, same encoding; a real value, not necessarily an integer
+ *   bias    fp32  [N] or NULL
+ *   y       fp32  [M][N]
+ *
+ * Conventions for every call below:
+ *   - Every array pointer is a DEVICE pointer owned by the caller; the library never
+ *     allocates, frees or retains memory.  Scratch comes from the caller's `workspace`.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous: W4A8_OK means the work was validated and enqueued.
+ *   - Shapes: K must be a positive multiple of 64; M >= 0 and N >= 0 (M == 0 or
+ *     N == 0 is an empty problem: nothing is launched and W4A8_OK is returned);
+ *     M, N, K <= 2^31 - 1.
+ *   - Alignment: x, a_q, wq, y and workspace must be 16-byte aligned; the other arrays
+ *     naturally aligned for their element type.
+ *   - A violated precondition returns a negative status and launches nothing.
+ *   - Inputs are assumed finite; non-finite activations give unspecified codes.
+ *   - Every wait inside the kernels is bounded.  A kernel that gives up records
+ *     W4A8_ERR_TIMEOUT in a per-device status word and returns early; read it with
+ *     w4a8_sync_status().
+ *   - The current CUDA device must be an sm_103 GPU; the library holds no state besides
+ *     that status word and the one-time device check.
+ */
+#ifndef W4A8_H_
+#define W4A8_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4A8_OK = 0,
+    W4A8_ERR_ARG = -1,        /* NULL pointer or negative size */
+    W4A8_ERR_ALIGN = -2,      /* pointer misaligned */
+    W4A8_ERR_SHAPE = -3,      /* K not a positive multiple of 64, size too large, bad window */
+    W4A8_ERR_CUDA = -4,       /* a CUDA runtime call or a launch failed */
+    W4A8_ERR_TIMEOUT = -5,    /* a kernel gave up on a bounded wait (read by w4a8_sync_status) */
+    W4A8_ERR_WORKSPACE = -6,  /* workspace NULL or smaller than the *_workspace_bytes value */
+    W4A8_ERR_DEVICE = -7      /* current device is not an sm_103 GPU */
+} w4a8_status;
+
+/* Activation pre-pass (section 4 step 1: absmax -> scale -> INT8 codes + srcKernelSum),
+ * one read of x.  Outputs a_q [M][K], a_scale [M], rowsum [M][K/64]. */
+int w4a8_quant_pack(const float *x, int64_t M, int64_t K,
+                    int8_t *a_q, float *a_scale, int32_t *rowsum, void *stream);
+
+/* Quantized linear from pre-quantized activations (section 3 eq. (2), section 4
+ * steps 2-3): block-64 integer contraction on the tensor cores, then the scale /
+ * zero-point / bias epilogue writing fp32 y [M][N] directly.
+ * workspace: at least w4a8_linear_workspace_bytes(M, N, K) bytes (the activation
+ * operand re-encoded for the tensor cores). */
+int w4a8_linear(const int8_t *a_q, const float *a_scale, const int32_t *rowsum,
+                const uint8_t *wq, const uint16_t *w_scale, const uint16_t *w_zero,
+                const float *bias, float *y, int64_t M, int64_t N, int64_t K,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/* Fused prefill linear: the pre-pass writes the tensor-core operand, the activation
+ * scales and the row sums straight into the workspace (no int8 a_q array), then
+ * the linear runs.  Same result, bit for bit, as w4a8_quant_pack + w4a8_linear.
+ * workspace: at least w4a8_prefill_workspace_bytes(M, N, K) bytes. */
+int w4a8_prefill_linear(const float *x, const uint8_t *wq, const uint16_t *w_scale,
+                        const uint16_t *w_zero, const float *bias, float *y,
+                        int64_t M, int64_t N, int64_t K,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* Split form of w4a8_prefill_linear, for callers that reuse one side across calls
+ * (one activation pre-pass shared by several linears that read the same input, or
+ * weight scales laid out once at load time):
+ *   w4a8_prepare_activations  section 4 step 1 into `act` (tensor-core operand planes,
+ *                             s_a, transposed row sums); act: >= w4a8_prepared_activations_bytes(M, K)
+ *   w4a8_prepare_weights      re-lays out s_w / z_w for the epilogue into `wsc`;
+ *                             wsc: >= w4a8_prepared_weights_bytes(N, K)
+ *   w4a8_linear_prepared      the contraction + epilogue from both (section 4 steps 2-3)
+ * The buffers are opaque; their contents are only valid for the same M / N / K.
+ * prepare_activations + prepare_weights + linear_prepared equals w4a8_prefill_linear
+ * bit for bit. */
+int w4a8_prepare_activations(const float *x, int64_t M, int64_t K, void *act, size_t act_bytes,
+                             void *stream);
+int w4a8_prepare_weights(const uint16_t *w_scale, const uint16_t *w_zero, int64_t N, int64_t K,
+                         void *wsc, size_t wsc_bytes, void *stream);
+int w4a8_linear_prepared(const void *act, const uint8_t *wq, const void *wsc, const float *bias,
+                         float *y, int64_t M, int64_t N, int64_t K, void *stream);
+size_t w4a8_prepared_activations_bytes(int64_t M, int64_t K);
+size_t w4a8_prepared_weights_bytes(int64_t N, int64_t K);
+
+/* Workspace sizes in bytes (0 for an empty problem; (size_t)-1 for invalid shapes). */
+size_t w4a8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+size_t w4a8_prefill_workspace_bytes(int64_t M, int64_t N, int64_t K);
+size_t w4a8_debug_workspace_bytes(int64_t m_cnt, int64_t K);
+
+/* Debug: the exact per-block int32 accumulators acc[m][n][b] (section 3 eq. (2), first
+ * sum) for the window m0 <= m < m0 + m_cnt, n0 <= n < n0 + n_cnt, computed by the same
+ * tensor-core contraction as w4a8_linear.  acc: int32 [m_cnt][n_cnt][K/64].
+ * The window must lie inside [0, M) x [0, N) and be non-empty. */
+int w4a8_debug_block_acc(const int8_t *a_q, const uint8_t *wq, int64_t M, int64_t N, int64_t K,
+                         int64_t m0, int64_t m_cnt, int64_t n0, int64_t n_cnt, int32_t *acc,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronizes `stream`, then returns and clears the current device's status word:
+ * W4A8_OK, W4A8_ERR_TIMEOUT if a kernel gave up on a wait since the last call, or
+ * W4A8_ERR_CUDA if the synchronization itself failed. */
+int w4a8_sync_status(void *stream);
+
+/* Diagnostic: launches one CTA that waits on a barrier nothing will ever complete,
+ * with a wait limit of `limit_us` microseconds (1..10^6), so that the bounded-wait
+ * path can be tested.  The kernel records W4A8_ERR_TIMEOUT and returns. */
+int w4a8_selftest_wait_timeout(int64_t limit_us, void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *w4a8_status_string(int status);
+
+/* ABI version of this header (major * 100 + minor). */
+int w4a8_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A8_H_ */

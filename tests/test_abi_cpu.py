@@ -1,0 +1,84 @@
+"""The C-ABI library loads and exports every symbol include/w4a8.h declares; argument
+validation that needs no GPU (shapes, null pointers, workspace sizes) returns the
+documented status codes.  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a8.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from w4a8_block_quantized_gb300 import build, binding
+    build.build()
+    return binding.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4a8_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    syms = declared_symbols()
+    for need in ("w4a8_quant_pack", "w4a8_linear", "w4a8_prefill_linear", "w4a8_debug_block_acc"):
+        assert need in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from w4a8_block_quantized_gb300 import binding
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in binding.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    from w4a8_block_quantized_gb300 import binding as b
+    for code in (b.W4A8_OK, b.W4A8_ERR_ARG, b.W4A8_ERR_ALIGN, b.W4A8_ERR_SHAPE, b.W4A8_ERR_CUDA,
+                 b.W4A8_ERR_TIMEOUT, b.W4A8_ERR_WORKSPACE, b.W4A8_ERR_DEVICE):
+        s = b.status_string(code)
+        assert s and s != "unknown status"
+    assert b.status_string(12345) == "unknown status"
+    assert lib.w4a8_abi_version() == 100
+
+
+def test_shape_checks_need_no_gpu(lib):
+    from w4a8_block_quantized_gb300 import binding as b
+    P = ctypes.c_void_p
+    dummy = P(16)  # never dereferenced: validation fails first
+    assert lib.w4a8_quant_pack(dummy, 4, 100, dummy, dummy, dummy, None) == b.W4A8_ERR_SHAPE
+    assert lib.w4a8_quant_pack(dummy, 4, 0, dummy, dummy, dummy, None) == b.W4A8_ERR_SHAPE
+    assert lib.w4a8_quant_pack(dummy, -1, 64, dummy, dummy, dummy, None) == b.W4A8_ERR_ARG
+    assert lib.w4a8_quant_pack(None, 4, 64, dummy, dummy, dummy, None) == b.W4A8_ERR_ARG
+    assert lib.w4a8_quant_pack(P(8), 4, 64, dummy, dummy, dummy, None) == b.W4A8_ERR_ALIGN
+    # empty problems are valid no-ops
+    assert lib.w4a8_quant_pack(None, 0, 64, None, None, None, None) == b.W4A8_OK
+    assert lib.w4a8_prefill_linear(None, None, None, None, None, None, 0, 8, 64, None, 0, None) == b.W4A8_OK
+    assert lib.w4a8_linear(None, None, None, None, None, None, None, None, 8, 0, 64, None, 0, None) == b.W4A8_OK
+    assert lib.w4a8_linear(dummy, dummy, dummy, dummy, dummy, dummy, None, dummy, 8, 8, 96, dummy, 1 << 20,
+                           None) == b.W4A8_ERR_SHAPE
+    # workspace too small is reported before any launch
+    need = lib.w4a8_prefill_workspace_bytes(8, 8, 64)
+    assert lib.w4a8_prefill_linear(dummy, dummy, P(32), P(32), None, dummy, 8, 8, 64, dummy, need - 1,
+                                   None) == b.W4A8_ERR_WORKSPACE
+    # debug window outside the problem
+    assert lib.w4a8_debug_block_acc(dummy, dummy, 8, 8, 64, 4, 8, 0, 8, dummy, dummy, 1 << 20,
+                                    None) == b.W4A8_ERR_SHAPE
+
+
+def test_workspace_sizes(lib):
+    M, N, K = 512, 3072, 1024
+    nb = K // 64
+    lin = lib.w4a8_linear_workspace_bytes(M, N, K)
+    pre = lib.w4a8_prefill_workspace_bytes(M, N, K)
+    # operand planes (2 bytes per activation) + transposed row sums + re-laid-out scales
+    assert lin >= 2 * M * K + nb * M * 4 + nb * N * 8
+    assert pre >= lin + 4 * M
+    assert lib.w4a8_linear_workspace_bytes(0, N, K) == 0
+    assert lib.w4a8_linear_workspace_bytes(M, N, 100) == ctypes.c_size_t(-1).value
+    assert lib.w4a8_debug_workspace_bytes(7, 128) >= 7 * 256

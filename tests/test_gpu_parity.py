@@ -1,0 +1,263 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same
+seeded inputs.  Integer stages bit-exact; fp32 output within the stated tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import check_y, dev, inputs_to_dev, to_dev
+from w4a8_block_quantized_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from w4a8_block_quantized_gb300 import binding, build
+    build.build()
+    binding.load()
+    oracle.build()
+    torch.cuda.set_device(0)
+    yield
+    assert binding.sync_status() == 0
+
+
+def B():
+    from w4a8_block_quantized_gb300 import binding
+    return binding
+
+
+# ------------------------------------------------------------------ pre-pass
+@pytest.mark.parametrize("M,K", [(1, 64), (3, 128), (128, 1024), (129, 1024), (77, 2048), (40, 4096),
+                                 (9, 6144), (33, 14336), (5, 16384), (3, 20480)])
+def test_quant_pack_bitexact(M, K):
+    d = synth.random_small(M, K, 1, seed=M * 7 + K)
+    x = d["x"]
+    a_q, s_a, rs = B().quant_pack(to_dev(x))
+    ra, rsa, rrs = oracle.quant_pack(x)
+    assert np.array_equal(s_a.cpu().numpy(), rsa)
+    assert np.array_equal(a_q.cpu().numpy(), ra)
+    assert np.array_equal(rs.cpu().numpy(), rrs)
+
+
+def test_quant_pack_golden_and_degenerate_rows():
+    from golden_cases import quant_tie_rule
+    x, a_q, s_a, rs = quant_tie_rule()
+    ga, gs, gr = B().quant_pack(to_dev(x))
+    assert np.array_equal(gs.cpu().numpy(), s_a)
+    assert np.array_equal(ga.cpu().numpy(), a_q)
+    assert np.array_equal(gr.cpu().numpy(), rs)
+
+
+# ------------------------------------------------------------------ block accumulators
+def _acc_case(a_q, q, m0=0, mc=None, n0=0, nc=None):
+    N = q.shape[0]
+    wq = synth.pack_u4(q)
+    got = B().debug_block_acc(to_dev(a_q), to_dev(wq), N, m0, mc, n0, nc).cpu().numpy()
+    ref = oracle.block_acc(a_q, wq, N, m0, mc, n0, nc)
+    assert np.array_equal(got, ref), f"{int((got != ref).sum())} accumulators differ"
+
+
+def test_block_acc_exact_extremes():
+    """Largest magnitudes and cancellation patterns the int8 x u4 block sums can take."""
+    K, M, N = 512, 130, 70
+    a = np.zeros((M, K), np.int8)
+    q = np.zeros((N, K), np.uint8)
+    a[0] = 127
+    a[1] = -127
+    a[2] = -128
+    a[3, 0::2], a[3, 1::2] = 127, -127           # alternating signs
+    a[4] = 1
+    a[4, ::64] = 127                              # one large term + many small ones
+    a[5] = -1
+    a[5, 5::64] = -128
+    rng = np.random.default_rng(0)
+    a[6:] = rng.integers(-128, 128, size=(M - 6, K)).astype(np.int8)
+    q[0] = 15
+    q[1, 0::2], q[1, 1::2] = 15, 0
+    q[2] = 1
+    q[3, ::3] = 15
+    q[4:] = rng.integers(0, 16, size=(N - 4, K)).astype(np.uint8)
+    _acc_case(a, q)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 64), (1, 64, 64), (127, 63, 128), (128, 256, 192), (129, 257, 256),
+                                   (300, 200, 1024), (64, 1000, 128), (200, 512, 2048)])
+def test_block_acc_random(M, N, K):
+    rng = np.random.default_rng(M * 1000 + N + K)
+    a = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    q = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+    _acc_case(a, q)
+
+
+def test_block_acc_windows():
+    rng = np.random.default_rng(3)
+    M, N, K = 400, 700, 256
+    a = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    q = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+    _acc_case(a, q, m0=5, mc=131, n0=3, nc=300)
+    _acc_case(a, q, m0=399, mc=1, n0=699, nc=1)
+    _acc_case(a, q, m0=128, mc=200, n0=256, nc=444)
+
+
+# ------------------------------------------------------------------ full linear
+def _run_both(d):
+    g = inputs_to_dev(d)
+    y_fused = B().prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"])
+    a_q, s_a, rs = B().quant_pack(g["x"])
+    y_sep = B().linear(a_q, s_a, rs, g["wq"], g["s_w"], g["z_w"], g["bias"])
+    return y_fused, y_sep
+
+
+@pytest.mark.parametrize("M,K,N,bias", [(1, 64, 1, False), (1, 64, 16, True), (7, 128, 33, True),
+                                        (128, 1024, 256, False), (129, 192, 257, True), (255, 1024, 130, True),
+                                        (300, 2048, 513, False), (64, 64, 4000, True), (513, 4096, 64, False),
+                                        (17, 16384, 100, True), (9, 20480, 70, False)])
+def test_linear_small_shapes(M, K, N, bias):
+    d = synth.random_small(M, K, N, seed=M + K + N, bias=bias)
+    y_fused, y_sep = _run_both(d)
+    y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
+    check_y(y_fused, y_ref, bound, f"fused {M}x{K}->{N}")
+    assert torch.equal(y_fused, y_sep), "fused and separate calls differ"
+
+
+@pytest.mark.parametrize("key", ["c0", "c1", "c2", "c3"])
+def test_workloads_full(key):
+    _, specs = synth.workload(key)
+    for spec in specs:
+        d = synth.make_linear(spec)
+        y_fused, y_sep = _run_both(d)
+        y_ref, bound, a_q, s_a, rs = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
+        check_y(y_fused, y_ref, bound, f"{key}/{spec.name}")
+        assert torch.equal(y_fused, y_sep)
+        ga, gs, gr = B().quant_pack(to_dev(d["x"]))
+        assert np.array_equal(ga.cpu().numpy(), a_q) and np.array_equal(gs.cpu().numpy(), s_a)
+        assert np.array_equal(gr.cpu().numpy(), rs)
+
+
+def test_workload_c4_sampled():
+    """7B-class sizes in the benchmark's launch configuration: codes, scales and row sums
+    bit-exact on every row; outputs on 48 sampled rows; accumulators on a window."""
+    _, specs = synth.workload("c4")
+    for spec in specs:
+        d = synth.make_linear(spec)
+        g = inputs_to_dev(d)
+        ws = B().workspace(B().prefill_workspace_bytes(spec.M, spec.N, spec.K), dev())
+        y = torch.full((spec.M, spec.N), float("nan"), device=dev())
+        B().prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"], y=y, ws=ws)
+        rows = np.unique(np.concatenate([np.linspace(0, spec.M - 1, 40).astype(np.int64),
+                                         [127, 128, 4095, 4096, 8063, 8064, 8190, 8191]]))
+        y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"], rows=rows)
+        check_y(y[torch.from_numpy(rows).to(dev())], y_ref, bound, f"c4/{spec.name}")
+        assert not torch.isnan(y).any(), "unwritten outputs"
+        a_q, s_a, rs = B().quant_pack(g["x"])
+        ra, rsa, rrs = oracle.quant_pack(d["x"])
+        assert np.array_equal(a_q.cpu().numpy(), ra)
+        assert np.array_equal(s_a.cpu().numpy(), rsa)
+        assert np.array_equal(rs.cpu().numpy(), rrs)
+        got = B().debug_block_acc(a_q, g["wq"], spec.N, 4000, 160, spec.N - 300, 300).cpu().numpy()
+        ref = oracle.block_acc(ra, d["wq"], spec.N, 4000, 160, spec.N - 300, 300)
+        assert np.array_equal(got, ref)
+        del g, y, ws
+        torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ edge cases
+def test_hand_cases_exact():
+    from golden_cases import linear_hand_cases
+    for c in linear_hand_cases():
+        g = inputs_to_dev(c)
+        y = B().prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"]).cpu().numpy()
+        assert np.array_equal(y.astype(np.float64), c["y"]), (c["name"], y, c["y"])
+
+
+def test_degenerate_inputs():
+    rng = np.random.default_rng(11)
+    M, N, K = 130, 70, 256
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x[0] = 0.0                      # zero row
+    x[1] = 0.0
+    x[1, 17] = -3.5                 # single spike
+    x[2] = 1.0                      # constant row: every code 127
+    x[3] = 1e-30                    # tiny values
+    x[4] = 3e30                     # huge values
+    c = 9
+    q = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    q[:5] = c                       # q == z exactly for the first 5 outputs
+    s_w = rng.uniform(0.005, 0.02, (N, K // 64)).astype(np.float16)
+    z_w = rng.uniform(6, 9, (N, K // 64)).astype(np.float16)
+    z_w[:5] = c
+    bias = rng.standard_normal(N).astype(np.float32)
+    d = dict(x=x, wq=synth.pack_u4(q), s_w=s_w, z_w=z_w, bias=bias)
+    y_fused, y_sep = _run_both(d)
+    y_ref, bound, _, _, _ = oracle.prefill_linear(x, d["wq"], s_w, z_w, bias)
+    check_y(y_fused, y_ref, bound, "degenerate")
+    y = y_fused.cpu().numpy()
+    assert np.array_equal(y[0], bias)                      # zero row -> bias
+    assert np.array_equal(y[:, :5], np.broadcast_to(bias[:5], (M, 5)))  # q == z -> bias exactly
+    assert torch.equal(y_fused, y_sep)
+
+
+def test_empty_and_invalid():
+    b = B()
+    x = torch.zeros((0, 128), device=dev())
+    a_q, s_a, rs = b.quant_pack(x)
+    assert a_q.shape == (0, 128)
+    wq = torch.zeros((16, 64), dtype=torch.uint8, device=dev())
+    sw = torch.ones((16, 2), dtype=torch.float16, device=dev())
+    y = b.prefill_linear(x, wq, sw, sw)
+    assert y.shape == (0, 16)
+    with pytest.raises(b.W4A8Error) as e:
+        b.quant_pack(torch.zeros((4, 96), device=dev()))
+    assert e.value.status == b.W4A8_ERR_SHAPE
+    flat = torch.zeros(4 * 128 + 1, device=dev())
+    with pytest.raises(b.W4A8Error) as e:
+        b.quant_pack(flat[1:].view(4, 128))                 # contiguous, base off by 4 bytes
+    assert e.value.status in (b.W4A8_ERR_ALIGN,)
+    assert b.sync_status() == 0
+
+
+def test_deterministic_and_fully_written():
+    d = synth.random_small(300, 1024, 700, seed=5, bias=True)
+    g = inputs_to_dev(d)
+    y1 = torch.full((300, 700), float("nan"), device=dev())
+    y2 = torch.full((300, 700), float("nan"), device=dev())
+    B().prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"], y=y1)
+    B().prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"], y=y2)
+    assert not torch.isnan(y1).any()
+    assert torch.equal(y1, y2)
+
+
+def test_bounded_wait_times_out_and_reports():
+    b = B()
+    assert b.sync_status() == 0
+    b.selftest_wait_timeout(20000)                          # 20 ms limit on a barrier nobody completes
+    assert b.sync_status() == b.W4A8_ERR_TIMEOUT
+    assert b.sync_status() == 0                             # status word cleared
+    d = synth.random_small(64, 128, 64, seed=2)             # the context is still usable
+    g = inputs_to_dev(d)
+    y = b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"])
+    y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
+    check_y(y, y_ref, bound, "after timeout")
+    assert b.sync_status() == 0
+
+
+def test_split_calls_equal_fused():
+    """prepare_activations + prepare_weights + linear_prepared == prefill_linear, bit for bit;
+    one prepared activation buffer serves several linears that read the same input."""
+    b = B()
+    M, K = 300, 2048
+    d0 = synth.random_small(M, K, 512, seed=21, bias=True)
+    x = to_dev(d0["x"])
+    act = b.prepare_activations(x)
+    for N, seed in ((512, 21), (130, 22), (1000, 23)):
+        d = synth.random_small(M, K, N, seed=seed, bias=True)
+        g = inputs_to_dev(d)
+        wsc = b.prepare_weights(g["s_w"], g["z_w"], K)
+        y_split = b.linear_prepared(act, g["wq"], wsc, M, K, bias=g["bias"])
+        y_fused = b.prefill_linear(x, g["wq"], g["s_w"], g["z_w"], g["bias"])
+        assert torch.equal(y_split, y_fused)
+        y_ref, bound, _, _, _ = oracle.prefill_linear(d0["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
+        check_y(y_split, y_ref, bound, f"split N={N}")
