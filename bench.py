@@ -42,6 +42,11 @@ def parse_args(argv=None):
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
+    p.add_argument("--shape", default=None,
+                   help="M,K,N: one linear of this shape instead of the workload (profiling aid)")
+    p.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
+    p.add_argument("--profile", action="store_true",
+                   help="only the warm-up and timed fused steps (for ncu captures); prints a short line")
     return p.parse_args(argv)
 
 
@@ -89,9 +94,10 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, enabled: bool = True):
         self.proc = None
         self.lines = []
+        self.enabled = enabled
         try:
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
             ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
@@ -101,6 +107,8 @@ class ClockSampler:
                     "-lms", "50", "-i", ident]
 
     def __enter__(self):
+        if not self.enabled:
+            return self
         try:
             self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
@@ -111,7 +119,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -122,10 +130,15 @@ class ClockSampler:
                 self.proc.kill()
             self.thread.join(timeout=2)
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen in [t0, t1] (wall clock); when the
+        window holds fewer than 3 samples, every sample taken after the sampler started."""
+        lines = [ln for t, ln in self.lines if (t0 is None or t >= t0) and (t1 is None or t <= t1)]
+        if len(lines) < 3:
+            lines = [ln for _, ln in self.lines]
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -154,9 +167,13 @@ def measured_peaks():
 
 
 # ------------------------------------------------------------------ workload
-def load_workload(key, device):
+def load_workload(key, device, shape=None):
     from w4a8_block_quantized_gb300 import binding, synth
-    title, specs = synth.workload(key)
+    if shape:
+        M, K, N = (int(v) for v in shape.split(","))
+        title, specs = f"custom M{M} K{K} N{N}", (synth.LinearSpec("custom", M, K, N),)
+    else:
+        title, specs = synth.workload(key)
     lin = []
     for spec in specs:
         d = synth.make_linear(spec)
@@ -176,7 +193,7 @@ def run_bench(args):
     device = torch.device("cuda", local)
     dist_init(world, "nccl")
     binding.load()
-    title, specs, lin = load_workload(args.workload, device)
+    title, specs, lin = load_workload(args.workload, device, args.shape)
     M = specs[0].M
     ops_per_step = sum(s.ops for s in specs)
     stream = torch.cuda.current_stream(device)
@@ -187,6 +204,9 @@ def run_bench(args):
             binding.prefill_linear(t["x"], t["wq"], t["s_w"], t["z_w"], t["bias"], y=t["y"], ws=t["ws"],
                                    stream=stream)
 
+    # The clock sampler starts before the warm-up so that nvidia-smi's own start-up (which
+    # can stall a fresh box for seconds) never falls inside the timed region.
+    clk = ClockSampler(local, enabled=not args.no_clocks).__enter__()
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
         step()
@@ -198,13 +218,15 @@ def run_bench(args):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     dist_barrier(world)
     torch.cuda.synchronize(device)
-    with ClockSampler(local) as clk:
-        for i in range(args.steps):
-            flush.zero_()
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize(device)
+    t_start = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    t_end = time.time()
+    clk.__exit__(None, None, None)
     dist_barrier(world)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_s = reduce_max(sum(step_ms) / 1e3, world, device)
@@ -213,6 +235,12 @@ def run_bench(args):
     ms_per_step = total_s * 1e3 / args.steps
     value_tops = whole_job_rate(ops_per_step * args.steps, world, total_s) / 1e12
     tok_s = whole_job_rate(M * args.steps, world, total_s)
+    if args.profile:
+        if rank == 0:
+            print(json.dumps({"profile": title, "ms_per_step": ms_per_step, "tops": value_tops,
+                              "status": binding.sync_status(stream),
+                              "step_ms": [round(v, 4) for v in step_ms[:20]]}), flush=True)
+        return
 
     # ---------------- kernel-level timing (same stream, CUDA events): the GEMM alone
     # through the split calls, and the pre-pass alone, each after an L2 flush.
@@ -278,7 +306,7 @@ def run_bench(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(lin, specs, args.cpu_seconds)
 
-    clocks = clk.summary()
+    clocks = clk.summary(t_start, t_end)
     out = {
         "metric": METRIC,
         "value": round(value_tops, 3),

@@ -9,6 +9,7 @@ from __future__ import annotations
 import concurrent.futures as cf
 import glob
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -44,6 +45,34 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
+# Kernels that re-split registers between warpgroups (setmaxnreg) need exactly this many
+# registers per thread at launch: the split in gemm.cu is sized against it, and a smaller
+# launch allocation would leave setmaxnreg.inc waiting for registers that never come.
+REGISTER_SPLIT_KERNELS = {"gemm_kernel": 96}
+
+
+def check_register_split(ptxas_log: str) -> None:
+    """Fail the build if a register-split kernel was not compiled with its launch count."""
+    current = None
+    seen = 0
+    for line in ptxas_log.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            current = m.group(1)
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and current:
+            for name, want in REGISTER_SPLIT_KERNELS.items():
+                if name in current:
+                    seen += 1
+                    if int(m.group(1)) != want:
+                        raise RuntimeError(f"{current}: ptxas used {m.group(1)} registers per thread, "
+                                           f"the warpgroup register split needs exactly {want}")
+            current = None
+    if seen == 0:
+        raise RuntimeError("register check: no register-split kernel found in the ptxas report")
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB
@@ -56,10 +85,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [cc, *common, "-c", src, "-o", obj]
+        split = os.path.basename(src) == "gemm.cu"
+        cmd = [cc, *common, *([] if ptxas_verbose or not split else ["-Xptxas", "-v"]), "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+        if split:
+            check_register_split(r.stdout + r.stderr)
         if verbose or ptxas_verbose:
             sys.stderr.write(r.stdout + r.stderr)
         return obj

@@ -108,14 +108,14 @@ CallLayout call_layout(int64_t M, int64_t N, int64_t K, bool with_sa) {
     return c;
 }
 
-// GEMM + epilogue from prepared activations (apk, rT at act offsets) and prepared scales.
-int run_linear(const uint8_t* act, const ActLayout& A, const float* s_a, const float4* sz, const uint8_t* wq,
+// GEMM + epilogue from prepared activations (apk, rx at act offsets) and prepared scales.
+int run_linear(const uint8_t* act, const ActLayout& A, const float* s_a, const float* wsc, const uint8_t* wq,
                const float* bias, float* y, int64_t M, int64_t N, int64_t K, const DeviceInfo& d, cudaStream_t st) {
     GemmMaps maps;
-    if (!make_map_u8(&maps.a, act + A.apk, 2 * K, M, 2 * K, 128, kTileM, CU_TENSOR_MAP_SWIZZLE_128B))
+    const int tn = pick_token_tile(M, N, d.num_sms);
+    if (!make_map_u8(&maps.a, act + A.apk, 2 * K, M, 2 * K, 128, tn, CU_TENSOR_MAP_SWIZZLE_128B))
         return W4A8_ERR_CUDA;
-    const int bn = pick_block_n(M, N, d.num_sms);
-    if (!make_map_u8(&maps.b, wq, K / 2, N, K / 2, 32, bn, CU_TENSOR_MAP_SWIZZLE_NONE)) return W4A8_ERR_CUDA;
+    if (!make_map_u8(&maps.b, wq, K / 2, N, K / 2, 32, kTileW, CU_TENSOR_MAP_SWIZZLE_NONE)) return W4A8_ERR_CUDA;
     GemmArgs g;
     g.M = M;
     g.N = N;
@@ -125,13 +125,13 @@ int run_linear(const uint8_t* act, const ActLayout& A, const float* s_a, const f
     g.n_cnt = N;
     g.M_pad = A.M_pad;
     g.N_pad = n_pad(N);
-    g.sz = sz;
-    g.rT = reinterpret_cast<const float*>(act + A.rT);
+    g.wsc = wsc;
+    g.rx = reinterpret_cast<const uint4*>(act + A.rx);
     g.s_a = s_a;
     g.bias = bias;
     g.y = y;
     g.status = d.status;
-    return launch_gemm(maps, g, bn, false, d.num_sms, st) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
+    return launch_gemm(maps, g, tn, false, st) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
 }
 
 }  // namespace
@@ -228,15 +228,15 @@ int w4a8_linear(const int8_t* a_q, const float* a_scale, const int32_t* rowsum, 
     p.M = M;
     p.K = K;
     p.apk = ws + L.act.apk;
-    p.rT = reinterpret_cast<float*>(ws + L.act.rT);
+    p.rx = reinterpret_cast<uint4*>(ws + L.act.rx);
     p.M_pad = L.act.M_pad;
     p.s_w = w_scale;
     p.z_w = w_zero;
     p.N = N;
     p.N_pad = n_pad(N);
-    p.sz = reinterpret_cast<float4*>(ws + L.wsc);
+    p.wsc = reinterpret_cast<float*>(ws + L.wsc);
     if (launch_pack(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
-    return run_linear(ws, L.act, a_scale, reinterpret_cast<const float4*>(ws + L.wsc), wq, bias, y, M, N, K, *d, st);
+    return run_linear(ws, L.act, a_scale, reinterpret_cast<const float*>(ws + L.wsc), wq, bias, y, M, N, K, *d, st);
 }
 
 int w4a8_prefill_linear(const float* x, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero,
@@ -263,15 +263,15 @@ int w4a8_prefill_linear(const float* x, const uint8_t* wq, const uint16_t* w_sca
     p.K = K;
     p.s_a_out = s_a;
     p.apk = ws + L.act.apk;
-    p.rT = reinterpret_cast<float*>(ws + L.act.rT);
+    p.rx = reinterpret_cast<uint4*>(ws + L.act.rx);
     p.M_pad = L.act.M_pad;
     p.s_w = w_scale;
     p.z_w = w_zero;
     p.N = N;
     p.N_pad = n_pad(N);
-    p.sz = reinterpret_cast<float4*>(ws + L.wsc);
+    p.wsc = reinterpret_cast<float*>(ws + L.wsc);
     if (launch_quant(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
-    return run_linear(ws, L.act, s_a, reinterpret_cast<const float4*>(ws + L.wsc), wq, bias, y, M, N, K, *d, st);
+    return run_linear(ws, L.act, s_a, reinterpret_cast<const float*>(ws + L.wsc), wq, bias, y, M, N, K, *d, st);
 }
 
 int w4a8_prepare_activations(const float* x, int64_t M, int64_t K, void* act, size_t act_bytes, void* stream) {
@@ -291,7 +291,7 @@ int w4a8_prepare_activations(const float* x, int64_t M, int64_t K, void* act, si
     p.K = K;
     p.s_a_out = reinterpret_cast<float*>(a + A.s_a);
     p.apk = a + A.apk;
-    p.rT = reinterpret_cast<float*>(a + A.rT);
+    p.rx = reinterpret_cast<uint4*>(a + A.rx);
     p.M_pad = A.M_pad;
     return launch_quant(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
 }
@@ -313,7 +313,7 @@ int w4a8_prepare_weights(const uint16_t* w_scale, const uint16_t* w_zero, int64_
     p.z_w = w_zero;
     p.N = N;
     p.N_pad = n_pad(N);
-    p.sz = static_cast<float4*>(wsc);
+    p.wsc = static_cast<float*>(wsc);
     return launch_pack(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
 }
 
@@ -329,7 +329,7 @@ int w4a8_linear_prepared(const void* act, const uint8_t* wq, const void* wsc, co
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
     const ActLayout A = act_layout(M, K, true, true);
     const uint8_t* a = static_cast<const uint8_t*>(act);
-    return run_linear(a, A, reinterpret_cast<const float*>(a + A.s_a), static_cast<const float4*>(wsc), wq, bias, y,
+    return run_linear(a, A, reinterpret_cast<const float*>(a + A.s_a), static_cast<const float*>(wsc), wq, bias, y,
                       M, N, K, *d, static_cast<cudaStream_t>(stream));
 }
 
@@ -356,10 +356,10 @@ int w4a8_debug_block_acc(const int8_t* a_q, const uint8_t* wq, int64_t M, int64_
     p.apk = ws + L.apk;
     if (launch_pack(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
     GemmMaps maps;
-    if (!make_map_u8(&maps.a, ws + L.apk, 2 * K, m_cnt, 2 * K, 128, kTileM, CU_TENSOR_MAP_SWIZZLE_128B))
+    const int tn = pick_token_tile(m_cnt, n_cnt, d->num_sms);
+    if (!make_map_u8(&maps.a, ws + L.apk, 2 * K, m_cnt, 2 * K, 128, tn, CU_TENSOR_MAP_SWIZZLE_128B))
         return W4A8_ERR_CUDA;
-    const int bn = pick_block_n(m_cnt, n_cnt, d->num_sms);
-    if (!make_map_u8(&maps.b, wq, K / 2, N, K / 2, 32, bn, CU_TENSOR_MAP_SWIZZLE_NONE)) return W4A8_ERR_CUDA;
+    if (!make_map_u8(&maps.b, wq, K / 2, N, K / 2, 32, kTileW, CU_TENSOR_MAP_SWIZZLE_NONE)) return W4A8_ERR_CUDA;
     GemmArgs g;
     g.M = m_cnt;
     g.N = N;
@@ -369,7 +369,7 @@ int w4a8_debug_block_acc(const int8_t* a_q, const uint8_t* wq, int64_t M, int64_
     g.n_cnt = n_cnt;
     g.acc = acc;
     g.status = d->status;
-    return launch_gemm(maps, g, bn, true, d->num_sms, st) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
+    return launch_gemm(maps, g, tn, true, st) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
 }
 
 int w4a8_sync_status(void* stream) {

@@ -3,25 +3,34 @@
 // "MNN LLM inference on the SpacemiT K3", section 3 eqs. (2)-(3) and section 4 steps 2-3.
 // There is no integer MMA kind on sm_103a, so the exact INT8 x U4 block products are
 // carried on the fp8 kind (tcgen05.mma kind::f8f6f4, E4M3 x E4M3 -> fp32 in TMEM):
+//   - a u4 weight code q, zero-extended to a byte, is exactly the e4m3 encoding of
+//     q * 2^-9 (the subnormal binade and the first normal binade share the step 2^-9), so
+//     the in-shared-memory unpack is two masks and two byte permutes per 8 weights;
 //   - activations arrive as the two nibble planes of eq. (3): e4m3(16*(a>>4)) and
 //     e4m3(a&15), both exact;
-//   - a u4 weight code q, zero-extended to a byte, is exactly the e4m3 encoding of
-//     q * 2^-9 (subnormal + first normal binade share the step 2^-9), so the in-shared-
-//     memory unpack is two masks and two byte permutes per 8 weights;
-//   - one block = 4 MMAs of K = 32 (hi plane x q, then lo plane x q) into one TMEM
-//     accumulator, which then holds acc * 2^-9 with |acc| <= 127*15*64 < 2^17: exact
-//     in fp32 provided the tensor core does not drop low-order bits (checked bit-exactly
-//     against the oracle by the debug call);
-//   - every 64-block gets its own accumulator (two TMEM buffers, ping-pong), drained by
-//     the epilogue warps: t = fma(-z/512, rs, acc') (one rounding of acc - z*rs),
-//     y += (512 s) * t, then y_out = fma(s_a, y, bias) written straight to HBM.
+//   - one 64-block = 4 MMAs of K = 32 (q x hi plane, then q x lo plane) into one TMEM
+//     accumulator, which then holds acc * 2^-9 with |acc| <= 128*15*64 < 2^17, exact in
+//     fp32 (checked bit for bit against the oracle through the debug call);
+//   - the zero-point term of eq. (2) is a fifth MMA on the same accumulator (kind::f16,
+//     K = 16, two live K slots): weights {-z_w, -z_w}, tokens {rh/8, rl/512} with the row
+//     sum rs = 64 rh + rl, all exact in fp16, so the accumulator ends the block holding
+//     (acc - z_w rs) * 2^-9;
+//   - every 64-block gets its own accumulator (ping-pong TMEM buffers), drained by the
+//     epilogue warps with one fma per output, y += (512 s_w) * D, and at the end
+//     y_out = fma(s_a, y, bias) is written straight to HBM.
 //
-// Warp roles (one CTA = one 128 x BN output tile, 12 warps):
-//   warp 0      TMA producer: activation planes (128-byte swizzle), packed weights, and
-//               (bulk copies) the block's scales and row sums
-//   warp 1      TMEM allocation + single-thread MMA issue
-//   warps 2-3   weight unpack u4 -> e4m3 into the 64-byte-swizzled K-major operand
-//   warps 4-11  epilogue (two warps per 32-lane TMEM quarter, half of the columns each)
+// Orientation: the weights are the MMA's M = 128 operand (TMEM lanes = output columns n)
+// and the tokens its N operand (TN = 64..256 TMEM columns).  An epilogue thread then owns
+// four weight rows, so s_w is a per-thread scalar for a block and the epilogue reads no
+// per-column data at all.
+//
+// Warp roles (one CTA = one 128-weight x TN-token output tile, 20 warps):
+//   warp 0       TMA producer: token planes (128-byte swizzle), packed weights; bulk
+//                copies of the block's row-sum operand, weight zeros and weight scales
+//   warp 1       TMEM allocation + single-thread MMA issue
+//   warps 2-3    weight unpack u4 -> e4m3 into the 64-byte-swizzled K-major operand, and
+//                the weight zeros into the zero-point operand
+//   warps 4-19   epilogue: 4 warps per 32-lane TMEM quarter, a quarter of the columns each
 // Every wait is bounded (WaitCtl); a CTA that gives up records a timeout and unwinds.
 #include "sm103_ptx.cuh"
 #include "w4a8_internal.h"
@@ -29,31 +38,45 @@
 namespace w4a8 {
 namespace {
 
-template <int BN>
+constexpr int kThreads = 640;
+constexpr int kEpiWarps = 16;
+constexpr uint32_t kLayoutSw128 = 2, kLayoutSw64 = 4;
+// Register split: launch = 640 x 96 (checked at build time); warps 0-3 drop to 48,
+// the 16 epilogue warps rise to 104: 128*48 + 512*104 = 59392 <= 61440.
+constexpr int kRegsLow = 48, kRegsHigh = 104;
+
+template <int TN>
 struct Cfg {
-    static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
-    static constexpr int kSc = kStages + 4;  // scale/row-sum ring (outlives the MMA stage)
-    static constexpr int kABytes = kTileM * 128;
-    static constexpr int kBunpBytes = BN * 64;
-    static constexpr int kBpkBytes = BN * 32;
-    static constexpr int kSzBytes = BN * 8;
-    static constexpr int kRBytes = kTileM * 4;
-    static constexpr int kOffA = 0;
-    static constexpr int kOffBunp = kOffA + kStages * kABytes;
-    static constexpr int kOffBpk = kOffBunp + kStages * kBunpBytes;
-    static constexpr int kOffSz = kOffBpk + kStages * kBpkBytes;
-    static constexpr int kOffR = kOffSz + kSc * kSzBytes;
-    static constexpr int kOffBar = kOffR + kSc * kRBytes;
-    static constexpr int kNumBars = 3 * kStages + 2 * kSc + 5;
+    static constexpr int kStages = TN == 256 ? 4 : (TN == 128 ? 6 : 8);
+    static constexpr int kSc = kStages + 4;          // weight-scale ring (read by the epilogue)
+    static constexpr int kNBuf = TN == 256 ? 2 : 4;  // TMEM accumulator buffers
+    static constexpr int kTBytes = TN * 128;         // token planes of one block
+    static constexpr int kWunpBytes = kTileW * 64;   // unpacked weights of one block
+    static constexpr int kWpkBytes = kTileW * 32;    // packed weights of one block
+    static constexpr int kAxBytes = kTileW * 16;     // zero-point operand, weight side (K 0..7)
+    static constexpr int kBxBytes = TN * 16;         // zero-point operand, token side (K 0..7)
+    static constexpr int kZhBytes = kTileW * 4;      // {-z_w, -z_w} staging for the unpack warps
+    static constexpr int kZeroBytes = 4096;          // K 8..15 of both zero-point operands
+    static constexpr int kSBytes = kTileW * 4;       // 512 s_w of the tile's rows
+    static constexpr int kOffT = 0;
+    static constexpr int kOffWunp = kOffT + kStages * kTBytes;
+    static constexpr int kOffWpk = kOffWunp + kStages * kWunpBytes;
+    static constexpr int kOffAx = kOffWpk + kStages * kWpkBytes;
+    static constexpr int kOffBx = kOffAx + kStages * kAxBytes;
+    static constexpr int kOffZh = kOffBx + kStages * kBxBytes;
+    static constexpr int kOffZero = kOffZh + kStages * kZhBytes;
+    static constexpr int kOffSc = kOffZero + kZeroBytes;
+    static constexpr int kOffBar = kOffSc + kSc * kSBytes;
+    static constexpr int kNumBars = 3 * kStages + 2 * kSc + 2 * kNBuf + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-    static constexpr uint32_t kTmemCols = 2 * BN;
-    static_assert(kOffBunp % 1024 == 0 && kOffBpk % 1024 == 0, "operand tiles must be 1024-aligned");
+    static constexpr uint32_t kTmemCols = kNBuf * TN;
+    static constexpr int kChunks = TN / 64;          // 16-column chunks per epilogue thread
+    static_assert(kOffWunp % 1024 == 0 && kOffWpk % 1024 == 0, "operand tiles must be 1024-aligned");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation");
+    static_assert(kZeroBytes >= kAxBytes && kZeroBytes >= kBxBytes, "zero half of the zero-point operands");
 };
-
-constexpr int kThreads = 384;
-constexpr uint32_t kLayoutSw128 = 2, kLayoutSw64 = 4;
 
 // u4 pairs -> e4m3 bytes in k order: nibbles k0..k7 of w become bytes of (o0: k0..k3, o1: k4..k7).
 __device__ __forceinline__ void expand8(uint32_t w, uint32_t& o0, uint32_t& o1) {
@@ -73,11 +96,21 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
     }
 }
 
-template <int BN, bool DEBUG>
+// 16 TMEM lanes x (2 x 8) fp32 columns: thread t receives, for repeat j = 0..1,
+// r[4j+0..1] = lane (t/4), columns 8j + 2(t%4) + {0,1}; r[4j+2..3] = lane (t/4)+8.
+__device__ __forceinline__ void tmem_ld_16x256b_x2(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+}
+
+template <int TN, bool DEBUG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
-    using C = Cfg<BN>;
-    constexpr int S = C::kStages, SC = C::kSc;
+    using C = Cfg<TN>;
+    constexpr int S = C::kStages, SC = C::kSc, NB = C::kNBuf;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -86,16 +119,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* scfull = unp + S;
     uint64_t* scempty = scfull + SC;
     uint64_t* tfull = scempty + SC;
-    uint64_t* tempty = tfull + 2;
-    uint64_t* drain = tempty + 2;
+    uint64_t* tempty = tfull + NB;
+    uint64_t* drain = tempty + NB;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t tiles_n = (args.n_cnt + BN - 1) / BN;
-    const int64_t tm = blockIdx.x / tiles_n, tn = blockIdx.x - tm * tiles_n;
-    const int64_t mt0 = tm * kTileM;            // first operand row of the tile
-    const int64_t nt0 = args.n0 + tn * BN;      // first weight row (output column) of the tile
+    const int64_t tiles_w = (args.n_cnt + kTileW - 1) / kTileW;
+    const int64_t tt = blockIdx.x / tiles_w, tw = blockIdx.x - tt * tiles_w;
+    const int64_t mt0 = tt * TN;                  // first token (operand row) of the tile
+    const int64_t nt0 = args.n0 + tw * kTileW;    // first weight row (output column) of the tile
     const int nb = static_cast<int>(args.K / kBlock);
     const WaitCtl ctl{abort_flag, args.status, args.wait_limit_ns};
 
@@ -107,17 +140,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int c = 0; c < SC; ++c) {
             mbar_init(&scfull[c], 1);
-            mbar_init(&scempty[c], 8);
+            mbar_init(&scempty[c], kEpiWarps);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NB; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 8);
+            mbar_init(&tempty[i], kEpiWarps);
         }
         mbar_init(drain, 1);
         *abort_flag = 0u;
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+    }
+    if (!DEBUG) {
+        // the zero-point operands: weight-side tiles (only their first 4 bytes per row are
+        // rewritten per block) and the shared zero K-half
+        for (int i = threadIdx.x; i < (C::kStages * C::kAxBytes) / 16; i += kThreads)
+            reinterpret_cast<uint4*>(smem + C::kOffAx)[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = threadIdx.x; i < C::kZeroBytes / 16; i += kThreads)
+            reinterpret_cast<uint4*>(smem + C::kOffZero)[i] = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::kTmemCols);
@@ -128,148 +170,174 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    // BN = 256 needs 128 accumulator registers per epilogue thread: move registers from
-    // the producer/MMA/unpack warpgroup (warps 0-3) to the two epilogue warpgroups.
-    // 128 x 64 + 256 x 208 = 61440 <= 384 x 168 registers at launch.
     if (warp < 4) {
-    if (BN == 256) regs_dec<64>();
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int nA = 0, nS = 0;  // blocks whose operand / scale copies were issued
-            for (int b = 0; b < nb; ++b) {
-                const int s = b % S, k = b / S;
-                if (k > 0 && !mbar_wait(&empty[s], (k - 1) & 1, ctl)) break;
-                mbar_arrive_expect_tx(&full[s], C::kABytes + C::kBpkBytes);
-                tma_load_2d(smem + C::kOffA + s * C::kABytes, &tmA, &full[s], b * 128, static_cast<int32_t>(mt0));
-                tma_load_2d(smem + C::kOffBpk + s * C::kBpkBytes, &tmB, &full[s], b * 32,
-                            static_cast<int32_t>(nt0));
-                nA = b + 1;
-                if (!DEBUG) {
-                    const int c = b % SC, kc = b / SC;
-                    if (kc > 0 && !mbar_wait(&scempty[c], (kc - 1) & 1, ctl)) break;
-                    mbar_arrive_expect_tx(&scfull[c], C::kSzBytes + C::kRBytes);
-                    bulk_load(smem + C::kOffSz + c * C::kSzBytes,
-                              args.sz + (static_cast<int64_t>(b) * args.N_pad + nt0) / 2, C::kSzBytes, &scfull[c]);
-                    bulk_load(smem + C::kOffR + c * C::kRBytes, args.rT + static_cast<int64_t>(b) * args.M_pad + mt0,
-                              C::kRBytes, &scfull[c]);
-                    nS = b + 1;
+        regs_dec<kRegsLow>();
+        if (warp == 0) {
+            // -------------------------------------------------------- TMA producer
+            if (lane == 0) {
+                int nA = 0, nS = 0;  // blocks whose operand / scale copies were issued
+                for (int b = 0; b < nb; ++b) {
+                    const int s = b % S, k = b / S;
+                    if (k > 0 && !mbar_wait(&empty[s], (k - 1) & 1, ctl)) break;
+                    const float* wrow = args.wsc + static_cast<int64_t>(b) * 2 * args.N_pad;
+                    mbar_arrive_expect_tx(&full[s], C::kTBytes + C::kWpkBytes +
+                                                        (DEBUG ? 0 : C::kBxBytes + C::kZhBytes));
+                    tma_load_2d(smem + C::kOffT + s * C::kTBytes, &tmA, &full[s], b * 128, static_cast<int32_t>(mt0));
+                    tma_load_2d(smem + C::kOffWpk + s * C::kWpkBytes, &tmB, &full[s], b * 32,
+                                static_cast<int32_t>(nt0));
+                    if (!DEBUG) {
+                        bulk_load(smem + C::kOffBx + s * C::kBxBytes, args.rx + static_cast<int64_t>(b) * args.M_pad + mt0,
+                                  C::kBxBytes, &full[s]);
+                        bulk_load(smem + C::kOffZh + s * C::kZhBytes,
+                                  reinterpret_cast<const uint32_t*>(wrow + args.N_pad) + nt0, C::kZhBytes, &full[s]);
+                    }
+                    nA = b + 1;
+                    if (!DEBUG) {
+                        const int c = b % SC, kc = b / SC;
+                        if (kc > 0 && !mbar_wait(&scempty[c], (kc - 1) & 1, ctl)) break;
+                        mbar_arrive_expect_tx(&scfull[c], C::kSBytes);
+                        bulk_load(smem + C::kOffSc + c * C::kSBytes, wrow + nt0, C::kSBytes, &scfull[c]);
+                        nS = b + 1;
+                    }
+                }
+                if (*abort_flag) {
+                    // let every copy already issued land before the CTA exits
+                    for (int j = (nA > S ? nA - S : 0); j < nA; ++j) drain_wait(&full[j % S], (j / S) & 1, 100000000ull);
+                    for (int j = (nS > SC ? nS - SC : 0); j < nS; ++j)
+                        drain_wait(&scfull[j % SC], (j / SC) & 1, 100000000ull);
                 }
             }
-            if (*abort_flag) {
-                // let every copy already issued land before the CTA exits
-                for (int j = (nA > S ? nA - S : 0); j < nA; ++j) drain_wait(&full[j % S], (j / S) & 1, 100000000ull);
-                for (int j = (nS > SC ? nS - SC : 0); j < nS; ++j)
-                    drain_wait(&scfull[j % SC], (j / SC) & 1, 100000000ull);
+        } else if (warp == 1) {
+            // -------------------------------------------------------- MMA issuer
+            // The wait for block b+1's operands is taken while block b's last MMAs are
+            // still queued on the tensor pipe, so the barrier latency does not leave the
+            // pipe idle between blocks.  (The wait for a drained TMEM buffer stays at the
+            // start of each block: taken early it would tie block b's MMAs to the drain of
+            // block b-1.)  The unpack warps arrive on unp[s] only after they observed
+            // full[s], so unp[s] also covers the TMA data of the stage.
+            if (lane == 0) {
+                constexpr uint32_t idesc = idesc_e4m3_f32(kTileW, TN);
+                // Descriptors of stage 0; stage s adds s * (tile bytes >> 4) to the start-address
+                // field, and a K offset of 32 bytes adds 2.  The field never overflows: every
+                // shared-memory address is below 2^18.
+                const uint32_t zr = smem_u32(smem + C::kOffZero);
+                const uint32_t ax0 = smem_u32(smem + C::kOffAx), bx0 = smem_u32(smem + C::kOffBx);
+                const uint64_t dW0 = smem_desc(smem_u32(smem + C::kOffWunp), 512, kLayoutSw64);
+                const uint64_t dT0 = smem_desc(smem_u32(smem + C::kOffT), 1024, kLayoutSw128);
+                const uint64_t dAx0 = smem_desc(ax0, 128, 0, zr - ax0);
+                const uint64_t dBx0 = smem_desc(bx0, 128, 0, zr - bx0);
+                auto ready = [&](int b) -> bool { return mbar_wait(&unp[b % S], (b / S) & 1, ctl); };
+                bool ok = nb > 0 && ready(0);
+                for (int b = 0; ok && b < nb; ++b) {
+                    const int s = b % S, buf = b % NB, u = b / NB;
+                    if (u > 0 && !mbar_wait(&tempty[buf], (u - 1) & 1, ctl)) break;
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(buf * TN);
+                    const uint64_t dW = dW0 + static_cast<uint64_t>(s * (C::kWunpBytes >> 4));
+                    const uint64_t dT = dT0 + static_cast<uint64_t>(s * (C::kTBytes >> 4));
+                    // q x hi plane (K 0..31, 32..63), then q x lo plane
+                    mma_f8f6f4(d, dW, dT, idesc, 0u);
+                    mma_f8f6f4(d, dW + 2, dT + 2, idesc, 1u);
+                    mma_f8f6f4(d, dW, dT + 4, idesc, 1u);
+                    if (b + 1 < nb) ok = ready(b + 1);
+                    mma_f8f6f4(d, dW + 2, dT + 6, idesc, 1u);
+                    if (!DEBUG) {
+                        // zero-point term: {-z, -z} x {rh/8, rl/512}; K 8..15 from the zero block
+                        // (each stage's leading byte offset shrinks as its start address grows)
+                        const uint64_t ax = static_cast<uint64_t>(s * (C::kAxBytes >> 4));
+                        const uint64_t bx = static_cast<uint64_t>(s * (C::kBxBytes >> 4));
+                        mma_f16(d, dAx0 + ax - (ax << 16), dBx0 + bx - (bx << 16), idesc, 1u);
+                    }
+                    mma_commit(&empty[s]);
+                    mma_commit(&tfull[buf]);
+                }
+                mma_commit(drain);
+                drain_wait(drain, 0, 100000000ull);
             }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_e4m3_f32(kTileM, BN);
+        } else {
+            // -------------------------------------------------------- weight unpack
+            const int ut = threadIdx.x - 64;
             for (int b = 0; b < nb; ++b) {
                 const int s = b % S, k = b / S;
-                if (!mbar_wait(&unp[s], k & 1, ctl)) break;
                 if (!mbar_wait(&full[s], k & 1, ctl)) break;
-                const int buf = b & 1, u = b >> 1;
-                if (u > 0 && !mbar_wait(&tempty[buf], (u - 1) & 1, ctl)) break;
-                tc_fence_after();
-                const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
-                const uint32_t a0 = smem_u32(smem + C::kOffA + s * C::kABytes);
-                const uint32_t b0 = smem_u32(smem + C::kOffBunp + s * C::kBunpBytes);
-                // hi plane x q (K 0..31, 32..63), then lo plane x q
-                mma_f8f6f4(d, smem_desc(a0 + 0, 1024, kLayoutSw128), smem_desc(b0 + 0, 512, kLayoutSw64), idesc, 0u);
-                mma_f8f6f4(d, smem_desc(a0 + 32, 1024, kLayoutSw128), smem_desc(b0 + 32, 512, kLayoutSw64), idesc, 1u);
-                mma_f8f6f4(d, smem_desc(a0 + 64, 1024, kLayoutSw128), smem_desc(b0 + 0, 512, kLayoutSw64), idesc, 1u);
-                mma_f8f6f4(d, smem_desc(a0 + 96, 1024, kLayoutSw128), smem_desc(b0 + 32, 512, kLayoutSw64), idesc, 1u);
-                mma_commit(&empty[s]);
-                mma_commit(&tfull[buf]);
+                const uint8_t* src = smem + C::kOffWpk + s * C::kWpkBytes;
+                uint8_t* dst = smem + C::kOffWunp + s * C::kWunpBytes;
+#pragma unroll
+                for (int j = 0; j < (kTileW * 2) / 64; ++j) {
+                    const int c = ut + 64 * j;  // 16-byte chunk of the packed tile
+                    const int row = c >> 1, half = c & 1;
+                    const uint4 w = *reinterpret_cast<const uint4*>(src + c * 16);
+                    uint4 o0, o1;
+                    expand8(w.x, o0.x, o0.y);
+                    expand8(w.y, o0.z, o0.w);
+                    expand8(w.z, o1.x, o1.y);
+                    expand8(w.w, o1.z, o1.w);
+                    const int sw = (row >> 1) & 3;  // 64-byte swizzle: chunk ^= address bits 7..8
+                    *reinterpret_cast<uint4*>(dst + row * 64 + (((2 * half) ^ sw) << 4)) = o0;
+                    *reinterpret_cast<uint4*>(dst + row * 64 + (((2 * half + 1) ^ sw) << 4)) = o1;
+                }
+                if (!DEBUG) {
+                    // {-z, -z} into K 0..1 of the weight-side zero-point operand (core matrix
+                    // rows of 16 bytes, 8-row groups 128 bytes apart)
+                    const uint32_t* zh = reinterpret_cast<const uint32_t*>(smem + C::kOffZh + s * C::kZhBytes);
+                    uint8_t* ax = smem + C::kOffAx + s * C::kAxBytes;
+#pragma unroll
+                    for (int r = ut; r < kTileW; r += 64) *reinterpret_cast<uint32_t*>(ax + r * 16) = zh[r];
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&unp[s]);
             }
-            mma_commit(drain);
-            drain_wait(drain, 0, 100000000ull);
         }
-    } else if (warp < 4) {
-        // ------------------------------------------------------------ weight unpack
-        const int ut = threadIdx.x - 64;
-        for (int b = 0; b < nb; ++b) {
-            const int s = b % S, k = b / S;
-            if (!mbar_wait(&full[s], k & 1, ctl)) break;
-            const uint8_t* src = smem + C::kOffBpk + s * C::kBpkBytes;
-            uint8_t* dst = smem + C::kOffBunp + s * C::kBunpBytes;
-#pragma unroll 4
-            for (int c = ut; c < BN * 2; c += 64) {
-                const int row = c >> 1, half = c & 1;
-                const uint4 w = *reinterpret_cast<const uint4*>(src + c * 16);
-                uint4 o0, o1;
-                expand8(w.x, o0.x, o0.y);
-                expand8(w.y, o0.z, o0.w);
-                expand8(w.z, o1.x, o1.y);
-                expand8(w.w, o1.z, o1.w);
-                const int sw = (row >> 1) & 3;  // 64-byte swizzle: chunk ^= address bits 7..8
-                *reinterpret_cast<uint4*>(dst + row * 64 + (((2 * half) ^ sw) << 4)) = o0;
-                *reinterpret_cast<uint4*>(dst + row * 64 + (((2 * half + 1) ^ sw) << 4)) = o1;
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&unp[s]);
-        }
-    }
     } else {
         // ------------------------------------------------------------ epilogue
-        if (BN == 256) regs_inc<208>();
-        constexpr int G = BN / 16;  // 8-column groups per thread
-        const int q = warp & 3, h = (warp - 4) >> 2;
+        regs_inc<kRegsHigh>();
+        constexpr int CH = C::kChunks;
+        const int q = warp & 3, h = (warp - 4) >> 2;  // TMEM lane quarter, column quarter
         const int r8 = lane >> 2, cp = lane & 3;
-        float2 yv[4][G];
+        float2 yv[4][CH][2];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int g = 0; g < G; ++g) yv[i][g] = make_float2(0.f, 0.f);
-        const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * (BN / 2));
+            for (int ch = 0; ch < CH; ++ch) yv[i][ch][0] = yv[i][ch][1] = make_float2(0.f, 0.f);
+        const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         for (int b = 0; b < nb; ++b) {
-            const int buf = b & 1, u = b >> 1;
+            const int buf = b % NB, u = b / NB;
             const int c = b % SC, kc = b / SC;
             if (!mbar_wait(&tfull[buf], u & 1, ctl)) break;
             if (!DEBUG && !mbar_wait(&scfull[c], kc & 1, ctl)) break;
             tc_fence_after();
-            float4 R4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float* szb = reinterpret_cast<const float*>(smem + C::kOffSz + c * C::kSzBytes);
-            if (!DEBUG) R4 = *reinterpret_cast<const float4*>(smem + C::kOffR + c * C::kRBytes + (q * 32 + r8 * 4) * 4);
-            const float Rr[4] = {R4.x, R4.y, R4.z, R4.w};
+            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (!DEBUG) s4 = *reinterpret_cast<const float4*>(smem + C::kOffSc + c * C::kSBytes + (q * 32 + r8 * 4) * 4);
+            const float sr[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-            for (int ch = 0; ch < G / 4; ++ch) {
-                uint32_t v0[16], v1[16];
-                const uint32_t ta = lane_addr + static_cast<uint32_t>(buf * BN + ch * 32);
-                tmem_ld_16x256b_x4(ta, v0);
-                tmem_ld_16x256b_x4(ta + (16u << 16), v1);
+            for (int ch = 0; ch < CH; ++ch) {
+                const int col0 = h * (TN / 4) + ch * 16;  // token column within the tile
+                uint32_t v0[8], v1[8];
+                const uint32_t ta = lane_addr + static_cast<uint32_t>(buf * TN + col0);
+                tmem_ld_16x256b_x2(ta, v0);                 // weight rows r8, r8 + 8 of the quarter
+                tmem_ld_16x256b_x2(ta + (16u << 16), v1);   // weight rows r8 + 16, r8 + 24
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int g = ch * 4 + j;
-                    const int col = h * (BN / 2) + g * 8 + 2 * cp;  // column within the tile
-                    float2 a2[4];
-                    a2[0] = make_float2(__uint_as_float(v0[4 * j + 0]), __uint_as_float(v0[4 * j + 1]));
-                    a2[1] = make_float2(__uint_as_float(v0[4 * j + 2]), __uint_as_float(v0[4 * j + 3]));
-                    a2[2] = make_float2(__uint_as_float(v1[4 * j + 0]), __uint_as_float(v1[4 * j + 1]));
-                    a2[3] = make_float2(__uint_as_float(v1[4 * j + 2]), __uint_as_float(v1[4 * j + 3]));
+                for (int g = 0; g < 2; ++g) {
+                    const float2 a2[4] = {
+                        make_float2(__uint_as_float(v0[4 * g + 0]), __uint_as_float(v0[4 * g + 1])),
+                        make_float2(__uint_as_float(v0[4 * g + 2]), __uint_as_float(v0[4 * g + 3])),
+                        make_float2(__uint_as_float(v1[4 * g + 0]), __uint_as_float(v1[4 * g + 1])),
+                        make_float2(__uint_as_float(v1[4 * g + 2]), __uint_as_float(v1[4 * g + 3]))};
                     if (DEBUG) {
-                        const int64_t n = nt0 + col;
+                        const int64_t m = mt0 + col0 + 8 * g + 2 * cp;  // token (window row)
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const int64_t m = mt0 + q * 32 + r8 + 8 * i;
-                            if (m < args.m_cnt) {
+                            const int64_t n = nt0 + q * 32 + r8 + 8 * i;  // weight row
+                            if (n < args.n0 + args.n_cnt) {
                                 int32_t* dst = args.acc + (m * args.n_cnt + (n - args.n0)) * nb + b;
-                                if (n < args.n0 + args.n_cnt) dst[0] = static_cast<int32_t>(a2[i].x * 512.0f);
-                                if (n + 1 < args.n0 + args.n_cnt) dst[nb] = static_cast<int32_t>(a2[i].y * 512.0f);
+                                if (m < args.m_cnt) dst[0] = static_cast<int32_t>(a2[i].x * 512.0f);
+                                if (m + 1 < args.m_cnt) dst[args.n_cnt * nb] = static_cast<int32_t>(a2[i].y * 512.0f);
                             }
                         }
                     } else {
-                        const float4 S4 = *reinterpret_cast<const float4*>(szb + col * 2);
-                        const float2 sc = make_float2(S4.x, S4.y), mz = make_float2(S4.z, S4.w);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float2 t2 = __ffma2_rn(mz, make_float2(Rr[i], Rr[i]), a2[i]);
-                            yv[i][g] = __ffma2_rn(sc, t2, yv[i][g]);
-                        }
+                        for (int i = 0; i < 4; ++i) yv[i][ch][g] = __ffma2_rn(make_float2(sr[i], sr[i]), a2[i], yv[i][ch][g]);
                     }
                 }
             }
@@ -281,31 +349,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (!DEBUG && !*abort_flag) {
+            float bias_r[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int64_t m = mt0 + q * 32 + r8 + 8 * i;
-                if (m >= args.M) continue;
-                const float sa = args.s_a[m];
-                float* yrow = args.y + m * args.N;
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const int64_t n = nt0 + h * (BN / 2) + g * 8 + 2 * cp;
-                    if (n + 1 < args.N) {
-                        const float b0 = args.bias ? args.bias[n] : 0.0f;
-                        const float b1 = args.bias ? args.bias[n + 1] : 0.0f;
-                        const float2 o = make_float2(fmaf(sa, yv[i][g].x, b0), fmaf(sa, yv[i][g].y, b1));
-                        if ((args.N & 1) == 0) {
-                            *reinterpret_cast<float2*>(yrow + n) = o;
-                        } else {
-                            yrow[n] = o.x;
-                            yrow[n + 1] = o.y;
-                        }
-                    } else if (n < args.N) {
-                        const float b0 = args.bias ? args.bias[n] : 0.0f;
-                        yrow[n] = fmaf(sa, yv[i][g].x, b0);
-                    }
-                }
+                const int64_t n = nt0 + q * 32 + r8 + 8 * i;
+                bias_r[i] = (args.bias && n < args.N) ? args.bias[n] : 0.0f;
             }
+#pragma unroll
+            for (int ch = 0; ch < CH; ++ch)
+#pragma unroll
+                for (int g = 0; g < 2; ++g)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int64_t m = mt0 + h * (TN / 4) + ch * 16 + 8 * g + 2 * cp + e;
+                        if (m >= args.M) continue;
+                        const float sa = args.s_a[m];
+                        float* yrow = args.y + m * args.N;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int64_t n = nt0 + q * 32 + r8 + 8 * i;
+                            if (n < args.N) yrow[n] = fmaf(sa, e ? yv[i][ch][g].y : yv[i][ch][g].x, bias_r[i]);
+                        }
+                    }
         }
     }
 
@@ -333,46 +398,45 @@ __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
     __syncthreads();
 }
 
-template <int BN, bool DEBUG>
+template <int TN, bool DEBUG>
 cudaError_t run(const GemmMaps& maps, const GemmArgs& a, cudaStream_t s) {
-    using C = Cfg<BN>;
+    using C = Cfg<TN>;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, DEBUG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<TN, DEBUG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    const int64_t tiles = ((a.m_cnt + kTileM - 1) / kTileM) * ((a.n_cnt + BN - 1) / BN);
-    gemm_kernel<BN, DEBUG><<<static_cast<unsigned>(tiles), kThreads, C::kSmemBytes, s>>>(maps.a, maps.b, a);
+    const int64_t tiles = ((a.m_cnt + TN - 1) / TN) * ((a.n_cnt + kTileW - 1) / kTileW);
+    gemm_kernel<TN, DEBUG><<<static_cast<unsigned>(tiles), kThreads, C::kSmemBytes, s>>>(maps.a, maps.b, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-int pick_block_n(int64_t m_cnt, int64_t n_cnt, int num_sms) {
-    // Estimated time ~ waves * (BN + fixed per-tile cost); ties go to the wider tile.
+int pick_token_tile(int64_t m_cnt, int64_t n_cnt, int num_sms) {
+    // Estimated time ~ waves * (TN + fixed per-tile cost); ties go to the wider tile.
     int best = 256;
     int64_t best_cost = -1;
     const int cands[3] = {256, 128, 64};
-    for (int bn : cands) {
-        const int64_t tiles = ((m_cnt + kTileM - 1) / kTileM) * ((n_cnt + bn - 1) / bn);
+    const int64_t tiles_w = (n_cnt + kTileW - 1) / kTileW;
+    for (int tn : cands) {
+        const int64_t tiles = ((m_cnt + tn - 1) / tn) * tiles_w;
         const int64_t waves = (tiles + num_sms - 1) / num_sms;
-        const int64_t cost = waves * (bn + 48);
+        const int64_t cost = waves * (tn + 48);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
-            best = bn;
+            best = tn;
         }
     }
     return best;
 }
 
-cudaError_t launch_gemm(const GemmMaps& maps, const GemmArgs& a, int block_n, bool debug, int num_sms,
-                        cudaStream_t s) {
-    (void)num_sms;
-    switch (block_n) {
+cudaError_t launch_gemm(const GemmMaps& maps, const GemmArgs& a, int tn, bool debug, cudaStream_t s) {
+    switch (tn) {
         case 256: return debug ? run<256, true>(maps, a, s) : run<256, false>(maps, a, s);
         case 128: return debug ? run<128, true>(maps, a, s) : run<128, false>(maps, a, s);
         case 64: return debug ? run<64, true>(maps, a, s) : run<64, false>(maps, a, s);

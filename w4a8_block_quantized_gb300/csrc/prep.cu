@@ -10,7 +10,7 @@
 //   - the API layout: int8 a_q [M][K], fp32 s_a [M], int32 rowsum [M][K/64], or
 //   - the tensor-core layout of the fused call: per row and 64-block the two e4m3
 //     nibble planes of section 3 eq. (3) (16*(a>>4) and a&15), s_a, and the row sums
-//     transposed for the GEMM epilogue.
+//     as the operand of the zero-point MMA.
 // The same launch also re-lays out the fp16 weight scales and zeros for the epilogue
 // (extra CTAs), so a call costs two launches in total.
 #include "sm103_ptx.cuh"
@@ -38,11 +38,18 @@ __device__ __forceinline__ void planes4(int a0, int a1, int a2, int a3, uint32_t
          (e4m3x2(static_cast<float>(a2 & 15), static_cast<float>(a3 & 15)) << 16);
 }
 
-// Position of row m in the transposed row-sum array: rows permuted within groups of 32
-// so that an epilogue thread finds its rows r, r+8, r+16, r+24 in one 16-byte vector.
-__device__ __forceinline__ int64_t perm32(int64_t m) {
-    const int r = static_cast<int>(m & 31);
-    return (m & ~static_cast<int64_t>(31)) + ((r & 7) << 2) + (r >> 3);
+// Zero-point operand of one token and block: rs = 64*rh + rl as the exact fp16 pair
+// {rh / 8, rl / 512} (see the rx layout in w4a8_internal.h), then 12 zero bytes.
+__device__ __forceinline__ uint4 rx_entry(int rs) {
+    const int rh = rs >> 6, rl = rs & 63;
+    const __half2 p = __floats2half2_rn(static_cast<float>(rh) * 0.125f, static_cast<float>(rl) * (1.0f / 512.0f));
+    return make_uint4(*reinterpret_cast<const uint32_t*>(&p), 0u, 0u, 0u);
+}
+
+// Position of weight row n in a prepared-scale row (see the wsc layout in w4a8_internal.h).
+__device__ __forceinline__ int64_t perm32(int64_t n) {
+    const int r = static_cast<int>(n & 31);
+    return (n & ~static_cast<int64_t>(31)) + ((r & 7) << 2) + (r >> 3);
 }
 
 // INT8 code of one activation: clamp(round_half_away(x / s), -127, 127), fp32 IEEE division.
@@ -54,25 +61,25 @@ __device__ __forceinline__ int quant1(float x, float s) {
 
 __device__ __forceinline__ float h2f(uint16_t bits) { return __half2float(__ushort_as_half(bits)); }
 
-// Weight-scale job: sz[b][p] = {512 s_w[2p,b], 512 s_w[2p+1,b], -z_w[2p,b]/512, -z_w[2p+1,b]/512},
-// zeros past N.  The powers of two undo the 2^-9 scale of the e4m3 weight operand.
+// Weight-scale job: per block b, 512 s_w[n,b] (fp32, rows permuted by perm32; the power
+// of two undoes the 2^-9 scale of the e4m3 weight operand) and {-z_w, -z_w} (fp16x2, row
+// order) for the zero-point MMA; zeros past N.
 __device__ void scales_job(const PrepArgs& a, int64_t cta, int64_t ctas) {
     const int64_t nb = a.K / kBlock;
-    const int64_t pairs = a.N_pad / 2;
-    const int64_t total = nb * pairs;
+    const int64_t total = nb * a.N_pad;
     for (int64_t i = cta * blockDim.x + threadIdx.x; i < total; i += ctas * blockDim.x) {
-        const int64_t b = i / pairs;
-        const int64_t n = 2 * (i - b * pairs);
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int64_t b = i / a.N_pad;
+        const int64_t n = i - b * a.N_pad;
+        float sv = 0.0f;
+        uint32_t zz = 0u;
         if (n < a.N) {
-            v.x = 512.0f * h2f(a.s_w[n * nb + b]);
-            v.z = -h2f(a.z_w[n * nb + b]) * (1.0f / 512.0f);
+            sv = 512.0f * h2f(a.s_w[n * nb + b]);
+            const uint32_t zb = static_cast<uint32_t>(a.z_w[n * nb + b]) ^ 0x8000u;  // -z_w, exact
+            zz = zb | (zb << 16);
         }
-        if (n + 1 < a.N) {
-            v.y = 512.0f * h2f(a.s_w[(n + 1) * nb + b]);
-            v.w = -h2f(a.z_w[(n + 1) * nb + b]) * (1.0f / 512.0f);
-        }
-        a.sz[i] = v;
+        float* row = a.wsc + b * 2 * a.N_pad;
+        row[perm32(n)] = sv;
+        reinterpret_cast<uint32_t*>(row + a.N_pad)[n] = zz;
     }
 }
 
@@ -80,7 +87,7 @@ __device__ void scales_job(const PrepArgs& a, int64_t cta, int64_t ctas) {
 template <int G, int V, bool PLANES>
 __global__ void __launch_bounds__(256) quant_kernel(const PrepArgs a, int row_ctas) {
     if (static_cast<int>(blockIdx.x) >= row_ctas) {
-        if (a.sz) scales_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
+        if (a.wsc) scales_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
         return;
     }
     __shared__ float red[2][8];
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(256) quant_kernel(const PrepArgs a, int row_ct
                     uint8_t* dst = a.apk + m * (2 * K) + b * 128 + ((f & 15) << 2);
                     *reinterpret_cast<uint32_t*>(dst) = hi;
                     *reinterpret_cast<uint32_t*>(dst + 64) = lo;
-                    if ((lane & 15) == 0) a.rT[b * a.M_pad + perm32(m)] = static_cast<float>(part);
+                    if ((lane & 15) == 0) a.rx[b * a.M_pad + m] = rx_entry(part);
                 } else {
                     const uint32_t w = (c0 & 0xff) | ((c1 & 0xff) << 8) | ((c2 & 0xff) << 16) |
                                        (static_cast<uint32_t>(c3 & 0xff) << 24);
@@ -162,7 +169,7 @@ __global__ void __launch_bounds__(256) quant_kernel(const PrepArgs a, int row_ct
 template <bool PLANES>
 __global__ void __launch_bounds__(256) quant_long_kernel(const PrepArgs a, int row_ctas) {
     if (static_cast<int>(blockIdx.x) >= row_ctas) {
-        if (a.sz) scales_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
+        if (a.wsc) scales_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
         return;
     }
     __shared__ float red[8];
@@ -211,7 +218,7 @@ __global__ void __launch_bounds__(256) quant_long_kernel(const PrepArgs a, int r
                     uint8_t* dst = a.apk + m * (2 * K) + b * 128 + ((f & 15) << 2);
                     *reinterpret_cast<uint32_t*>(dst) = hi;
                     *reinterpret_cast<uint32_t*>(dst + 64) = lo;
-                    if ((lane & 15) == 0) a.rT[b * a.M_pad + perm32(m)] = static_cast<float>(part);
+                    if ((lane & 15) == 0) a.rx[b * a.M_pad + m] = rx_entry(part);
                 } else {
                     const uint32_t w = (c0 & 0xff) | ((c1 & 0xff) << 8) | ((c2 & 0xff) << 16) |
                                        (static_cast<uint32_t>(c3 & 0xff) << 24);
@@ -227,7 +234,7 @@ __global__ void __launch_bounds__(256) quant_long_kernel(const PrepArgs a, int r
 // re-lay out the weight scales.  Rows row0 .. row0 + M - 1 of a_q_in.
 __global__ void __launch_bounds__(256) pack_kernel(const PrepArgs a, int row_ctas) {
     if (static_cast<int>(blockIdx.x) >= row_ctas) {
-        if (a.sz) scales_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
+        if (a.wsc) scales_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
         return;
     }
     const int64_t K = a.K, nb = K / kBlock, c16 = K / 16;
@@ -250,18 +257,18 @@ __global__ void __launch_bounds__(256) pack_kernel(const PrepArgs a, int row_cta
         *reinterpret_cast<uint4*>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(dst + 64) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    if (a.rs_in && a.rT) {
+    if (a.rs_in && a.rx) {
         const int64_t tot = a.M * nb;
         for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < tot; i += stride) {
             const int64_t b = i / a.M, m = i - b * a.M;
-            a.rT[b * a.M_pad + perm32(m)] = static_cast<float>(a.rs_in[(a.row0 + m) * nb + b]);
+            a.rx[b * a.M_pad + m] = rx_entry(a.rs_in[(a.row0 + m) * nb + b]);
         }
     }
 }
 
 int scale_ctas(const PrepArgs& a) {
-    if (!a.sz) return 0;
-    const int64_t total = (a.K / kBlock) * (a.N_pad / 2);
+    if (!a.wsc) return 0;
+    const int64_t total = (a.K / kBlock) * a.N_pad;
     const int64_t c = (total + 255) / 256;
     return static_cast<int>(c < 304 ? c : 304);
 }

@@ -69,6 +69,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(a, parity)) return true;
+        if (i > 8u) __nanosleep(32);  // long waits back off, leaving issue slots to working warps
         if ((i & 31u) == 0u) {
             if (*ctl.abort) return false;
             if (globaltimer_ns() - t0 > ctl.limit_ns) {
@@ -152,6 +153,17 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (fp16 or bf16 operands), issued by one thread.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far completes.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -174,12 +186,16 @@ __device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)
 }
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading/stride byte
-// offsets, fixed version field, swizzle mode.  `layout`: 2 = 128-byte swizzle,
-// 4 = 64-byte swizzle.  K-major operands with the swizzle atom base aligned.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo_bytes, uint32_t layout) {
+// offsets, fixed version field, swizzle mode.  `layout`: 0 = no swizzle, 2 = 128-byte
+// swizzle, 4 = 64-byte swizzle.  K-major operands; a swizzled tile's atom base is aligned
+// and its leading byte offset is unused.  Without swizzle the operand is built from 8-row x
+// 16-byte core matrices: `sbo` is the byte step between 8-row groups and `lbo` the byte
+// step between the two 16-byte halves along K.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo_bytes, uint32_t layout,
+                                              uint32_t lbo_bytes = 16) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(1u) << 16;                            // leading byte offset (unused here)
+    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;  // leading byte offset
     d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;  // stride byte offset
     d |= static_cast<uint64_t>(1u) << 46;                            // descriptor version
     d |= static_cast<uint64_t>(layout & 7u) << 61;
@@ -187,7 +203,8 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo_bytes
 }
 
 // Instruction descriptor for kind::f8f6f4 with E4M3 A and B, fp32 accumulator,
-// both operands K-major, shape M x N.
+// both operands K-major, shape M x N.  The same bits describe kind::f16 with fp16 A and B
+// (format code 0 in both kinds).
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
     return (1u << 4)             // D format: f32
            | (0u << 7)           // A format: e4m3
