@@ -57,7 +57,8 @@ typedef enum {
     W4A8_ERR_CUDA = -4,       /* a CUDA runtime call or a launch failed */
     W4A8_ERR_TIMEOUT = -5,    /* a kernel gave up on a bounded wait (read by w4a8_sync_status) */
     W4A8_ERR_WORKSPACE = -6,  /* workspace NULL or smaller than the *_workspace_bytes value */
-    W4A8_ERR_DEVICE = -7      /* current device is not an sm_103 GPU */
+    W4A8_ERR_DEVICE = -7,     /* current device is not an sm_103 GPU */
+    W4A8_ERR_SCRATCH_LIMIT = -8 /* problem needs more scratch than w4a8_prefill_linear_noalloc holds */
 } w4a8_status;
 
 /* Activation pre-pass (section 4 step 1: absmax -> scale -> INT8 codes + srcKernelSum),
@@ -103,6 +104,28 @@ int w4a8_linear_prepared(const void *act, const uint8_t *wq, const void *wsc, co
                          float *y, int64_t M, int64_t N, int64_t K, void *stream);
 size_t w4a8_prepared_activations_bytes(int64_t M, int64_t K);
 size_t w4a8_prepared_weights_bytes(int64_t N, int64_t K);
+
+/* w4a8_prefill_linear for callers that cannot allocate device memory (no counterpart in
+ * the paper; it exists for integration only).  Some callers have no way to hand the
+ * library a workspace: code that runs where cudaMalloc is not allowed or not wanted (an
+ * allocator-free runtime, a region that must not synchronize the device, a host with no
+ * spare memory budget for per-call buffers).  This entry point takes the same inputs
+ * and output as w4a8_prefill_linear but keeps its scratch in one fixed array that the
+ * library reserves statically on every GPU it is loaded on (W4A8_NOALLOC_SCRATCH_BYTES,
+ * held until the process exits), so it allocates and frees nothing.
+ *   - Problems whose w4a8_prefill_workspace_bytes(M, N, K) exceeds the array are rejected
+ *     with W4A8_ERR_SCRATCH_LIMIT before anything is launched.
+ *   - The first call on a device looks up the array's device address (a one-time
+ *     runtime query per device); make that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the previous call's
+ *     contents: calls that can overlap on the GPU (other streams, other threads) race on
+ *     it and must be serialized by the caller.  Nothing in it needs clearing between
+ *     calls: every scratch byte that feeds a stored output is rewritten by each call.
+ *   - Results are bit-identical to w4a8_prefill_linear on the same inputs. */
+#define W4A8_NOALLOC_SCRATCH_BYTES (16u << 20)
+int w4a8_prefill_linear_noalloc(const float *x, const uint8_t *wq, const uint16_t *w_scale,
+                                const uint16_t *w_zero, const float *bias, float *y,
+                                int64_t M, int64_t N, int64_t K, void *stream);
 
 /* Workspace sizes in bytes (0 for an empty problem; (size_t)-1 for invalid shapes). */
 size_t w4a8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);

@@ -22,6 +22,8 @@ W4A8_ERR_CUDA = -4
 W4A8_ERR_TIMEOUT = -5
 W4A8_ERR_WORKSPACE = -6
 W4A8_ERR_DEVICE = -7
+W4A8_ERR_SCRATCH_LIMIT = -8
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 # name -> (restype, argtypes); every symbol include/w4a8.h declares
 _P = ctypes.c_void_p
@@ -31,6 +33,7 @@ SIGNATURES = {
     "w4a8_quant_pack": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P]),
     "w4a8_linear": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "w4a8_prefill_linear": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    "w4a8_prefill_linear_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "w4a8_prepare_activations": (ctypes.c_int, [_P, _I64, _I64, _P, _SZ, _P]),
     "w4a8_prepare_weights": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _SZ, _P]),
     "w4a8_linear_prepared": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
@@ -158,6 +161,20 @@ def prefill_linear(x, wq, w_scale, w_zero, bias=None, y=None, ws=None, stream=No
     rc = load().w4a8_prefill_linear(_ptr(x), _ptr(wq), _ptr(w_scale), _ptr(w_zero), _ptr(bias), _ptr(y),
                                     M, N, K, _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "w4a8_prefill_linear")
+    return y
+
+
+def prefill_linear_noalloc(x, wq, w_scale, w_zero, bias=None, y=None, stream=None):
+    """w4a8_prefill_linear_noalloc: the fused call on the library's static scratch buffer,
+    for callers that cannot allocate device memory.  Serialize calls that could overlap."""
+    _want(x, torch.float32, "x")
+    _want(wq, torch.uint8, "wq")
+    M, K = x.shape
+    N = wq.shape[0]
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if y is None else y
+    rc = load().w4a8_prefill_linear_noalloc(_ptr(x), _ptr(wq), _ptr(w_scale), _ptr(w_zero), _ptr(bias), _ptr(y),
+                                            M, N, K, _stream(stream))
+    _check(rc, "w4a8_prefill_linear_noalloc")
     return y
 
 

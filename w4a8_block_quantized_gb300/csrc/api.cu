@@ -153,6 +153,7 @@ const char* w4a8_status_string(int status) {
         case W4A8_ERR_TIMEOUT: return "a kernel gave up on a bounded wait";
         case W4A8_ERR_WORKSPACE: return "workspace missing or too small";
         case W4A8_ERR_DEVICE: return "current device is not an sm_103 GPU";
+        case W4A8_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the static no-alloc buffer holds";
         default: return "unknown status";
     }
 }
@@ -395,6 +396,52 @@ int w4a8_selftest_wait_timeout(int64_t limit_us, void* stream) {
                                 static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? W4A8_OK
                : W4A8_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free variant
+// Scratch of w4a8_prefill_linear_noalloc: reserved statically on every device the library
+// is loaded on.  Host code must not use the array's name as an address (on the host it is
+// only a stand-in for the device symbol); the device address comes from
+// cudaGetSymbolAddress, resolved once per device with that device current.
+namespace w4a8 {
+namespace {
+static __device__ __align__(256) uint8_t g_noalloc_scratch[W4A8_NOALLOC_SCRATCH_BYTES];
+uint8_t* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+int noalloc_scratch(uint8_t** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return W4A8_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return W4A8_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return W4A8_ERR_CUDA;
+        g_noalloc_ptr[dev] = static_cast<uint8_t*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return W4A8_OK;
+}
+}  // namespace
+}  // namespace w4a8
+
+extern "C" {
+
+int w4a8_prefill_linear_noalloc(const float* x, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero,
+                                const float* bias, float* y, int64_t M, int64_t N, int64_t K, void* stream) {
+    int rc = check_shape(M, N, K);
+    if (rc != W4A8_OK) return rc;
+    if (M == 0 || N == 0) return W4A8_OK;
+    const size_t need = call_layout(M, N, K, true).total;
+    if (need > W4A8_NOALLOC_SCRATCH_BYTES) return W4A8_ERR_SCRATCH_LIMIT;
+    DeviceInfo* d = nullptr;
+    if ((rc = current_device(&d)) != W4A8_OK) return rc;
+    uint8_t* scratch = nullptr;
+    if ((rc = noalloc_scratch(&scratch)) != W4A8_OK) return rc;
+    return w4a8_prefill_linear(x, wq, w_scale, w_zero, bias, y, M, N, K, scratch, W4A8_NOALLOC_SCRATCH_BYTES,
+                               stream);
 }
 
 }  // extern "C"
