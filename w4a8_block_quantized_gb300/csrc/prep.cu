@@ -59,6 +59,68 @@ __device__ __forceinline__ int quant1(float x, float s) {
     return static_cast<int>(r);
 }
 
+// The same code, as a float, without a division in the common case.  With r = RN(1/s),
+// t = RN(x * r) lies within |x/s| * (2^-23 + 2^-48) of x/s, and the IEEE quotient
+// RN(x/s) within |x/s| * 2^-24; for |x/s| <= 127.5 the two differ by less than 2^-15.  So
+// unless t is within 2^-15 of a half-integer, round_half_away(t) equals round_half_away of
+// the IEEE quotient.  near_tie() flags the rest, which are recomputed with the division.
+__device__ __forceinline__ bool near_tie(float t) {
+    const float a = fabsf(t);
+    return fabsf((a - truncf(a)) - 0.5f) <= 0x1p-15f;
+}
+
+// round_half_away(t), and whether t lies within 2^-15 of a half-integer.
+__device__ __forceinline__ float round_flag(float t, bool& tie) {
+    const float a = fabsf(t);
+    const float ti = truncf(a);
+    const float f = a - ti;  // exact
+    tie |= fabsf(f - 0.5f) <= 0x1p-15f;
+    return copysignf(f >= 0.5f ? ti + 1.0f : ti, t);
+}
+
+// Quantize one lane's V float4 of a row to float codes.  No clamp is applied: for finite
+// inputs |x| <= absmax and s = RN(absmax/127), so |x/s| <= 127 (1 + 2^-24) and no code can
+// exceed 127 in magnitude, exactly as the clamped definition gives.  The rare near-tie
+// elements of the warp are recomputed with the IEEE division (warp-uniform branch).
+template <int V>
+__device__ __forceinline__ void quant_lane(const float4 (&x)[V], float4 (&q)[V], float s, float r) {
+    bool tie = false;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+        q[i].x = round_flag(x[i].x * r, tie);
+        q[i].y = round_flag(x[i].y * r, tie);
+        q[i].z = round_flag(x[i].z * r, tie);
+        q[i].w = round_flag(x[i].w * r, tie);
+    }
+    if (__any_sync(0xffffffffu, tie)) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            if (near_tie(x[i].x * r)) q[i].x = roundf(__fdiv_rn(x[i].x, s));
+            if (near_tie(x[i].y * r)) q[i].y = roundf(__fdiv_rn(x[i].y, s));
+            if (near_tie(x[i].z * r)) q[i].z = roundf(__fdiv_rn(x[i].z, s));
+            if (near_tie(x[i].w * r)) q[i].w = roundf(__fdiv_rn(x[i].w, s));
+        }
+    }
+}
+
+// Section 3 eq. (3) planes of four float codes (exact integers in [-127, 127]): hi word holds
+// e4m3(16 * floor(q / 16)) (the signed high nibble times 16), lo word e4m3(q - that) (the
+// unsigned low nibble), element j in byte j.
+__device__ __forceinline__ void planes4f(float4 q, uint32_t& hi, uint32_t& lo) {
+    const float h0 = 16.0f * floorf(q.x * 0.0625f), h1 = 16.0f * floorf(q.y * 0.0625f);
+    const float h2 = 16.0f * floorf(q.z * 0.0625f), h3 = 16.0f * floorf(q.w * 0.0625f);
+    hi = e4m3x2(h0, h1) | (e4m3x2(h2, h3) << 16);
+    lo = e4m3x2(q.x - h0, q.y - h1) | (e4m3x2(q.z - h2, q.w - h3) << 16);
+}
+
+// Four float codes as int8 bytes: adding 1.5 * 2^23 puts the integer, in two's complement,
+// in the low mantissa bits, whose low byte is the code.
+__device__ __forceinline__ uint32_t bytes4f(float4 q) {
+    const uint32_t b0 = __float_as_uint(q.x + 12582912.0f), b1 = __float_as_uint(q.y + 12582912.0f);
+    const uint32_t b2 = __float_as_uint(q.z + 12582912.0f), b3 = __float_as_uint(q.w + 12582912.0f);
+    return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+}
+
 __device__ __forceinline__ float h2f(uint16_t bits) { return __half2float(__ushort_as_half(bits)); }
 
 // Weight-scale job: per block b, 512 s_w[n,b] (fp32, rows permuted by perm32; the power
@@ -84,35 +146,41 @@ __device__ void scales_job(const PrepArgs& a, int64_t cta, int64_t ctas) {
 }
 
 // Register-resident pre-pass: G warps per row, V float4 per lane (row length K <= 128*G*V).
+// With V <= 8 the next iteration's row is loaded while the current one is quantized.
 template <int G, int V, bool PLANES>
-__global__ void __launch_bounds__(256) quant_kernel(const PrepArgs a, int row_ctas) {
+__global__ void __launch_bounds__(256, 2) quant_kernel(const PrepArgs a, int row_ctas) {
     if (static_cast<int>(blockIdx.x) >= row_ctas) {
         if (a.wsc) scales_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
         return;
     }
+    constexpr bool kPrefetch = V <= 8;
     __shared__ float red[2][8];
     constexpr int RPC = 8 / G;  // rows per CTA iteration
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wg = warp % G, rsub = warp / G;
     const int64_t K = a.K, n4 = K / 4, nb = K / kBlock;
-    int par = 0;
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPC; base < a.M;
-         base += static_cast<int64_t>(row_ctas) * RPC) {
-        const int64_t m = base + rsub;
+    const int64_t step = static_cast<int64_t>(row_ctas) * RPC;
+    auto load = [&](float4 (&v)[V], int64_t m) {
         const bool active = m < a.M;
         const float4* xr = reinterpret_cast<const float4*>(a.x) + (active ? (a.row0 + m) * n4 : 0);
-        float4 v[V];
-        float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             const int64_t f = static_cast<int64_t>(i * G + wg) * 32 + lane;
-            if (active && f < n4) {
-                v[i] = __ldcs(xr + f);
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
-            } else {
-                v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            v[i] = (active && f < n4) ? __ldcs(xr + f) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+    };
+    float4 v[V], nv[V];
+    int par = 0;
+    int64_t base = static_cast<int64_t>(blockIdx.x) * RPC;
+    if (base < a.M) load(v, base + rsub);
+    for (; base < a.M; base += step) {
+        const int64_t m = base + rsub;
+        const bool active = m < a.M;
+        if (kPrefetch && base + step < a.M) load(nv, base + step + rsub);
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
 #pragma unroll
         for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         if (G > 1) {
@@ -125,41 +193,61 @@ __global__ void __launch_bounds__(256) quant_kernel(const PrepArgs a, int row_ct
             par ^= 1;
         }
         const float s = __fdiv_rn(amax, 127.0f);
-        if (active && wg == 0 && lane == 0) {
-            if (a.s_a_out) a.s_a_out[m] = s;
-        }
-        const bool nz = amax > 0.0f;
+        const float r = __frcp_rn(s);
+        if (active && wg == 0 && lane == 0 && a.s_a_out) a.s_a_out[m] = s;
+        // the lane's V float4 in parts of H (bounded register pressure), each: quantize, write
+        // the operand or codes, then the 64-element block sums with the chains interleaved
+        constexpr int H = V > 8 ? V / 4 : (V >= 2 ? V / 2 : 1);
 #pragma unroll
-        for (int i = 0; i < V; ++i) {
-            const int64_t f = static_cast<int64_t>(i * G + wg) * 32 + lane;
-            int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
-            if (nz) {
-                c0 = quant1(v[i].x, s);
-                c1 = quant1(v[i].y, s);
-                c2 = quant1(v[i].z, s);
-                c3 = quant1(v[i].w, s);
+        for (int h0 = 0; h0 < V; h0 += H) {
+            float4 xh[H], q[H];
+#pragma unroll
+            for (int j = 0; j < H; ++j) xh[j] = v[h0 + j];
+            if (amax > 0.0f) {
+                quant_lane<H>(xh, q, s, r);
+            } else {
+#pragma unroll
+                for (int j = 0; j < H; ++j) q[j] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            int part = c0 + c1 + c2 + c3;  // 16 lanes = one 64-element block
-            part += __shfl_xor_sync(0xffffffffu, part, 8);
-            part += __shfl_xor_sync(0xffffffffu, part, 4);
-            part += __shfl_xor_sync(0xffffffffu, part, 2);
-            part += __shfl_xor_sync(0xffffffffu, part, 1);
-            if (active && f < n4) {
-                const int64_t b = f >> 4;
-                if (PLANES) {
-                    uint32_t hi, lo;
-                    planes4(c0, c1, c2, c3, hi, lo);
-                    uint8_t* dst = a.apk + m * (2 * K) + b * 128 + ((f & 15) << 2);
-                    *reinterpret_cast<uint32_t*>(dst) = hi;
-                    *reinterpret_cast<uint32_t*>(dst + 64) = lo;
-                    if ((lane & 15) == 0) a.rx[b * a.M_pad + m] = rx_entry(part);
-                } else {
-                    const uint32_t w = (c0 & 0xff) | ((c1 & 0xff) << 8) | ((c2 & 0xff) << 16) |
-                                       (static_cast<uint32_t>(c3 & 0xff) << 24);
-                    *reinterpret_cast<uint32_t*>(a.a_q_out + m * K + 4 * f) = w;
-                    if ((lane & 15) == 0) a.rs_out[m * nb + b] = part;
+            float part[H];
+#pragma unroll
+            for (int j = 0; j < H; ++j) {
+                const int64_t f = static_cast<int64_t>((h0 + j) * G + wg) * 32 + lane;
+                part[j] = (q[j].x + q[j].y) + (q[j].z + q[j].w);  // exact
+                if (active && f < n4) {
+                    if (PLANES) {
+                        uint32_t hi, lo;
+                        planes4f(q[j], hi, lo);
+                        uint8_t* dst = a.apk + m * (2 * K) + (f >> 4) * 128 + ((f & 15) << 2);
+                        *reinterpret_cast<uint32_t*>(dst) = hi;
+                        *reinterpret_cast<uint32_t*>(dst + 64) = lo;
+                    } else {
+                        *reinterpret_cast<uint32_t*>(a.a_q_out + m * K + 4 * f) = bytes4f(q[j]);
+                    }
                 }
             }
+#pragma unroll
+            for (int o = 8; o; o >>= 1)
+#pragma unroll
+                for (int j = 0; j < H; ++j) part[j] += __shfl_xor_sync(0xffffffffu, part[j], o);
+            if (active && (lane & 15) == 0) {
+#pragma unroll
+                for (int j = 0; j < H; ++j) {
+                    const int64_t f = static_cast<int64_t>((h0 + j) * G + wg) * 32 + lane;
+                    if (f < n4) {
+                        const int64_t b = f >> 4;
+                        const int rs = static_cast<int>(part[j]);
+                        if (PLANES) a.rx[b * a.M_pad + m] = rx_entry(rs);
+                        else a.rs_out[m * nb + b] = rs;
+                    }
+                }
+            }
+        }
+        if (kPrefetch) {
+#pragma unroll
+            for (int i = 0; i < V; ++i) v[i] = nv[i];
+        } else if (base + step < a.M) {
+            load(v, base + step + rsub);
         }
     }
 }
@@ -286,13 +374,14 @@ cudaError_t run_quant(const PrepArgs& a, cudaStream_t s) {
 template <bool PLANES>
 cudaError_t dispatch_quant(const PrepArgs& a, cudaStream_t s) {
     const int64_t n4 = a.K / 4;
-    // smallest warp group G whose lanes hold the row in at most 16 float4 each
+    // smallest warp group G whose lanes hold the row in at most 8 float4 each (so the next
+    // row can be prefetched), then 16 float4 without prefetch, then the two-pass kernel
     if (n4 <= 32 * 2) return run_quant<1, 2, PLANES>(a, s);
     if (n4 <= 32 * 4) return run_quant<1, 4, PLANES>(a, s);
     if (n4 <= 32 * 8) return run_quant<1, 8, PLANES>(a, s);
-    if (n4 <= 32 * 16) return run_quant<1, 16, PLANES>(a, s);
-    if (n4 <= 64 * 16) return run_quant<2, 16, PLANES>(a, s);
-    if (n4 <= 128 * 16) return run_quant<4, 16, PLANES>(a, s);
+    if (n4 <= 64 * 8) return run_quant<2, 8, PLANES>(a, s);
+    if (n4 <= 128 * 8) return run_quant<4, 8, PLANES>(a, s);
+    if (n4 <= 256 * 8) return run_quant<8, 8, PLANES>(a, s);
     if (n4 <= 256 * 16) return run_quant<8, 16, PLANES>(a, s);
     const int row_ctas = static_cast<int>(a.M < 152 * 4 ? a.M : 152 * 4);
     quant_long_kernel<PLANES><<<row_ctas + scale_ctas(a), 256, 0, s>>>(a, row_ctas);
