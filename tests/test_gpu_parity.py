@@ -261,3 +261,35 @@ def test_split_calls_equal_fused():
         assert torch.equal(y_split, y_fused)
         y_ref, bound, _, _, _ = oracle.prefill_linear(d0["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
         check_y(y_split, y_ref, bound, f"split N={N}")
+
+
+def test_quant_pack_near_ties_bitexact():
+    """Activations placed on and around the rounding boundaries (k + 1/2) * s_a, for scales
+    that are not powers of two: the codes must match the oracle's IEEE-division rounding
+    bit for bit (the kernel divides only near such boundaries)."""
+    rng = np.random.default_rng(123)
+    rows = []
+    for absmax in (1.0, 3.7, 0.013, 255.99, 1e-3, 77.77, 1.0e6, 0.3333333):
+        a32 = np.float32(absmax)
+        s = np.float32(a32 / np.float32(127.0))
+        xs = [a32, -a32]
+        for k in range(-126, 127, 3):
+            c = np.float32((k + 0.5) * np.float64(s))
+            xs += [c, np.nextafter(c, np.float32(np.inf)), np.nextafter(c, np.float32(-np.inf))]
+            c2 = np.nextafter(np.nextafter(c, np.float32(np.inf)), np.float32(np.inf))
+            xs += [c2, np.nextafter(c2, np.float32(np.inf))]
+        xs = np.array(xs, np.float32)
+        xs = xs[np.abs(xs) <= a32]
+        K = ((len(xs) + 63) // 64) * 64
+        row = np.zeros(K, np.float32)
+        row[:len(xs)] = rng.permutation(xs)
+        rows.append(row)
+    K = max(len(r) for r in rows)
+    x = np.zeros((len(rows), K), np.float32)
+    for i, r in enumerate(rows):
+        x[i, :len(r)] = r
+    a_q, s_a, rs = B().quant_pack(to_dev(x))
+    ra, rsa, rrs = oracle.quant_pack(x)
+    assert np.array_equal(s_a.cpu().numpy(), rsa)
+    assert np.array_equal(a_q.cpu().numpy(), ra)
+    assert np.array_equal(rs.cpu().numpy(), rrs)
