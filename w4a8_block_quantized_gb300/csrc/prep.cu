@@ -69,13 +69,15 @@ __device__ __forceinline__ bool near_tie(float t) {
     return fabsf((a - truncf(a)) - 0.5f) <= 0x1p-15f;
 }
 
-// round_half_away(t), and whether t lies within 2^-15 of a half-integer.
-__device__ __forceinline__ float round_flag(float t, bool& tie) {
-    const float a = fabsf(t);
-    const float ti = truncf(a);
-    const float f = a - ti;  // exact
-    tie |= fabsf(f - 0.5f) <= 0x1p-15f;
-    return copysignf(f >= 0.5f ? ti + 1.0f : ti, t);
+// t rounded to the nearest integer (ties to even), and whether t lies within 2^-15 of a
+// half-integer.  |t - rint(t)| is exact (the two are within a factor two of each other, or
+// the integer is 0) and equals the distance of frac(|t|) from the nearer integer, so the
+// flag is the near_tie() test.  Away from the flagged values round-to-even and
+// round-half-away agree; the flagged ones are recomputed by the caller.
+__device__ __forceinline__ float rint_flag(float t, bool& tie) {
+    const float q = rintf(t);
+    tie |= fabsf(t - q) >= 0.5f - 0x1p-15f;
+    return q;
 }
 
 // Quantize one lane's V float4 of a row to float codes.  No clamp is applied: for finite
@@ -87,10 +89,10 @@ __device__ __forceinline__ void quant_lane(const float4 (&x)[V], float4 (&q)[V],
     bool tie = false;
 #pragma unroll
     for (int i = 0; i < V; ++i) {
-        q[i].x = round_flag(x[i].x * r, tie);
-        q[i].y = round_flag(x[i].y * r, tie);
-        q[i].z = round_flag(x[i].z * r, tie);
-        q[i].w = round_flag(x[i].w * r, tie);
+        q[i].x = rint_flag(x[i].x * r, tie);
+        q[i].y = rint_flag(x[i].y * r, tie);
+        q[i].z = rint_flag(x[i].z * r, tie);
+        q[i].w = rint_flag(x[i].w * r, tie);
     }
     if (__any_sync(0xffffffffu, tie)) {
 #pragma unroll
