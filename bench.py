@@ -268,19 +268,19 @@ def run_bench(args):
     for t in lin:
         s = t["spec"]
         act = binding.prepare_activations(t["x"], stream=stream)
-        wsc = binding.prepare_weights(t["s_w"], t["z_w"], s.K, stream=stream)
-        prepared.append((act, wsc))
+        pw = binding.prepare_weights(t["wq"], t["s_w"], t["z_w"], stream=stream)
+        prepared.append((act, pw))
     kreps = max(20, min(args.steps, 200))
     for _ in range(kreps):
         g_ms = p_ms = 0.0
-        for t, (act, wsc) in zip(lin, prepared):
+        for t, (act, pw) in zip(lin, prepared):
             s = t["spec"]
             e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             flush.zero_()
             e0.record(stream)
             binding.prepare_activations(t["x"], act=act, stream=stream)
             e1.record(stream)
-            binding.linear_prepared(act, t["wq"], wsc, s.M, s.K, bias=t["bias"], y=t["y"], stream=stream)
+            binding.linear_prepared(act, pw, s.M, s.N, s.K, bias=t["bias"], y=t["y"], stream=stream)
             e2.record(stream)
             e2.synchronize()
             p_ms += e0.elapsed_time(e1)

@@ -87,21 +87,24 @@ int w4a8_prefill_linear(const float *x, const uint8_t *wq, const uint16_t *w_sca
 
 /* Split form of w4a8_prefill_linear, for callers that reuse one side across calls
  * (one activation pre-pass shared by several linears that read the same input, or
- * weight scales laid out once at load time):
+ * weights prepared once at load time):
  *   w4a8_prepare_activations  section 4 step 1 into `act` (tensor-core operand planes,
  *                             s_a, transposed row sums); act: >= w4a8_prepared_activations_bytes(M, K)
- *   w4a8_prepare_weights      re-lays out s_w / z_w for the epilogue into `wsc`;
- *                             wsc: >= w4a8_prepared_weights_bytes(N, K)
+ *   w4a8_prepare_weights      the weight operand of the tensor cores (the u4 codes of wq
+ *                             expanded to one byte each) and s_w / z_w laid out for the
+ *                             epilogue and the zero-point term, into `pw`;
+ *                             pw: >= w4a8_prepared_weights_bytes(N, K)
  *   w4a8_linear_prepared      the contraction + epilogue from both (section 4 steps 2-3)
- * The buffers are opaque; their contents are only valid for the same M / N / K.
+ * The buffers are opaque; their contents are only valid for the same M / N / K.  wq, the
+ * scales and the zeros are not read again after w4a8_prepare_weights.
  * prepare_activations + prepare_weights + linear_prepared equals w4a8_prefill_linear
  * bit for bit. */
 int w4a8_prepare_activations(const float *x, int64_t M, int64_t K, void *act, size_t act_bytes,
                              void *stream);
-int w4a8_prepare_weights(const uint16_t *w_scale, const uint16_t *w_zero, int64_t N, int64_t K,
-                         void *wsc, size_t wsc_bytes, void *stream);
-int w4a8_linear_prepared(const void *act, const uint8_t *wq, const void *wsc, const float *bias,
-                         float *y, int64_t M, int64_t N, int64_t K, void *stream);
+int w4a8_prepare_weights(const uint8_t *wq, const uint16_t *w_scale, const uint16_t *w_zero,
+                         int64_t N, int64_t K, void *pw, size_t pw_bytes, void *stream);
+int w4a8_linear_prepared(const void *act, const void *pw, const float *bias, float *y,
+                         int64_t M, int64_t N, int64_t K, void *stream);
 size_t w4a8_prepared_activations_bytes(int64_t M, int64_t K);
 size_t w4a8_prepared_weights_bytes(int64_t N, int64_t K);
 
@@ -130,12 +133,13 @@ int w4a8_prefill_linear_noalloc(const float *x, const uint8_t *wq, const uint16_
 /* Workspace sizes in bytes (0 for an empty problem; (size_t)-1 for invalid shapes). */
 size_t w4a8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 size_t w4a8_prefill_workspace_bytes(int64_t M, int64_t N, int64_t K);
-size_t w4a8_debug_workspace_bytes(int64_t m_cnt, int64_t K);
+size_t w4a8_debug_workspace_bytes(int64_t m_cnt, int64_t n_cnt, int64_t K);
 
 /* Debug: the exact per-block int32 accumulators acc[m][n][b] (section 3 eq. (2), first
  * sum) for the window m0 <= m < m0 + m_cnt, n0 <= n < n0 + n_cnt, computed by the same
- * tensor-core contraction as w4a8_linear.  acc: int32 [m_cnt][n_cnt][K/64].
- * The window must lie inside [0, M) x [0, N) and be non-empty. */
+ * tensor-core contraction as w4a8_linear.  acc: int32 [m_cnt][n_cnt][K/64], indexed by
+ * the position inside the window.  The window must lie inside [0, M) x [0, N) and be
+ * non-empty.  workspace: at least w4a8_debug_workspace_bytes(m_cnt, n_cnt, K) bytes. */
 int w4a8_debug_block_acc(const int8_t *a_q, const uint8_t *wq, int64_t M, int64_t N, int64_t K,
                          int64_t m0, int64_t m_cnt, int64_t n0, int64_t n_cnt, int32_t *acc,
                          void *workspace, size_t workspace_bytes, void *stream);

@@ -44,7 +44,7 @@ def test_status_strings(lib):
         s = b.status_string(code)
         assert s and s != "unknown status"
     assert b.status_string(12345) == "unknown status"
-    assert lib.w4a8_abi_version() == 100
+    assert lib.w4a8_abi_version() == 200
 
 
 def test_shape_checks_need_no_gpu(lib):
@@ -76,9 +76,10 @@ def test_workspace_sizes(lib):
     nb = K // 64
     lin = lib.w4a8_linear_workspace_bytes(M, N, K)
     pre = lib.w4a8_prefill_workspace_bytes(M, N, K)
-    # operand planes (2 bytes per activation) + transposed row sums + re-laid-out scales
-    assert lin >= 2 * M * K + nb * M * 4 + nb * N * 8
+    # operand planes (2 bytes per activation) + transposed row sums (16 bytes per entry)
+    # + expanded weights (1 byte each) + scales and weight-side zero-point rows (4 + 16 bytes)
+    assert lin >= 2 * M * K + nb * M * 16 + N * K + nb * N * 20
     assert pre >= lin + 4 * M
     assert lib.w4a8_linear_workspace_bytes(0, N, K) == 0
     assert lib.w4a8_linear_workspace_bytes(M, N, 100) == ctypes.c_size_t(-1).value
-    assert lib.w4a8_debug_workspace_bytes(7, 128) >= 7 * 256
+    assert lib.w4a8_debug_workspace_bytes(7, 9, 128) >= 7 * 256 + 9 * 128

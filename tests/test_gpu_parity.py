@@ -255,8 +255,8 @@ def test_split_calls_equal_fused():
     for N, seed in ((512, 21), (130, 22), (1000, 23)):
         d = synth.random_small(M, K, N, seed=seed, bias=True)
         g = inputs_to_dev(d)
-        wsc = b.prepare_weights(g["s_w"], g["z_w"], K)
-        y_split = b.linear_prepared(act, g["wq"], wsc, M, K, bias=g["bias"])
+        pw = b.prepare_weights(g["wq"], g["s_w"], g["z_w"])
+        y_split = b.linear_prepared(act, pw, M, N, K, bias=g["bias"])
         y_fused = b.prefill_linear(x, g["wq"], g["s_w"], g["z_w"], g["bias"])
         assert torch.equal(y_split, y_fused)
         y_ref, bound, _, _, _ = oracle.prefill_linear(d0["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])

@@ -35,13 +35,13 @@ SIGNATURES = {
     "w4a8_prefill_linear": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "w4a8_prefill_linear_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "w4a8_prepare_activations": (ctypes.c_int, [_P, _I64, _I64, _P, _SZ, _P]),
-    "w4a8_prepare_weights": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _SZ, _P]),
-    "w4a8_linear_prepared": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "w4a8_prepare_weights": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _SZ, _P]),
+    "w4a8_linear_prepared": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "w4a8_prepared_activations_bytes": (_SZ, [_I64, _I64]),
     "w4a8_prepared_weights_bytes": (_SZ, [_I64, _I64]),
     "w4a8_linear_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "w4a8_prefill_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
-    "w4a8_debug_workspace_bytes": (_SZ, [_I64, _I64]),
+    "w4a8_debug_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "w4a8_debug_block_acc": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P, _SZ, _P]),
     "w4a8_sync_status": (ctypes.c_int, [_P]),
     "w4a8_selftest_wait_timeout": (ctypes.c_int, [_I64, _P]),
@@ -110,8 +110,8 @@ def prefill_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(load().w4a8_prefill_workspace_bytes(M, N, K))
 
 
-def debug_workspace_bytes(m_cnt: int, K: int) -> int:
-    return int(load().w4a8_debug_workspace_bytes(m_cnt, K))
+def debug_workspace_bytes(m_cnt: int, n_cnt: int, K: int) -> int:
+    return int(load().w4a8_debug_workspace_bytes(m_cnt, n_cnt, K))
 
 
 def workspace(nbytes: int, device) -> torch.Tensor:
@@ -196,23 +196,24 @@ def prepare_activations(x, act=None, stream=None):
     return act
 
 
-def prepare_weights(w_scale, w_zero, K: int, wsc=None, stream=None):
-    """w4a8_prepare_weights: the epilogue layout of s_w / z_w (returned)."""
+def prepare_weights(wq, w_scale, w_zero, pw=None, stream=None):
+    """w4a8_prepare_weights: the tensor-core weight operand and the scale / zero layout
+    (an opaque buffer, returned)."""
+    _want(wq, torch.uint8, "wq")
     _want(w_scale, torch.float16, "w_scale")
     _want(w_zero, torch.float16, "w_zero")
-    N = w_scale.shape[0]
-    wsc = workspace(prepared_weights_bytes(N, K), w_scale.device) if wsc is None else wsc
-    rc = load().w4a8_prepare_weights(_ptr(w_scale), _ptr(w_zero), N, K, _ptr(wsc), wsc.numel(), _stream(stream))
+    N, K = wq.shape[0], 2 * wq.shape[1]
+    pw = workspace(prepared_weights_bytes(N, K), wq.device) if pw is None else pw
+    rc = load().w4a8_prepare_weights(_ptr(wq), _ptr(w_scale), _ptr(w_zero), N, K, _ptr(pw), pw.numel(),
+                                     _stream(stream))
     _check(rc, "w4a8_prepare_weights")
-    return wsc
+    return pw
 
 
-def linear_prepared(act, wq, wsc, M: int, K: int, bias=None, y=None, stream=None):
+def linear_prepared(act, pw, M: int, N: int, K: int, bias=None, y=None, stream=None):
     """w4a8_linear_prepared: contraction + epilogue from prepared operands -> y fp32 [M,N]."""
-    _want(wq, torch.uint8, "wq")
-    N = wq.shape[0]
-    y = torch.empty((M, N), dtype=torch.float32, device=wq.device) if y is None else y
-    rc = load().w4a8_linear_prepared(_ptr(act), _ptr(wq), _ptr(wsc), _ptr(bias), _ptr(y), M, N, K, _stream(stream))
+    y = torch.empty((M, N), dtype=torch.float32, device=act.device) if y is None else y
+    rc = load().w4a8_linear_prepared(_ptr(act), _ptr(pw), _ptr(bias), _ptr(y), M, N, K, _stream(stream))
     _check(rc, "w4a8_linear_prepared")
     return y
 
@@ -225,7 +226,7 @@ def debug_block_acc(a_q, wq, N, m0=0, m_cnt=None, n0=0, n_cnt=None, ws=None, str
     n_cnt = N - n0 if n_cnt is None else n_cnt
     acc = torch.empty((m_cnt, n_cnt, K // 64), dtype=torch.int32, device=a_q.device)
     if ws is None:
-        ws = workspace(debug_workspace_bytes(m_cnt, K), a_q.device)
+        ws = workspace(debug_workspace_bytes(m_cnt, n_cnt, K), a_q.device)
     rc = load().w4a8_debug_block_acc(_ptr(a_q), _ptr(wq), M, N, K, m0, m_cnt, n0, n_cnt, _ptr(acc),
                                      _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "w4a8_debug_block_acc")

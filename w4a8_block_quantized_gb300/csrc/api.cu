@@ -49,38 +49,6 @@ int current_device(DeviceInfo** out) {
     return W4A8_OK;
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-// 2-D uint8 tensor map: `rows` rows of `inner` bytes at `stride` bytes; box inner x rows.
-bool make_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t stride,
-                 uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {inner, rows};
-    const cuuint64_t strides[1] = {stride};
-    const cuuint32_t box[2] = {box_inner, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 constexpr int64_t kMaxDim = 2147483647LL;
@@ -91,47 +59,57 @@ int check_shape(int64_t M, int64_t N, int64_t K) {
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return W4A8_ERR_SHAPE;
     // tensor-map coordinates and the weight-row byte stride stay within 32 bits
     if (2 * K > kMaxDim || N > (int64_t(1) << 31)) return W4A8_ERR_SHAPE;
+    // the GEMM counts its 64-blocks (output tiles x K/64) in 32 bits
+    const int64_t tiles = ((M + kTileT - 1) / kTileT) * ((N + kTileW - 1) / kTileW);
+    if (tiles > kMaxDim / (K / kBlock)) return W4A8_ERR_SHAPE;
     return W4A8_OK;
 }
 
-// Workspace of the one-call entry points: prepared activations, then prepared scales.
+// Workspace of the one-call entry points: prepared activations, then prepared weights.
 struct CallLayout {
     ActLayout act;
-    size_t wsc = 0, total = 0;
+    WLayout w;
+    size_t w_off = 0, total = 0;
 };
 
 CallLayout call_layout(int64_t M, int64_t N, int64_t K, bool with_sa) {
     CallLayout c;
-    c.act = act_layout(M, K, with_sa, true);
-    c.wsc = c.act.total;
-    c.total = c.wsc + wsc_bytes(N, K);
+    c.act = act_layout(M, K, with_sa);
+    c.w = w_layout(N, K);
+    c.w_off = c.act.total;
+    c.total = c.w_off + c.w.total;
     return c;
 }
 
-// GEMM + epilogue from prepared activations (apk, rx at act offsets) and prepared scales.
-int run_linear(const uint8_t* act, const ActLayout& A, const float* s_a, const float* wsc, const uint8_t* wq,
-               const float* bias, float* y, int64_t M, int64_t N, int64_t K, const DeviceInfo& d, cudaStream_t st) {
-    GemmMaps maps;
-    const int tn = pick_token_tile(M, N, d.num_sms);
-    if (!make_map_u8(&maps.a, act + A.apk, 2 * K, M, 2 * K, 128, tn, CU_TENSOR_MAP_SWIZZLE_128B))
-        return W4A8_ERR_CUDA;
-    if (!make_map_u8(&maps.b, wq, K / 2, N, K / 2, 32, kTileW, CU_TENSOR_MAP_SWIZZLE_NONE)) return W4A8_ERR_CUDA;
+// GEMM + epilogue from prepared activations (token records) and prepared weights.
+int run_linear(const uint8_t* trec, const float* s_a, const uint8_t* pw, const float* bias, float* y, int64_t M,
+               int64_t N, int64_t K, const DeviceInfo& d, cudaStream_t st) {
+    const WLayout W = w_layout(N, K);
     GemmArgs g;
     g.M = M;
     g.N = N;
     g.K = K;
-    g.m_cnt = M;
-    g.n0 = 0;
-    g.n_cnt = N;
-    g.M_pad = A.M_pad;
-    g.N_pad = n_pad(N);
-    g.wsc = wsc;
-    g.rx = reinterpret_cast<const uint4*>(act + A.rx);
+    g.trec = trec;
+    g.wrec = pw;
+    g.sc = reinterpret_cast<const float*>(pw + W.sc);
     g.s_a = s_a;
     g.bias = bias;
     g.y = y;
     g.status = d.status;
-    return launch_gemm(maps, g, tn, false, st) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
+    return launch_gemm(g, false, d.num_sms, st) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
+}
+
+// Weight job arguments: all N rows of wq into the weight records at `wrec`.
+void set_weight_job(PrepArgs* p, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero, int64_t N,
+                    int64_t K, uint8_t* wrec) {
+    p->K = K;
+    p->wq = wq;
+    p->n_first = 0;
+    p->s_w = w_scale;
+    p->z_w = w_zero;
+    p->N = N;
+    p->wrec = wrec;
+    p->sc = reinterpret_cast<float*>(wrec + w_layout(N, K).sc);
 }
 
 }  // namespace
@@ -141,7 +119,7 @@ using namespace w4a8;
 
 extern "C" {
 
-int w4a8_abi_version(void) { return 100; }
+int w4a8_abi_version(void) { return 200; }
 
 const char* w4a8_status_string(int status) {
     switch (status) {
@@ -170,21 +148,21 @@ size_t w4a8_prefill_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return call_layout(M, N, K, true).total;
 }
 
-size_t w4a8_debug_workspace_bytes(int64_t m_cnt, int64_t K) {
-    if (check_shape(m_cnt, 1, K) != W4A8_OK || m_cnt == 0) return static_cast<size_t>(-1);
-    return act_layout(m_cnt, K, false, false).total;
+size_t w4a8_debug_workspace_bytes(int64_t m_cnt, int64_t n_cnt, int64_t K) {
+    if (check_shape(m_cnt, n_cnt, K) != W4A8_OK || m_cnt == 0 || n_cnt == 0) return static_cast<size_t>(-1);
+    return act_layout(m_cnt, K, false).total + w_layout(n_cnt, K).total;
 }
 
 size_t w4a8_prepared_activations_bytes(int64_t M, int64_t K) {
     if (check_shape(M, 1, K) != W4A8_OK) return static_cast<size_t>(-1);
     if (M == 0) return 0;
-    return act_layout(M, K, true, true).total;
+    return act_layout(M, K, true).total;
 }
 
 size_t w4a8_prepared_weights_bytes(int64_t N, int64_t K) {
     if (check_shape(1, N, K) != W4A8_OK) return static_cast<size_t>(-1);
     if (N == 0) return 0;
-    return wsc_bytes(N, K);
+    return w_layout(N, K).total;
 }
 
 int w4a8_quant_pack(const float* x, int64_t M, int64_t K, int8_t* a_q, float* a_scale, int32_t* rowsum,
@@ -227,17 +205,10 @@ int w4a8_linear(const int8_t* a_q, const float* a_scale, const int32_t* rowsum, 
     p.a_q_in = a_q;
     p.rs_in = rowsum;
     p.M = M;
-    p.K = K;
-    p.apk = ws + L.act.apk;
-    p.rx = reinterpret_cast<uint4*>(ws + L.act.rx);
-    p.M_pad = L.act.M_pad;
-    p.s_w = w_scale;
-    p.z_w = w_zero;
-    p.N = N;
-    p.N_pad = n_pad(N);
-    p.wsc = reinterpret_cast<float*>(ws + L.wsc);
+    p.trec = ws + L.act.rec;
+    set_weight_job(&p, wq, w_scale, w_zero, N, K, ws + L.w_off);
     if (launch_pack(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
-    return run_linear(ws, L.act, a_scale, reinterpret_cast<const float*>(ws + L.wsc), wq, bias, y, M, N, K, *d, st);
+    return run_linear(ws + L.act.rec, a_scale, ws + L.w_off, bias, y, M, N, K, *d, st);
 }
 
 int w4a8_prefill_linear(const float* x, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero,
@@ -261,18 +232,11 @@ int w4a8_prefill_linear(const float* x, const uint8_t* wq, const uint16_t* w_sca
     PrepArgs p;
     p.x = x;
     p.M = M;
-    p.K = K;
     p.s_a_out = s_a;
-    p.apk = ws + L.act.apk;
-    p.rx = reinterpret_cast<uint4*>(ws + L.act.rx);
-    p.M_pad = L.act.M_pad;
-    p.s_w = w_scale;
-    p.z_w = w_zero;
-    p.N = N;
-    p.N_pad = n_pad(N);
-    p.wsc = reinterpret_cast<float*>(ws + L.wsc);
+    p.trec = ws + L.act.rec;
+    set_weight_job(&p, wq, w_scale, w_zero, N, K, ws + L.w_off);
     if (launch_quant(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
-    return run_linear(ws, L.act, s_a, reinterpret_cast<const float*>(ws + L.wsc), wq, bias, y, M, N, K, *d, st);
+    return run_linear(ws + L.act.rec, s_a, ws + L.w_off, bias, y, M, N, K, *d, st);
 }
 
 int w4a8_prepare_activations(const float* x, int64_t M, int64_t K, void* act, size_t act_bytes, void* stream) {
@@ -281,7 +245,7 @@ int w4a8_prepare_activations(const float* x, int64_t M, int64_t K, void* act, si
     if (M == 0) return W4A8_OK;
     if (!x || !act) return W4A8_ERR_ARG;
     if (!aligned(x, 16) || !aligned(act, 16)) return W4A8_ERR_ALIGN;
-    const ActLayout A = act_layout(M, K, true, true);
+    const ActLayout A = act_layout(M, K, true);
     if (act_bytes < A.total) return W4A8_ERR_WORKSPACE;
     DeviceInfo* d = nullptr;
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
@@ -291,46 +255,39 @@ int w4a8_prepare_activations(const float* x, int64_t M, int64_t K, void* act, si
     p.M = M;
     p.K = K;
     p.s_a_out = reinterpret_cast<float*>(a + A.s_a);
-    p.apk = a + A.apk;
-    p.rx = reinterpret_cast<uint4*>(a + A.rx);
-    p.M_pad = A.M_pad;
+    p.trec = a + A.rec;
     return launch_quant(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
 }
 
-int w4a8_prepare_weights(const uint16_t* w_scale, const uint16_t* w_zero, int64_t N, int64_t K, void* wsc,
-                         size_t wsc_size, void* stream) {
+int w4a8_prepare_weights(const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero, int64_t N, int64_t K,
+                         void* pw, size_t pw_bytes, void* stream) {
     int rc = check_shape(1, N, K);
     if (rc != W4A8_OK) return rc;
     if (N == 0) return W4A8_OK;
-    if (!w_scale || !w_zero || !wsc) return W4A8_ERR_ARG;
-    if (!aligned(w_scale, 2) || !aligned(w_zero, 2) || !aligned(wsc, 16)) return W4A8_ERR_ALIGN;
-    if (wsc_size < wsc_bytes(N, K)) return W4A8_ERR_WORKSPACE;
+    if (!wq || !w_scale || !w_zero || !pw) return W4A8_ERR_ARG;
+    if (!aligned(wq, 16) || !aligned(w_scale, 2) || !aligned(w_zero, 2) || !aligned(pw, 16)) return W4A8_ERR_ALIGN;
+    const WLayout W = w_layout(N, K);
+    if (pw_bytes < W.total) return W4A8_ERR_WORKSPACE;
     DeviceInfo* d = nullptr;
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
     PrepArgs p;
     p.M = 0;
-    p.K = K;
-    p.s_w = w_scale;
-    p.z_w = w_zero;
-    p.N = N;
-    p.N_pad = n_pad(N);
-    p.wsc = static_cast<float*>(wsc);
+    set_weight_job(&p, wq, w_scale, w_zero, N, K, static_cast<uint8_t*>(pw));
     return launch_pack(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
 }
 
-int w4a8_linear_prepared(const void* act, const uint8_t* wq, const void* wsc, const float* bias, float* y,
-                         int64_t M, int64_t N, int64_t K, void* stream) {
+int w4a8_linear_prepared(const void* act, const void* pw, const float* bias, float* y, int64_t M, int64_t N,
+                         int64_t K, void* stream) {
     int rc = check_shape(M, N, K);
     if (rc != W4A8_OK) return rc;
     if (M == 0 || N == 0) return W4A8_OK;
-    if (!act || !wq || !wsc || !y) return W4A8_ERR_ARG;
-    if (!aligned(act, 16) || !aligned(wq, 16) || !aligned(wsc, 16) || !aligned(y, 16) || (bias && !aligned(bias, 4)))
-        return W4A8_ERR_ALIGN;
+    if (!act || !pw || !y) return W4A8_ERR_ARG;
+    if (!aligned(act, 16) || !aligned(pw, 16) || !aligned(y, 16) || (bias && !aligned(bias, 4))) return W4A8_ERR_ALIGN;
     DeviceInfo* d = nullptr;
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
-    const ActLayout A = act_layout(M, K, true, true);
+    const ActLayout A = act_layout(M, K, true);
     const uint8_t* a = static_cast<const uint8_t*>(act);
-    return run_linear(a, A, reinterpret_cast<const float*>(a + A.s_a), static_cast<const float*>(wsc), wq, bias, y,
+    return run_linear(a + A.rec, reinterpret_cast<const float*>(a + A.s_a), static_cast<const uint8_t*>(pw), bias, y,
                       M, N, K, *d, static_cast<cudaStream_t>(stream));
 }
 
@@ -342,35 +299,36 @@ int w4a8_debug_block_acc(const int8_t* a_q, const uint8_t* wq, int64_t M, int64_
     if (!a_q || !wq || !acc) return W4A8_ERR_ARG;
     if (m0 < 0 || n0 < 0 || m_cnt <= 0 || n_cnt <= 0 || m0 + m_cnt > M || n0 + n_cnt > N) return W4A8_ERR_SHAPE;
     if (!aligned(a_q, 16) || !aligned(wq, 16) || !aligned(acc, 4)) return W4A8_ERR_ALIGN;
-    const ActLayout L = act_layout(m_cnt, K, false, false);
-    if (!workspace || workspace_bytes < L.total) return W4A8_ERR_WORKSPACE;
+    const ActLayout L = act_layout(m_cnt, K, false);
+    const WLayout W = w_layout(n_cnt, K);
+    if (!workspace || workspace_bytes < L.total + W.total) return W4A8_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return W4A8_ERR_ALIGN;
     DeviceInfo* d = nullptr;
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint8_t* wrec = ws + L.total;
+    // the window's token rows re-encoded, its weight rows expanded (no scales or zeros)
     PrepArgs p;
     p.a_q_in = a_q;
     p.M = m_cnt;
     p.K = K;
     p.row0 = m0;
-    p.apk = ws + L.apk;
+    p.trec = ws + L.rec;
+    p.wq = wq;
+    p.n_first = n0;
+    p.N = n_cnt;
+    p.wrec = wrec;
     if (launch_pack(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
-    GemmMaps maps;
-    const int tn = pick_token_tile(m_cnt, n_cnt, d->num_sms);
-    if (!make_map_u8(&maps.a, ws + L.apk, 2 * K, m_cnt, 2 * K, 128, tn, CU_TENSOR_MAP_SWIZZLE_128B))
-        return W4A8_ERR_CUDA;
-    if (!make_map_u8(&maps.b, wq, K / 2, N, K / 2, 32, kTileW, CU_TENSOR_MAP_SWIZZLE_NONE)) return W4A8_ERR_CUDA;
     GemmArgs g;
     g.M = m_cnt;
-    g.N = N;
+    g.N = n_cnt;
     g.K = K;
-    g.m_cnt = m_cnt;
-    g.n0 = n0;
-    g.n_cnt = n_cnt;
+    g.trec = ws + L.rec;
+    g.wrec = wrec;
     g.acc = acc;
     g.status = d->status;
-    return launch_gemm(maps, g, tn, true, st) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
+    return launch_gemm(g, true, d->num_sms, st) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
 }
 
 int w4a8_sync_status(void* stream) {

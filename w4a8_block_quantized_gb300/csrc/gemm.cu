@@ -3,9 +3,9 @@
 // "MNN LLM inference on the SpacemiT K3", section 3 eqs. (2)-(3) and section 4 steps 2-3.
 // There is no integer MMA kind on sm_103a, so the exact INT8 x U4 block products are
 // carried on the fp8 kind (tcgen05.mma kind::f8f6f4, E4M3 x E4M3 -> fp32 in TMEM):
-//   - a u4 weight code q, zero-extended to a byte, is exactly the e4m3 encoding of
-//     q * 2^-9 (the subnormal binade and the first normal binade share the step 2^-9), so
-//     the in-shared-memory unpack is two masks and two byte permutes per 8 weights;
+//   - the weights arrive expanded to one byte per u4 code q (the pre-pass does it), and
+//     that byte is exactly the e4m3 encoding of q * 2^-9 (the subnormal binade and the
+//     first normal binade share the step 2^-9);
 //   - activations arrive as the two nibble planes of eq. (3): e4m3(16*(a>>4)) and
 //     e4m3(a&15), both exact;
 //   - one 64-block = 4 MMAs of K = 32 (q x hi plane, then q x lo plane) into one TMEM
@@ -15,23 +15,39 @@
 //     K = 16, two live K slots): weights {-z_w, -z_w}, tokens {rh/8, rl/512} with the row
 //     sum rs = 64 rh + rl, all exact in fp16, so the accumulator ends the block holding
 //     (acc - z_w rs) * 2^-9;
-//   - every 64-block gets its own accumulator (ping-pong TMEM buffers), drained by the
-//     epilogue warps with one fma per output, y += (512 s_w) * D, and at the end
-//     y_out = fma(s_a, y, bias) is written straight to HBM.
+//   - every 64-block gets its own accumulator (four TMEM buffers of 128 columns), drained
+//     by the epilogue warps two blocks at a time with one fma per output and block,
+//     y += (512 s_w) * D; at the end of a tile y_out = fma(s_a, y, bias) goes straight
+//     to HBM.
 //
 // Orientation: the weights are the MMA's M = 128 operand (TMEM lanes = output columns n)
-// and the tokens its N operand (TN = 64..256 TMEM columns).  An epilogue thread then owns
-// four weight rows, so s_w is a per-thread scalar for a block and the epilogue reads no
-// per-column data at all.
+// and the tokens its N = 128 operand.  An epilogue thread owns one weight row (its TMEM
+// lane) and 32 token columns, so s_w is one scalar per thread and block.
 //
-// Warp roles (one CTA = one 128-weight x TN-token output tile, 20 warps):
-//   warp 0       TMA producer: token planes (128-byte swizzle), packed weights; bulk
-//                copies of the block's row-sum operand, weight zeros and weight scales
-//   warp 1       TMEM allocation + single-thread MMA issue
-//   warps 2-3    weight unpack u4 -> e4m3 into the 64-byte-swizzled K-major operand, and
-//                the weight zeros into the zero-point operand
-//   warps 4-19   epilogue: 4 warps per 32-lane TMEM quarter, a quarter of the columns each
-// Every wait is bounded (WaitCtl); a CTA that gives up records a timeout and unwinds.
+// Every operand of a (tile, 64-block) pair sits in one record written by the pre-pass in
+// shared-memory order (w4a8_internal.h): token planes + token zero-point rows, and e4m3
+// weights + weight zero-point rows + scales.  A pipeline stage holds two consecutive
+// blocks and is filled by two bulk copies: issuing an asynchronous copy or barrier
+// operation costs a thread on the order of a hundred cycles, so the copy count per block,
+// not the bytes, decides whether the producer keeps up with the tensor pipe.  The weight
+// scales stay out of the records: the epilogue loads them from memory one stage ahead, so
+// a stage is free as soon as its MMAs complete.
+//
+// Warp roles (one persistent CTA per SM walking 128 x 128 output tiles, 20 warps):
+//   warp 0       producer: two bulk copies per stage
+//   warps 1-3    MMA issue, one stage each in turn; one lane of the warp issues.  The
+//                issue cost of one thread's MMA sequence exceeds the tensor time of a
+//                stage, three warps' together do not.  Warp 1 also owns TMEM.
+//   warps 4-19   epilogue: 4 warps per 32-lane TMEM quarter, 32 of the 128 columns each;
+//                a stage's two blocks per drain keep four TMEM loads in flight per wait
+//
+// The barrier of a stage gates its MMAs: it completes once the stage's copies have landed
+// (producer arrival + transaction bytes) and the epilogue has released the two TMEM
+// buffers the stage overwrites (one arrival per epilogue warp), so an issuer waits once per
+// block.  The epilogue drains a stage's two blocks together (four TMEM loads in flight per
+// wait), releases their buffers as soon as the accumulators are in registers, then folds
+// them into y; it frees a stage once its accumulators are complete.  Every wait is bounded (WaitCtl); a CTA
+// that gives up records a timeout and unwinds.
 #include "sm103_ptx.cuh"
 #include "w4a8_internal.h"
 
@@ -40,50 +56,41 @@ namespace {
 
 constexpr int kThreads = 640;
 constexpr int kEpiWarps = 16;
+constexpr int kIssuers = 3;
+constexpr int kStages = 3;    // stages of two blocks
+constexpr int kNBuf = 4;      // TMEM accumulator buffers of kTileT columns (two per stage)
 constexpr uint32_t kLayoutSw128 = 2, kLayoutSw64 = 4;
-// Register split: launch = 640 x 96 (checked at build time); warps 0-3 drop to 48,
-// the 16 epilogue warps rise to 104: 128*48 + 512*104 = 59392 <= 61440.
-constexpr int kRegsLow = 48, kRegsHigh = 104;
+// Register split: launch = 640 x 96 (checked at build time); warps 0-3 drop to 32,
+// the 16 epilogue warps rise to 112: 128*32 + 512*112 = 61440 = 640*96.
+constexpr int kRegsLow = 32, kRegsHigh = 112;
 
-template <int TN>
-struct Cfg {
-    static constexpr int kStages = TN == 256 ? 4 : (TN == 128 ? 6 : 8);
-    static constexpr int kSc = kStages + 4;          // weight-scale ring (read by the epilogue)
-    static constexpr int kNBuf = TN == 256 ? 2 : 4;  // TMEM accumulator buffers
-    static constexpr int kTBytes = TN * 128;         // token planes of one block
-    static constexpr int kWunpBytes = kTileW * 64;   // unpacked weights of one block
-    static constexpr int kWpkBytes = kTileW * 32;    // packed weights of one block
-    static constexpr int kAxBytes = kTileW * 16;     // zero-point operand, weight side (K 0..7)
-    static constexpr int kBxBytes = TN * 16;         // zero-point operand, token side (K 0..7)
-    static constexpr int kZhBytes = kTileW * 4;      // {-z_w, -z_w} staging for the unpack warps
-    static constexpr int kZeroBytes = 4096;          // K 8..15 of both zero-point operands
-    static constexpr int kSBytes = kTileW * 4;       // 512 s_w of the tile's rows
-    static constexpr int kOffT = 0;
-    static constexpr int kOffWunp = kOffT + kStages * kTBytes;
-    static constexpr int kOffWpk = kOffWunp + kStages * kWunpBytes;
-    static constexpr int kOffAx = kOffWpk + kStages * kWpkBytes;
-    static constexpr int kOffBx = kOffAx + kStages * kAxBytes;
-    static constexpr int kOffZh = kOffBx + kStages * kBxBytes;
-    static constexpr int kOffZero = kOffZh + kStages * kZhBytes;
-    static constexpr int kOffSc = kOffZero + kZeroBytes;
-    static constexpr int kOffBar = kOffSc + kSc * kSBytes;
-    static constexpr int kNumBars = 3 * kStages + 2 * kSc + 2 * kNBuf + 1;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-    static constexpr uint32_t kTmemCols = kNBuf * TN;
-    static constexpr int kChunks = TN / 64;          // 16-column chunks per epilogue thread
-    static_assert(kOffWunp % 1024 == 0 && kOffWpk % 1024 == 0, "operand tiles must be 1024-aligned");
-    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-    static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation");
-    static_assert(kZeroBytes >= kAxBytes && kZeroBytes >= kBxBytes, "zero half of the zero-point operands");
-};
+constexpr int kStageTok = 2 * kTokRec;               // token records of a stage's two blocks
+constexpr int kStageBytes = kStageTok + 2 * kWRec;   // + weight records
+constexpr int kZeroBytes = 4096;                     // K 8..15 of both zero-point operands
+constexpr int kOffZero = kStages * kStageBytes;
+constexpr int kOffBar = kOffZero + kZeroBytes;
+constexpr int kNumBars = 2 * kStages + 2 + kIssuers;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+constexpr uint32_t kTmemCols = kNBuf * kTileT;
+static_assert(kTokRec % 1024 == 0 && kWRec % 1024 == 0 && kStageBytes % 1024 == 0,
+              "swizzled operand tiles must stay 1024-aligned");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kTmemCols == 512, "TMEM allocation");
+static_assert(kNBuf / 2 <= kStages, "a stage barrier carries a buffer release only after its previous phase");
+static_assert(kZeroBytes >= kTileW * 16 && kZeroBytes >= kTileT * 16, "zero half of the zero-point operands");
 
-// u4 pairs -> e4m3 bytes in k order: nibbles k0..k7 of w become bytes of (o0: k0..k3, o1: k4..k7).
-__device__ __forceinline__ void expand8(uint32_t w, uint32_t& o0, uint32_t& o1) {
-    const uint32_t lo = w & 0x0F0F0F0Fu;         // k0 k2 k4 k6
-    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;  // k1 k3 k5 k7
-    o0 = __byte_perm(lo, hi, 0x5140);
-    o1 = __byte_perm(lo, hi, 0x7362);
+// Grouped raster over the output tiles: groups of kGroup token tiles, the token tile
+// varying fastest inside a group, so the CTAs running at one time share token and weight
+// tiles in L2.
+constexpr int64_t kGroup = 8;
+__device__ __forceinline__ void tile_at(int64_t t, int64_t tiles_t, int64_t tiles_w, int64_t& tt, int64_t& tw) {
+    const int64_t per = kGroup * tiles_w;
+    const int64_t grp = t / per, r = t - grp * per;
+    const int64_t g0 = grp * kGroup;
+    const int64_t gsz = tiles_t - g0 < kGroup ? tiles_t - g0 : kGroup;
+    tt = g0 + r % gsz;
+    tw = r / gsz;
 }
 
 // Bounded wait that ignores the abort flag: used while unwinding to let copies and MMAs
@@ -96,73 +103,47 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
     }
 }
 
-// 16 TMEM lanes x (2 x 8) fp32 columns: thread t receives, for repeat j = 0..1,
-// r[4j+0..1] = lane (t/4), columns 8j + 2(t%4) + {0,1}; r[4j+2..3] = lane (t/4)+8.
-__device__ __forceinline__ void tmem_ld_16x256b_x2(uint32_t taddr, uint32_t (&r)[8]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-        : "r"(taddr)
-        : "memory");
-}
-
-template <int TN, bool DEBUG>
+template <bool DEBUG>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
-    using C = Cfg<TN>;
-    constexpr int S = C::kStages, SC = C::kSc, NB = C::kNBuf;
+    gemm_kernel(const GemmArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-    uint64_t* empty = full + S;
-    uint64_t* unp = empty + S;
-    uint64_t* scfull = unp + S;
-    uint64_t* scempty = scfull + SC;
-    uint64_t* tfull = scempty + SC;
-    uint64_t* tempty = tfull + NB;
-    uint64_t* drain = tempty + NB;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
+    uint64_t* empty = full + kStages;
+    uint64_t* tfull = empty + kStages;   // one per pair of TMEM buffers
+    uint64_t* drain = tfull + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t tiles_w = (args.n_cnt + kTileW - 1) / kTileW;
-    const int64_t tt = blockIdx.x / tiles_w, tw = blockIdx.x - tt * tiles_w;
-    const int64_t mt0 = tt * TN;                  // first token (operand row) of the tile
-    const int64_t nt0 = args.n0 + tw * kTileW;    // first weight row (output column) of the tile
-    const int nb = static_cast<int>(args.K / kBlock);
+    const int64_t tiles_t = (args.M + kTileT - 1) / kTileT;
+    const int64_t tiles_w = (args.N + kTileW - 1) / kTileW;
+    const int64_t ntiles = tiles_t * tiles_w;
+    const int64_t first = blockIdx.x;
+    // the host keeps ntiles * K/64 below 2^31, so the stage counters below fit 32 bits
+    const uint32_t my_tiles = ntiles > first ? static_cast<uint32_t>((ntiles - 1 - first) / gridDim.x + 1) : 0u;
+    const uint32_t nb = static_cast<uint32_t>(args.K / kBlock);
+    const uint32_t spt = (nb + 1) / 2;         // stages per tile
+    const uint32_t total = my_tiles * spt;     // stages of this CTA, counted across its tiles
     const WaitCtl ctl{abort_flag, args.status, args.wait_limit_ns};
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1 + kEpiWarps);
             mbar_init(&empty[s], 1);
-            mbar_init(&unp[s], 64);
         }
-        for (int c = 0; c < SC; ++c) {
-            mbar_init(&scfull[c], 1);
-            mbar_init(&scempty[c], kEpiWarps);
-        }
-        for (int i = 0; i < NB; ++i) {
-            mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], kEpiWarps);
-        }
-        mbar_init(drain, 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&tfull[i], 2);  // one commit per block slot
+        for (int i = 0; i < kIssuers; ++i) mbar_init(&drain[i], 1);
         *abort_flag = 0u;
         fence_barrier_init();
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
     }
     if (!DEBUG) {
-        // the zero-point operands: weight-side tiles (only their first 4 bytes per row are
-        // rewritten per block) and the shared zero K-half
-        for (int i = threadIdx.x; i < (C::kStages * C::kAxBytes) / 16; i += kThreads)
-            reinterpret_cast<uint4*>(smem + C::kOffAx)[i] = make_uint4(0u, 0u, 0u, 0u);
-        for (int i = threadIdx.x; i < C::kZeroBytes / 16; i += kThreads)
-            reinterpret_cast<uint4*>(smem + C::kOffZero)[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = threadIdx.x; i < kZeroBytes / 16; i += kThreads)
+            reinterpret_cast<uint4*>(smem + kOffZero)[i] = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, C::kTmemCols);
+        tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -173,204 +154,172 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 4) {
         regs_dec<kRegsLow>();
         if (warp == 0) {
-            // -------------------------------------------------------- TMA producer
+            // -------------------------------------------------------- producer
             if (lane == 0) {
-                int nA = 0, nS = 0;  // blocks whose operand / scale copies were issued
-                for (int b = 0; b < nb; ++b) {
-                    const int s = b % S, k = b / S;
-                    if (k > 0 && !mbar_wait(&empty[s], (k - 1) & 1, ctl)) break;
-                    const float* wrow = args.wsc + static_cast<int64_t>(b) * 2 * args.N_pad;
-                    mbar_arrive_expect_tx(&full[s], C::kTBytes + C::kWpkBytes +
-                                                        (DEBUG ? 0 : C::kBxBytes + C::kZhBytes));
-                    tma_load_2d(smem + C::kOffT + s * C::kTBytes, &tmA, &full[s], b * 128, static_cast<int32_t>(mt0));
-                    tma_load_2d(smem + C::kOffWpk + s * C::kWpkBytes, &tmB, &full[s], b * 32,
-                                static_cast<int32_t>(nt0));
-                    if (!DEBUG) {
-                        bulk_load(smem + C::kOffBx + s * C::kBxBytes, args.rx + static_cast<int64_t>(b) * args.M_pad + mt0,
-                                  C::kBxBytes, &full[s]);
-                        bulk_load(smem + C::kOffZh + s * C::kZhBytes,
-                                  reinterpret_cast<const uint32_t*>(wrow + args.N_pad) + nt0, C::kZhBytes, &full[s]);
-                    }
-                    nA = b + 1;
-                    if (!DEBUG) {
-                        const int c = b % SC, kc = b / SC;
-                        if (kc > 0 && !mbar_wait(&scempty[c], (kc - 1) & 1, ctl)) break;
-                        mbar_arrive_expect_tx(&scfull[c], C::kSBytes);
-                        bulk_load(smem + C::kOffSc + c * C::kSBytes, wrow + nt0, C::kSBytes, &scfull[c]);
-                        nS = b + 1;
+                uint32_t j = 0, issued = 0;  // stage counter; stages whose copies were issued
+                bool ok = true;
+                for (uint32_t i = 0; ok && i < my_tiles; ++i) {
+                    int64_t tt, tw;
+                    tile_at(first + static_cast<int64_t>(i) * gridDim.x, tiles_t, tiles_w, tt, tw);
+                    const uint8_t* tsrc = args.trec + static_cast<int64_t>(tt) * nb * kTokRec;
+                    const uint8_t* wsrc = args.wrec + static_cast<int64_t>(tw) * nb * kWRec;
+                    for (uint32_t p = 0; p < spt; ++p, ++j) {
+                        const int s = static_cast<int>(j % kStages);
+                        const uint32_t k = j / kStages;
+                        if (k > 0 && !mbar_wait(&empty[s], (k - 1) & 1, ctl)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t b0 = 2 * p, cnt = nb - b0 < 2 ? 1u : 2u;
+                        uint8_t* st = smem + s * kStageBytes;
+                        mbar_arrive_expect_tx(&full[s], cnt * (kTokRec + kWRec));
+                        bulk_load(st, tsrc + static_cast<int64_t>(b0) * kTokRec, cnt * kTokRec, &full[s]);
+                        bulk_load(st + kStageTok, wsrc + static_cast<int64_t>(b0) * kWRec, cnt * kWRec, &full[s]);
+                        issued = j + 1;
                     }
                 }
                 if (*abort_flag) {
                     // let every copy already issued land before the CTA exits
-                    for (int j = (nA > S ? nA - S : 0); j < nA; ++j) drain_wait(&full[j % S], (j / S) & 1, 100000000ull);
-                    for (int j = (nS > SC ? nS - SC : 0); j < nS; ++j)
-                        drain_wait(&scfull[j % SC], (j / SC) & 1, 100000000ull);
+                    for (uint32_t q = (issued > kStages ? issued - kStages : 0); q < issued; ++q)
+                        drain_wait(&full[q % kStages], (q / kStages) & 1, 100000000ull);
                 }
-            }
-        } else if (warp == 1) {
-            // -------------------------------------------------------- MMA issuer
-            // The wait for block b+1's operands is taken while block b's last MMAs are
-            // still queued on the tensor pipe, so the barrier latency does not leave the
-            // pipe idle between blocks.  (The wait for a drained TMEM buffer stays at the
-            // start of each block: taken early it would tie block b's MMAs to the drain of
-            // block b-1.)  The unpack warps arrive on unp[s] only after they observed
-            // full[s], so unp[s] also covers the TMA data of the stage.
-            if (lane == 0) {
-                constexpr uint32_t idesc = idesc_e4m3_f32(kTileW, TN);
-                // Descriptors of stage 0; stage s adds s * (tile bytes >> 4) to the start-address
-                // field, and a K offset of 32 bytes adds 2.  The field never overflows: every
-                // shared-memory address is below 2^18.
-                const uint32_t zr = smem_u32(smem + C::kOffZero);
-                const uint32_t ax0 = smem_u32(smem + C::kOffAx), bx0 = smem_u32(smem + C::kOffBx);
-                const uint64_t dW0 = smem_desc(smem_u32(smem + C::kOffWunp), 512, kLayoutSw64);
-                const uint64_t dT0 = smem_desc(smem_u32(smem + C::kOffT), 1024, kLayoutSw128);
-                const uint64_t dAx0 = smem_desc(ax0, 128, 0, zr - ax0);
-                const uint64_t dBx0 = smem_desc(bx0, 128, 0, zr - bx0);
-                auto ready = [&](int b) -> bool { return mbar_wait(&unp[b % S], (b / S) & 1, ctl); };
-                bool ok = nb > 0 && ready(0);
-                for (int b = 0; ok && b < nb; ++b) {
-                    const int s = b % S, buf = b % NB, u = b / NB;
-                    if (u > 0 && !mbar_wait(&tempty[buf], (u - 1) & 1, ctl)) break;
-                    tc_fence_after();
-                    const uint32_t d = tmem_base + static_cast<uint32_t>(buf * TN);
-                    const uint64_t dW = dW0 + static_cast<uint64_t>(s * (C::kWunpBytes >> 4));
-                    const uint64_t dT = dT0 + static_cast<uint64_t>(s * (C::kTBytes >> 4));
-                    // q x hi plane (K 0..31, 32..63), then q x lo plane
-                    mma_f8f6f4(d, dW, dT, idesc, 0u);
-                    mma_f8f6f4(d, dW + 2, dT + 2, idesc, 1u);
-                    mma_f8f6f4(d, dW, dT + 4, idesc, 1u);
-                    if (b + 1 < nb) ok = ready(b + 1);
-                    mma_f8f6f4(d, dW + 2, dT + 6, idesc, 1u);
-                    if (!DEBUG) {
-                        // zero-point term: {-z, -z} x {rh/8, rl/512}; K 8..15 from the zero block
-                        // (each stage's leading byte offset shrinks as its start address grows)
-                        const uint64_t ax = static_cast<uint64_t>(s * (C::kAxBytes >> 4));
-                        const uint64_t bx = static_cast<uint64_t>(s * (C::kBxBytes >> 4));
-                        mma_f16(d, dAx0 + ax - (ax << 16), dBx0 + bx - (bx << 16), idesc, 1u);
-                    }
-                    mma_commit(&empty[s]);
-                    mma_commit(&tfull[buf]);
-                }
-                mma_commit(drain);
-                drain_wait(drain, 0, 100000000ull);
             }
         } else {
-            // -------------------------------------------------------- weight unpack
-            const int ut = threadIdx.x - 64;
-            for (int b = 0; b < nb; ++b) {
-                const int s = b % S, k = b / S;
-                if (!mbar_wait(&full[s], k & 1, ctl)) break;
-                const uint8_t* src = smem + C::kOffWpk + s * C::kWpkBytes;
-                uint8_t* dst = smem + C::kOffWunp + s * C::kWunpBytes;
-#pragma unroll
-                for (int j = 0; j < (kTileW * 2) / 64; ++j) {
-                    const int c = ut + 64 * j;  // 16-byte chunk of the packed tile
-                    const int row = c >> 1, half = c & 1;
-                    const uint4 w = *reinterpret_cast<const uint4*>(src + c * 16);
-                    uint4 o0, o1;
-                    expand8(w.x, o0.x, o0.y);
-                    expand8(w.y, o0.z, o0.w);
-                    expand8(w.z, o1.x, o1.y);
-                    expand8(w.w, o1.z, o1.w);
-                    const int sw = (row >> 1) & 3;  // 64-byte swizzle: chunk ^= address bits 7..8
-                    *reinterpret_cast<uint4*>(dst + row * 64 + (((2 * half) ^ sw) << 4)) = o0;
-                    *reinterpret_cast<uint4*>(dst + row * 64 + (((2 * half + 1) ^ sw) << 4)) = o1;
+            // -------------------------------------------------------- MMA issue (warps 1-3)
+            const int iw = warp - 1;
+            constexpr uint32_t idesc = idesc_e4m3_f32(kTileW, kTileT);
+            // Descriptors of stage 0, slot 0; a record at byte offset o adds o >> 4 to the
+            // start-address field, and a K offset of 32 bytes adds 2.  The field never
+            // overflows: every shared-memory address is below 2^18.  The zero-point operands
+            // take K 8..15 from the zero block, one leading byte offset away, which shrinks
+            // as the start address grows.
+            const uint32_t zr = smem_u32(smem + kOffZero);
+            const uint32_t t0a = smem_u32(smem), w0a = smem_u32(smem + kStageTok);
+            const uint64_t dT0 = smem_desc(t0a, 1024, kLayoutSw128);
+            const uint64_t dW0 = smem_desc(w0a, 512, kLayoutSw64);
+            const uint64_t dBx0 = smem_desc(t0a + kTokRx, 128, 0, zr - (t0a + kTokRx));
+            const uint64_t dAx0 = smem_desc(w0a + kWZx, 128, 0, zr - (w0a + kWZx));
+            // Work item i = 2 j + k is block slot k of stage j; warp 1 + (i % 3) issues it, so the
+            // two blocks of a stage go out from two warps at once.  Stage j accumulates in the
+            // TMEM buffer pair j % 2 (slot k in buffer 2 (j % 2) + k).
+            for (uint32_t i = iw; i < 2 * total; i += kIssuers) {
+                const uint32_t j = i >> 1, k = i & 1u;
+                const int s = static_cast<int>(j % kStages);
+                const uint32_t pair = j & 1u;
+                const uint32_t b0 = 2 * (j % spt), cnt = nb - b0 < 2 ? 1u : 2u;
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (j / kStages) & 1, ctl))) break;
+                tc_fence_after();
+                if (elect_one()) {
+                    if (k < cnt) {
+                        const uint32_t d = tmem_base + (2 * pair + k) * kTileT;
+                        const uint64_t ot = static_cast<uint64_t>((s * kStageBytes + static_cast<int>(k) * kTokRec) >> 4);
+                        const uint64_t ow = static_cast<uint64_t>((s * kStageBytes + static_cast<int>(k) * kWRec) >> 4);
+                        const uint64_t dT = dT0 + ot, dW = dW0 + ow;
+                        // q x hi plane (K 0..31, 32..63), then q x lo plane
+                        mma_f8f6f4(d, dW, dT, idesc, 0u);
+                        mma_f8f6f4(d, dW + 2, dT + 2, idesc, 1u);
+                        mma_f8f6f4(d, dW, dT + 4, idesc, 1u);
+                        mma_f8f6f4(d, dW + 2, dT + 6, idesc, 1u);
+                        // zero-point term: {-z, -z} x {rh/8, rl/512}
+                        if (!DEBUG) mma_f16(d, dAx0 + ow - (ow << 16), dBx0 + ot - (ot << 16), idesc, 1u);
+                    }
+                    // a stage's accumulators are complete once both slots' commits have arrived
+                    // (a slot without a block commits at once)
+                    mma_commit(&tfull[pair]);
                 }
-                if (!DEBUG) {
-                    // {-z, -z} into K 0..1 of the weight-side zero-point operand (core matrix
-                    // rows of 16 bytes, 8-row groups 128 bytes apart)
-                    const uint32_t* zh = reinterpret_cast<const uint32_t*>(smem + C::kOffZh + s * C::kZhBytes);
-                    uint8_t* ax = smem + C::kOffAx + s * C::kAxBytes;
-#pragma unroll
-                    for (int r = ut; r < kTileW; r += 64) *reinterpret_cast<uint32_t*>(ax + r * 16) = zh[r];
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&unp[s]);
+                __syncwarp();
             }
+            // this warp's MMAs complete before the CTA releases TMEM
+            if (elect_one()) mma_commit(&drain[iw]);
+            __syncwarp();
+            drain_wait(&drain[iw], 0, 100000000ull);
         }
     } else {
         // ------------------------------------------------------------ epilogue
         regs_inc<kRegsHigh>();
-        constexpr int CH = C::kChunks;
         const int q = warp & 3, h = (warp - 4) >> 2;  // TMEM lane quarter, column quarter
-        const int r8 = lane >> 2, cp = lane & 3;
-        float2 yv[4][CH][2];
+        const int row = q * 32 + lane;                // this thread's weight row in the tile
+        const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 32);
+        // the TMEM buffers start free: release the first two stages
+        if (lane == 0)
+            for (uint32_t q0 = 0; q0 < 2 && q0 < total; ++q0) mbar_arrive(&full[q0]);
+        uint32_t j = 0;  // stage counter of this CTA
+        bool ok = true;
+        for (uint32_t i = 0; ok && i < my_tiles; ++i) {
+            int64_t tt, tw;
+            tile_at(first + static_cast<int64_t>(i) * gridDim.x, tiles_t, tiles_w, tt, tw);
+            const int64_t mt0 = tt * kTileT + h * 32;  // first token column of this warp
+            const int64_t n = tw * kTileW + row;       // this thread's weight row
+            // this row's scales, block after block; each stage's pair is loaded one stage ahead
+            const float* sct = DEBUG ? nullptr : args.sc + static_cast<int64_t>(tw) * nb * kTileW + row;
+            float ns0 = 0.0f, ns1 = 0.0f;
+            if (!DEBUG) {
+                ns0 = __ldg(sct);
+                if (nb > 1) ns1 = __ldg(sct + kTileW);
+            }
+            float y[32];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int ch = 0; ch < CH; ++ch) yv[i][ch][0] = yv[i][ch][1] = make_float2(0.f, 0.f);
-        const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        for (int b = 0; b < nb; ++b) {
-            const int buf = b % NB, u = b / NB;
-            const int c = b % SC, kc = b / SC;
-            if (!mbar_wait(&tfull[buf], u & 1, ctl)) break;
-            if (!DEBUG && !mbar_wait(&scfull[c], kc & 1, ctl)) break;
-            tc_fence_after();
-            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (!DEBUG) s4 = *reinterpret_cast<const float4*>(smem + C::kOffSc + c * C::kSBytes + (q * 32 + r8 * 4) * 4);
-            const float sr[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-            for (int ch = 0; ch < CH; ++ch) {
-                const int col0 = h * (TN / 4) + ch * 16;  // token column within the tile
-                uint32_t v0[8], v1[8];
-                const uint32_t ta = lane_addr + static_cast<uint32_t>(buf * TN + col0);
-                tmem_ld_16x256b_x2(ta, v0);                 // weight rows r8, r8 + 8 of the quarter
-                tmem_ld_16x256b_x2(ta + (16u << 16), v1);   // weight rows r8 + 16, r8 + 24
+            for (int c = 0; c < 32; ++c) y[c] = 0.0f;
+            for (uint32_t p = 0; p < spt; ++p, ++j) {
+                const int s = static_cast<int>(j % kStages);
+                const bool two = 2 * p + 1 < nb;
+                const float s0 = ns0, s1 = ns1;
+                if (!DEBUG && p + 1 < spt) {
+                    ns0 = __ldg(sct + (2 * p + 2) * kTileW);
+                    ns1 = 2 * p + 3 < nb ? __ldg(sct + (2 * p + 3) * kTileW) : 0.0f;
+                }
+                const uint32_t pair = j & 1u, b0 = 2 * pair, b1 = b0 + 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(&tfull[pair], (j >> 1) & 1, ctl))) {
+                    ok = false;
+                    break;
+                }
+                // the stage's MMAs are complete: its operands are no longer needed
+                if (warp == 4 && lane == 0) mbar_arrive(&empty[s]);
+                tc_fence_after();
+                uint32_t v[64];
+                tmem_ld_32x32b_x16(tl + b0 * kTileT, v);
+                tmem_ld_32x32b_x16(tl + b0 * kTileT + 16, v + 16);
+                if (two) {
+                    tmem_ld_32x32b_x16(tl + b1 * kTileT, v + 32);
+                    tmem_ld_32x32b_x16(tl + b1 * kTileT + 16, v + 48);
+                }
                 tmem_wait_ld();
+                // the accumulators are in registers: the buffers are free for the stage two later
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0 && j + 2 < total) mbar_arrive(&full[(j + 2) % kStages]);
+                if (DEBUG) {
+                    if (n < args.N) {
 #pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    const float2 a2[4] = {
-                        make_float2(__uint_as_float(v0[4 * g + 0]), __uint_as_float(v0[4 * g + 1])),
-                        make_float2(__uint_as_float(v0[4 * g + 2]), __uint_as_float(v0[4 * g + 3])),
-                        make_float2(__uint_as_float(v1[4 * g + 0]), __uint_as_float(v1[4 * g + 1])),
-                        make_float2(__uint_as_float(v1[4 * g + 2]), __uint_as_float(v1[4 * g + 3]))};
-                    if (DEBUG) {
-                        const int64_t m = mt0 + col0 + 8 * g + 2 * cp;  // token (window row)
+                        for (int e = 0; e < 2; ++e) {
+                            if (e == 1 && !two) break;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int64_t n = nt0 + q * 32 + r8 + 8 * i;  // weight row
-                            if (n < args.n0 + args.n_cnt) {
-                                int32_t* dst = args.acc + (m * args.n_cnt + (n - args.n0)) * nb + b;
-                                if (m < args.m_cnt) dst[0] = static_cast<int32_t>(a2[i].x * 512.0f);
-                                if (m + 1 < args.m_cnt) dst[args.n_cnt * nb] = static_cast<int32_t>(a2[i].y * 512.0f);
+                            for (int c = 0; c < 32; ++c) {
+                                const int64_t m = mt0 + c;
+                                if (m < args.M)
+                                    args.acc[(m * args.N + n) * nb + 2 * p + e] =
+                                        static_cast<int32_t>(__uint_as_float(v[32 * e + c]) * 512.0f);
                             }
                         }
-                    } else {
+                    }
+                } else {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) yv[i][ch][g] = __ffma2_rn(make_float2(sr[i], sr[i]), a2[i], yv[i][ch][g]);
+                    for (int c = 0; c < 32; ++c) y[c] = fmaf(s0, __uint_as_float(v[c]), y[c]);
+                    if (two) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) y[c] = fmaf(s1, __uint_as_float(v[32 + c]), y[c]);
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&tempty[buf]);
-                if (!DEBUG) mbar_arrive(&scempty[c]);
+            if (!ok) break;
+            if (!DEBUG && n < args.N) {
+                const float bn = args.bias ? args.bias[n] : 0.0f;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int64_t m = mt0 + c;
+                    if (m < args.M) args.y[m * args.N + n] = fmaf(args.s_a[m], y[c], bn);
+                }
             }
-        }
-        if (!DEBUG && !*abort_flag) {
-            float bias_r[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int64_t n = nt0 + q * 32 + r8 + 8 * i;
-                bias_r[i] = (args.bias && n < args.N) ? args.bias[n] : 0.0f;
-            }
-#pragma unroll
-            for (int ch = 0; ch < CH; ++ch)
-#pragma unroll
-                for (int g = 0; g < 2; ++g)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int64_t m = mt0 + h * (TN / 4) + ch * 16 + 8 * g + 2 * cp + e;
-                        if (m >= args.M) continue;
-                        const float sa = args.s_a[m];
-                        float* yrow = args.y + m * args.N;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int64_t n = nt0 + q * 32 + r8 + 8 * i;
-                            if (n < args.N) yrow[n] = fmaf(sa, e ? yv[i][ch][g].y : yv[i][ch][g].x, bias_r[i]);
-                        }
-                    }
         }
     }
 
@@ -379,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::kTmemCols);
+        tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -398,50 +347,27 @@ __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
     __syncthreads();
 }
 
-template <int TN, bool DEBUG>
-cudaError_t run(const GemmMaps& maps, const GemmArgs& a, cudaStream_t s) {
-    using C = Cfg<TN>;
+template <bool DEBUG>
+cudaError_t run(const GemmArgs& a, int num_sms, cudaStream_t s) {
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<TN, DEBUG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<DEBUG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    const int64_t tiles = ((a.m_cnt + TN - 1) / TN) * ((a.n_cnt + kTileW - 1) / kTileW);
-    gemm_kernel<TN, DEBUG><<<static_cast<unsigned>(tiles), kThreads, C::kSmemBytes, s>>>(maps.a, maps.b, a);
+    const int64_t tiles = ((a.M + kTileT - 1) / kTileT) * ((a.N + kTileW - 1) / kTileW);
+    const int64_t grid = tiles < num_sms ? tiles : num_sms;
+    gemm_kernel<DEBUG><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-int pick_token_tile(int64_t m_cnt, int64_t n_cnt, int num_sms) {
-    // Estimated time ~ waves * (TN + fixed per-tile cost); ties go to the wider tile.
-    int best = 256;
-    int64_t best_cost = -1;
-    const int cands[3] = {256, 128, 64};
-    const int64_t tiles_w = (n_cnt + kTileW - 1) / kTileW;
-    for (int tn : cands) {
-        const int64_t tiles = ((m_cnt + tn - 1) / tn) * tiles_w;
-        const int64_t waves = (tiles + num_sms - 1) / num_sms;
-        const int64_t cost = waves * (tn + 48);
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best = tn;
-        }
-    }
-    return best;
-}
-
-cudaError_t launch_gemm(const GemmMaps& maps, const GemmArgs& a, int tn, bool debug, cudaStream_t s) {
-    switch (tn) {
-        case 256: return debug ? run<256, true>(maps, a, s) : run<256, false>(maps, a, s);
-        case 128: return debug ? run<128, true>(maps, a, s) : run<128, false>(maps, a, s);
-        case 64: return debug ? run<64, true>(maps, a, s) : run<64, false>(maps, a, s);
-        default: return cudaErrorInvalidValue;
-    }
+cudaError_t launch_gemm(const GemmArgs& a, bool debug, int num_sms, cudaStream_t s) {
+    if (num_sms < 1) return cudaErrorInvalidValue;
+    return debug ? run<true>(a, num_sms, s) : run<false>(a, num_sms, s);
 }
 
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s) {

@@ -11,8 +11,9 @@
 //   - the tensor-core layout of the fused call: per row and 64-block the two e4m3
 //     nibble planes of section 3 eq. (3) (16*(a>>4) and a&15), s_a, and the row sums
 //     as the operand of the zero-point MMA.
-// The same launch also re-lays out the fp16 weight scales and zeros for the epilogue
-// (extra CTAs), so a call costs two launches in total.
+// The same launch also prepares the weight side in its extra CTAs (the u4 codes expanded
+// to the GEMM's e4m3 operand, the fp16 scales and zeros laid out for the epilogue and the
+// zero-point MMA), so a call costs two launches in total.
 #include "sm103_ptx.cuh"
 #include "w4a8_internal.h"
 
@@ -46,10 +47,16 @@ __device__ __forceinline__ uint4 rx_entry(int rs) {
     return make_uint4(*reinterpret_cast<const uint32_t*>(&p), 0u, 0u, 0u);
 }
 
-// Position of weight row n in a prepared-scale row (see the wsc layout in w4a8_internal.h).
-__device__ __forceinline__ int64_t perm32(int64_t n) {
-    const int r = static_cast<int>(n & 31);
-    return (n & ~static_cast<int64_t>(31)) + ((r & 7) << 2) + (r >> 3);
+// Token record of row m, block b (the layout in w4a8_internal.h).
+__device__ __forceinline__ uint8_t* token_rec(uint8_t* trec, int64_t m, int64_t b, int64_t nb) {
+    return trec + ((m >> 7) * nb + b) * kTokRec;
+}
+
+// Byte offset, inside a token record, of the 4 codes k = 4j .. 4j+3 of the block (j < 16) of
+// row r in plane p (0 = high nibbles, 1 = low nibbles): 128-byte swizzle of 16-byte chunks.
+__device__ __forceinline__ int plane_off(int r, int j, int p) {
+    const int c = (j >> 2) + 4 * p;
+    return r * 128 + ((c ^ (r & 7)) << 4) + ((j & 3) << 2);
 }
 
 // INT8 code of one activation: clamp(round_half_away(x / s), -127, 127), fp32 IEEE division.
@@ -125,25 +132,60 @@ __device__ __forceinline__ uint32_t bytes4f(float4 q) {
 
 __device__ __forceinline__ float h2f(uint16_t bits) { return __half2float(__ushort_as_half(bits)); }
 
-// Weight-scale job: per block b, 512 s_w[n,b] (fp32, rows permuted by perm32; the power
-// of two undoes the 2^-9 scale of the e4m3 weight operand) and {-z_w, -z_w} (fp16x2, row
-// order) for the zero-point MMA; zeros past N.
-__device__ void scales_job(const PrepArgs& a, int64_t cta, int64_t ctas) {
+// u4 pairs -> bytes in k order: nibbles k0..k7 of w become bytes of (o0: k0..k3, o1: k4..k7).
+// A byte holding the code q is the e4m3 encoding of q * 2^-9, the GEMM's weight operand.
+__device__ __forceinline__ void expand8(uint32_t w, uint32_t& o0, uint32_t& o1) {
+    const uint32_t lo = w & 0x0F0F0F0Fu;         // k0 k2 k4 k6
+    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;  // k1 k3 k5 k7
+    o0 = __byte_perm(lo, hi, 0x5140);
+    o1 = __byte_perm(lo, hi, 0x7362);
+}
+
+// Weight job (the weight records of w4a8_internal.h), spread over the CTAs past the row
+// CTAs.  One thread per (row n, block b), rows padded to a multiple of 128: the 32 packed
+// bytes expanded to 64 e4m3 bytes in 64-byte-swizzled order; then {-z_w, -z_w} (fp16 pair,
+// exact) with 12 zero bytes, and 512 s_w[n,b] (fp32, into the scale array; the power of two
+// undoes the 2^-9 scale of the e4m3 weight operand); zeros for rows past N.
+__device__ void weights_job(const PrepArgs& a, int64_t cta, int64_t ctas) {
     const int64_t nb = a.K / kBlock;
-    const int64_t total = nb * a.N_pad;
-    for (int64_t i = cta * blockDim.x + threadIdx.x; i < total; i += ctas * blockDim.x) {
-        const int64_t b = i / a.N_pad;
-        const int64_t n = i - b * a.N_pad;
-        float sv = 0.0f;
-        uint32_t zz = 0u;
+    const int64_t tiles = (a.N + kTileW - 1) / kTileW;
+    const int64_t total = tiles * nb * kTileW;
+    const int64_t stride = ctas * blockDim.x;
+    for (int64_t i = cta * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int64_t rb = i >> 7;  // record index: tile * nb + b
+        const int r = static_cast<int>(i & 127);
+        const int64_t n = (rb / nb) * kTileW + r;
+        const int64_t b = rb - (rb / nb) * nb;
+        uint8_t* rec = a.wrec + rb * kWRec;
+        uint4 o[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
+                      make_uint4(0u, 0u, 0u, 0u)};
         if (n < a.N) {
-            sv = 512.0f * h2f(a.s_w[n * nb + b]);
-            const uint32_t zb = static_cast<uint32_t>(a.z_w[n * nb + b]) ^ 0x8000u;  // -z_w, exact
-            zz = zb | (zb << 16);
+            const uint4* src = reinterpret_cast<const uint4*>(a.wq + (a.n_first + n) * (a.K / 2) + b * 32);
+            const uint4 w0 = __ldcs(src), w1 = __ldcs(src + 1);
+            expand8(w0.x, o[0].x, o[0].y);
+            expand8(w0.y, o[0].z, o[0].w);
+            expand8(w0.z, o[1].x, o[1].y);
+            expand8(w0.w, o[1].z, o[1].w);
+            expand8(w1.x, o[2].x, o[2].y);
+            expand8(w1.y, o[2].z, o[2].w);
+            expand8(w1.z, o[3].x, o[3].y);
+            expand8(w1.w, o[3].z, o[3].w);
         }
-        float* row = a.wsc + b * 2 * a.N_pad;
-        row[perm32(n)] = sv;
-        reinterpret_cast<uint32_t*>(row + a.N_pad)[n] = zz;
+        const int sw = (r >> 1) & 3;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(rec + r * 64 + ((c ^ sw) << 4)) = o[c];
+        if (a.s_w) {
+            float sv = 0.0f;
+            uint32_t zz = 0u;
+            if (n < a.N) {
+                const int64_t src = (a.n_first + n) * nb + b;
+                sv = 512.0f * h2f(a.s_w[src]);
+                const uint32_t zb = static_cast<uint32_t>(a.z_w[src]) ^ 0x8000u;  // -z_w, exact
+                zz = zb | (zb << 16);
+            }
+            *reinterpret_cast<uint4*>(rec + kWZx + r * 16) = make_uint4(zz, 0u, 0u, 0u);
+            a.sc[i] = sv;  // [tile][b][r]: the same linear index as the thread's item
+        }
     }
 }
 
@@ -152,7 +194,7 @@ __device__ void scales_job(const PrepArgs& a, int64_t cta, int64_t ctas) {
 template <int G, int V, bool PLANES>
 __global__ void __launch_bounds__(256, 2) quant_kernel(const PrepArgs a, int row_ctas) {
     if (static_cast<int>(blockIdx.x) >= row_ctas) {
-        if (a.wsc) scales_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
+        if (a.wrec) weights_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
         return;
     }
     constexpr bool kPrefetch = V <= 8;
@@ -220,9 +262,10 @@ __global__ void __launch_bounds__(256, 2) quant_kernel(const PrepArgs a, int row
                     if (PLANES) {
                         uint32_t hi, lo;
                         planes4f(q[j], hi, lo);
-                        uint8_t* dst = a.apk + m * (2 * K) + (f >> 4) * 128 + ((f & 15) << 2);
-                        *reinterpret_cast<uint32_t*>(dst) = hi;
-                        *reinterpret_cast<uint32_t*>(dst + 64) = lo;
+                        uint8_t* rec = token_rec(a.trec, m, f >> 4, nb);
+                        const int row = static_cast<int>(m & 127), j = static_cast<int>(f & 15);
+                        *reinterpret_cast<uint32_t*>(rec + plane_off(row, j, 0)) = hi;
+                        *reinterpret_cast<uint32_t*>(rec + plane_off(row, j, 1)) = lo;
                     } else {
                         *reinterpret_cast<uint32_t*>(a.a_q_out + m * K + 4 * f) = bytes4f(q[j]);
                     }
@@ -239,7 +282,8 @@ __global__ void __launch_bounds__(256, 2) quant_kernel(const PrepArgs a, int row
                     if (f < n4) {
                         const int64_t b = f >> 4;
                         const int rs = static_cast<int>(part[j]);
-                        if (PLANES) a.rx[b * a.M_pad + m] = rx_entry(rs);
+                        if (PLANES)
+                            *reinterpret_cast<uint4*>(token_rec(a.trec, m, b, nb) + kTokRx + (m & 127) * 16) = rx_entry(rs);
                         else a.rs_out[m * nb + b] = rs;
                     }
                 }
@@ -259,7 +303,7 @@ __global__ void __launch_bounds__(256, 2) quant_kernel(const PrepArgs a, int row
 template <bool PLANES>
 __global__ void __launch_bounds__(256) quant_long_kernel(const PrepArgs a, int row_ctas) {
     if (static_cast<int>(blockIdx.x) >= row_ctas) {
-        if (a.wsc) scales_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
+        if (a.wrec) weights_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
         return;
     }
     __shared__ float red[8];
@@ -305,10 +349,11 @@ __global__ void __launch_bounds__(256) quant_long_kernel(const PrepArgs a, int r
                 if (PLANES) {
                     uint32_t hi, lo;
                     planes4(c0, c1, c2, c3, hi, lo);
-                    uint8_t* dst = a.apk + m * (2 * K) + b * 128 + ((f & 15) << 2);
-                    *reinterpret_cast<uint32_t*>(dst) = hi;
-                    *reinterpret_cast<uint32_t*>(dst + 64) = lo;
-                    if ((lane & 15) == 0) a.rx[b * a.M_pad + m] = rx_entry(part);
+                    uint8_t* rec = token_rec(a.trec, m, b, nb);
+                    const int r = static_cast<int>(m & 127), j = static_cast<int>(f & 15);
+                    *reinterpret_cast<uint32_t*>(rec + plane_off(r, j, 0)) = hi;
+                    *reinterpret_cast<uint32_t*>(rec + plane_off(r, j, 1)) = lo;
+                    if ((lane & 15) == 0) *reinterpret_cast<uint4*>(rec + kTokRx + r * 16) = rx_entry(part);
                 } else {
                     const uint32_t w = (c0 & 0xff) | ((c1 & 0xff) << 8) | ((c2 & 0xff) << 16) |
                                        (static_cast<uint32_t>(c3 & 0xff) << 24);
@@ -324,7 +369,7 @@ __global__ void __launch_bounds__(256) quant_long_kernel(const PrepArgs a, int r
 // re-lay out the weight scales.  Rows row0 .. row0 + M - 1 of a_q_in.
 __global__ void __launch_bounds__(256) pack_kernel(const PrepArgs a, int row_ctas) {
     if (static_cast<int>(blockIdx.x) >= row_ctas) {
-        if (a.wsc) scales_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
+        if (a.wrec) weights_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
         return;
     }
     const int64_t K = a.K, nb = K / kBlock, c16 = K / 16;
@@ -342,25 +387,29 @@ __global__ void __launch_bounds__(256) pack_kernel(const PrepArgs a, int row_cta
             planes4(static_cast<int8_t>(u & 0xff), static_cast<int8_t>((u >> 8) & 0xff),
                     static_cast<int8_t>((u >> 16) & 0xff), static_cast<int8_t>(u >> 24), hi[j], lo[j]);
         }
-        const int64_t b = c >> 2;
-        uint8_t* dst = a.apk + m * (2 * K) + b * 128 + ((c & 3) << 4);
-        *reinterpret_cast<uint4*>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(dst + 64) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        uint8_t* rec = token_rec(a.trec, m, c >> 2, nb);
+        const int r = static_cast<int>(m & 127), j4 = static_cast<int>(c & 3);
+        *reinterpret_cast<uint4*>(rec + r * 128 + ((j4 ^ (r & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(rec + r * 128 + (((j4 + 4) ^ (r & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    if (a.rs_in && a.rx) {
+    if (a.rs_in) {
         const int64_t tot = a.M * nb;
         for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < tot; i += stride) {
-            const int64_t b = i / a.M, m = i - b * a.M;
-            a.rx[b * a.M_pad + m] = rx_entry(a.rs_in[(a.row0 + m) * nb + b]);
+            const int64_t m = i / nb, b = i - m * nb;
+            *reinterpret_cast<uint4*>(token_rec(a.trec, m, b, nb) + kTokRx + (m & 127) * 16) =
+                rx_entry(a.rs_in[(a.row0 + m) * nb + b]);
         }
     }
 }
 
-int scale_ctas(const PrepArgs& a) {
-    if (!a.wsc) return 0;
-    const int64_t total = (a.K / kBlock) * a.N_pad;
-    const int64_t c = (total + 255) / 256;
-    return static_cast<int>(c < 304 ? c : 304);
+// CTAs for the weight job: one (row, block) item per thread up to eight CTAs per SM, then
+// a few items per thread (each item is an independent 32-byte read, so many threads in
+// flight hide the latency).
+int weight_ctas(const PrepArgs& a) {
+    if (!a.wrec) return 0;
+    const int64_t items = ((a.N + kTileW - 1) / kTileW) * (a.K / kBlock) * kTileW;
+    const int64_t c = (items + 255) / 256;
+    return static_cast<int>(c < 152 * 8 ? c : 152 * 8);
 }
 
 template <int G, int V, bool PLANES>
@@ -368,7 +417,7 @@ cudaError_t run_quant(const PrepArgs& a, cudaStream_t s) {
     constexpr int RPC = 8 / G;
     const int64_t need = (a.M + RPC - 1) / RPC;
     const int row_ctas = static_cast<int>(need < 152 * 8 ? need : 152 * 8);
-    const int grid = row_ctas + scale_ctas(a);
+    const int grid = row_ctas + weight_ctas(a);
     quant_kernel<G, V, PLANES><<<grid, 256, 0, s>>>(a, row_ctas);
     return cudaGetLastError();
 }
@@ -386,14 +435,14 @@ cudaError_t dispatch_quant(const PrepArgs& a, cudaStream_t s) {
     if (n4 <= 256 * 8) return run_quant<8, 8, PLANES>(a, s);
     if (n4 <= 256 * 16) return run_quant<8, 16, PLANES>(a, s);
     const int row_ctas = static_cast<int>(a.M < 152 * 4 ? a.M : 152 * 4);
-    quant_long_kernel<PLANES><<<row_ctas + scale_ctas(a), 256, 0, s>>>(a, row_ctas);
+    quant_long_kernel<PLANES><<<row_ctas + weight_ctas(a), 256, 0, s>>>(a, row_ctas);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_quant(const PrepArgs& a, cudaStream_t s) {
-    return a.apk ? dispatch_quant<true>(a, s) : dispatch_quant<false>(a, s);
+    return a.trec ? dispatch_quant<true>(a, s) : dispatch_quant<false>(a, s);
 }
 
 cudaError_t launch_pack(const PrepArgs& a, cudaStream_t s) {
@@ -401,7 +450,7 @@ cudaError_t launch_pack(const PrepArgs& a, cudaStream_t s) {
     const int64_t need = (work + 255) / 256;
     int row_ctas = static_cast<int>(need < 152 * 8 ? need : 152 * 8);
     if (row_ctas < 1) row_ctas = 1;
-    pack_kernel<<<row_ctas + scale_ctas(a), 256, 0, s>>>(a, row_ctas);
+    pack_kernel<<<row_ctas + weight_ctas(a), 256, 0, s>>>(a, row_ctas);
     return cudaGetLastError();
 }
 

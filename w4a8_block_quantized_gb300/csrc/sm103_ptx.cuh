@@ -81,6 +81,36 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+// ---------------------------------------------------------------- shared-memory counters
+// A monotonic counter in shared memory as a lighter signal than an mbarrier: producers add
+// with release semantics, a consumer polls with acquire loads until the count is reached.
+__device__ __forceinline__ void smem_add_release(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t smem_ld_acquire(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+// Wait until the counter at p reaches `target` (counts stay below 2^31), bounded like mbar_wait.
+__device__ __forceinline__ bool counter_wait(const uint32_t* p, uint32_t target, const WaitCtl& ctl) {
+    if (static_cast<int32_t>(smem_ld_acquire(p) - target) >= 0) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (static_cast<int32_t>(smem_ld_acquire(p) - target) >= 0) return true;
+        if (i > 64u) __nanosleep(32);
+        if ((i & 31u) == 0u) {
+            if (*ctl.abort) return false;
+            if (globaltimer_ns() - t0 > ctl.limit_ns) {
+                *ctl.abort = 1u;
+                atomicOr(ctl.status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- register split
 // Per-warpgroup register re-allocation.  The totals over the CTA must stay within the
 // registers the CTA was launched with (threads x registers per thread at launch).
@@ -183,6 +213,29 @@ __device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
+}
+
+// 32 TMEM lanes x 16 fp32 columns: thread t of the warp receives lane (quarter base + t),
+// columns c .. c+15 of `taddr`, r[j] = column c + j.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// One lane of the (converged) warp, the same lane for every call with a full mask.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t p;
+    asm volatile(
+        "{\n\t.reg .b32 r;\n\t.reg .pred q;\n\t"
+        "elect.sync r|q, 0xffffffff;\n\t"
+        "selp.b32 %0, 1, 0, q;\n\t}"
+        : "=r"(p));
+    return p != 0;
 }
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading/stride byte

@@ -13,52 +13,71 @@ namespace w4a8 {
 constexpr uint32_t kStatusTimeout = 1u;
 
 constexpr int kBlock = 64;     // weights per (s_w, z_w) pair along K
-constexpr int kTileW = 128;    // GEMM tile weight rows (output columns n) = TMEM lanes
-constexpr int kPadM = 256;     // token padding of the transposed row sums (largest token tile)
-constexpr int kPadN = 256;     // weight-row padding of the re-laid-out weight scales
+constexpr int kTileW = 128;    // GEMM tile weight rows (output columns n) = TMEM lanes = MMA M
+constexpr int kTileT = 128;    // GEMM tile tokens = MMA N
 
 inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
-
-// Layout of the prepared activations (a caller-owned buffer):
-//   apk : tensor-core activation operand, uint8 [M][2K]; per row and 64-block,
-//         64 bytes of e4m3(16 * (a >> 4)) then 64 bytes of e4m3(a & 15)
-//   s_a : fp32 [M]                           (omitted when the caller passes s_a)
-//   rx  : [K/64][M_pad] x 16 bytes: the block row sum rs = 64*rh + rl (rh = rs >> 6,
-//         rl = rs & 63) as the fp16 pair {rh / 8, rl / 512} followed by 12 zero bytes, the
-//         K-major operand of the zero-point MMA (exact: |rh| <= 127, 0 <= rl <= 63)
-// Layout of the prepared weight scales:
-//   wsc : [K/64] x { fp32 [N_pad] 512 s_w[n,b], weight row n at 4*(n % 8) + (n % 32) / 8
-//         within its group of 32 rows (an epilogue thread's rows n, n+8, n+16, n+24 in one
-//         16-byte vector); fp16x2 [N_pad] {-z_w[n,b], -z_w[n,b]} in row order }, zero past N
 inline size_t align_ws(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
+// Operand records: the GEMM moves each (tile, 64-block) operand with one bulk copy, so the
+// producers write it in shared-memory order.
+//
+// Token record (kTokRec bytes) for tokens 128t .. 128t+127 and block b, row r = m % 128:
+//   [0, 16384)      the two e4m3 nibble planes of section 3 eq. (3) in the 128-byte-swizzled
+//                   K-major layout: row r at 128 r; its 16-byte chunk c (c < 4: e4m3(16*(a>>4))
+//                   for k = 16c .. 16c+15 of the block, c >= 4: e4m3(a & 15) for k = 16(c-4) ..)
+//                   stored at chunk position c ^ (r % 8)
+//   [16384, 18432)  row r at 16384 + 16 r: the block row sum rs = 64*rh + rl (rh = rs >> 6,
+//                   rl = rs & 63) as the fp16 pair {rh / 8, rl / 512} then 12 zero bytes, the
+//                   token side of the zero-point MMA (exact: |rh| <= 127, 0 <= rl <= 63)
+// Weight record (kWRec bytes) for weight rows 128t .. 128t+127 and block b, row r = n % 128:
+//   [0, 8192)       the e4m3 weight operand in the 64-byte-swizzled K-major layout: row r at
+//                   64 r, its 16-byte chunk c (k = 16c .. 16c+15) at chunk position c ^ ((r/2) % 4);
+//                   the byte of a weight is its u4 code q, the e4m3 encoding of q * 2^-9
+//                   (subnormals and the first normal binade share the step 2^-9)
+//   [8192, 10240)   row r at 8192 + 16 r: the fp16 pair {-z_w, -z_w} then 12 zero bytes, the
+//                   weight side of the zero-point MMA
+// Weight scales (read by the epilogue straight from memory): fp32 512 s_w[n,b] (the power
+// of two undoes the 2^-9) at [tile][b][r].
+// Rows past M or N are not read into any stored output; the weight side writes them as 0.
+constexpr int kTokRec = 18432;
+constexpr int kTokRx = 16384;
+constexpr int kWRec = 10240;
+constexpr int kWZx = 8192;
+
+// Prepared activations (a caller-owned buffer): token records [ceil(M/128)][K/64], then
+// s_a fp32 [M] (omitted when the caller passes s_a).
 struct ActLayout {
-    size_t apk = 0, s_a = 0, rx = 0, total = 0;
-    int64_t M_pad = 0;
+    size_t rec = 0, s_a = 0, total = 0;
+    int64_t tiles = 0;
 };
 
-inline ActLayout act_layout(int64_t M, int64_t K, bool with_sa, bool with_rows) {
+inline ActLayout act_layout(int64_t M, int64_t K, bool with_sa) {
     ActLayout L;
-    const int64_t nb = K / kBlock;
-    L.M_pad = round_up(M, kPadM);
-    size_t off = 0;
-    off = align_ws(off + static_cast<size_t>(M) * static_cast<size_t>(2 * K));
+    L.tiles = (M + kTileT - 1) / kTileT;
+    size_t off = align_ws(static_cast<size_t>(L.tiles) * static_cast<size_t>(K / kBlock) * kTokRec);
     if (with_sa) {
         L.s_a = off;
         off = align_ws(off + static_cast<size_t>(M) * 4);
-    }
-    if (with_rows) {
-        L.rx = off;
-        off = align_ws(off + static_cast<size_t>(nb) * static_cast<size_t>(L.M_pad) * 16);
     }
     L.total = off;
     return L;
 }
 
-inline int64_t n_pad(int64_t N) { return round_up(N, kPadN); }
+// Prepared weights (a caller-owned buffer): weight records [ceil(N/128)][K/64], then the
+// weight scales [ceil(N/128)][K/64][128].
+struct WLayout {
+    size_t sc = 0, total = 0;
+    int64_t tiles = 0;
+};
 
-inline size_t wsc_bytes(int64_t N, int64_t K) {
-    return align_ws(static_cast<size_t>(K / kBlock) * static_cast<size_t>(n_pad(N)) * 8);
+inline WLayout w_layout(int64_t N, int64_t K) {
+    WLayout L;
+    L.tiles = (N + kTileW - 1) / kTileW;
+    const size_t recs = static_cast<size_t>(L.tiles) * static_cast<size_t>(K / kBlock);
+    L.sc = align_ws(recs * kWRec);
+    L.total = align_ws(L.sc + recs * kTileW * 4);
+    return L;
 }
 
 // ---------------------------------------------------------------- pre-pass / pack
@@ -66,50 +85,45 @@ struct PrepArgs {
     // row job, quantize mode (x != nullptr) or pack mode (a_q_in != nullptr)
     const float* x = nullptr;
     const int8_t* a_q_in = nullptr;
-    const int32_t* rs_in = nullptr;  // pack mode: row sums [M][K/64] to re-lay out (may be null)
+    const int32_t* rs_in = nullptr;  // pack mode: row sums [M][K/64] (may be null: rx left unwritten)
     int64_t M = 0, K = 0;
     int64_t row0 = 0;                // first source row (debug window); outputs start at row 0
     // API-layout outputs (quant_pack)
     int8_t* a_q_out = nullptr;
     float* s_a_out = nullptr;
     int32_t* rs_out = nullptr;
-    // GEMM-layout outputs
-    uint8_t* apk = nullptr;
-    uint4* rx = nullptr;
-    int64_t M_pad = 0;
-    // weight-scale job (skipped when sz == nullptr)
+    // GEMM-layout output: token records
+    uint8_t* trec = nullptr;
+    // weight job (skipped when wrec == nullptr): rows n_first .. n_first + N - 1 of wq into
+    // weight records; the zero-point rows and the scales (sc) only when s_w != nullptr
+    const uint8_t* wq = nullptr;
+    int64_t n_first = 0;
     const uint16_t* s_w = nullptr;
     const uint16_t* z_w = nullptr;
-    int64_t N = 0, N_pad = 0;
-    float* wsc = nullptr;
+    int64_t N = 0;
+    uint8_t* wrec = nullptr;
+    float* sc = nullptr;
 };
 
-cudaError_t launch_quant(const PrepArgs& a, cudaStream_t s);  // x -> codes (+ scales job)
-cudaError_t launch_pack(const PrepArgs& a, cudaStream_t s);   // a_q -> apk (+ rx, scales)
+cudaError_t launch_quant(const PrepArgs& a, cudaStream_t s);  // x -> codes (+ weight job)
+cudaError_t launch_pack(const PrepArgs& a, cudaStream_t s);   // a_q -> token records (+ weight job)
 
 // ---------------------------------------------------------------- GEMM
 struct GemmArgs {
-    int64_t M = 0, N = 0, K = 0;       // full problem (N, K) and rows in the operand map
-    int64_t m_cnt = 0, n0 = 0, n_cnt = 0;  // rows [0, m_cnt) of apk, columns [n0, n0 + n_cnt)
-    int64_t M_pad = 0, N_pad = 0;
-    const float* wsc = nullptr;
-    const uint4* rx = nullptr;
+    int64_t M = 0, N = 0, K = 0;       // output rows / columns (row stride N) and depth
+    const uint8_t* trec = nullptr;      // token records [ceil(M/128)][K/64]
+    const uint8_t* wrec = nullptr;      // weight records [ceil(N/128)][K/64]
+    const float* sc = nullptr;          // weight scales [ceil(N/128)][K/64][128]
     const float* s_a = nullptr;
     const float* bias = nullptr;
-    float* y = nullptr;                 // [M][N], row stride N
-    int32_t* acc = nullptr;             // debug: [m_cnt][n_cnt][K/64]
+    float* y = nullptr;                 // [M][N]
+    int32_t* acc = nullptr;             // debug: [M][N][K/64]
     uint32_t* status = nullptr;
     uint64_t wait_limit_ns = 1000000000ull;
 };
 
-struct GemmMaps {
-    CUtensorMap a;  // apk (tokens), uint8 [rows][2K], box 128 x TN, 128-byte swizzle
-    CUtensorMap b;  // wq (weights), uint8 [N][K/2], box 32 x 128, no swizzle
-};
-
-// Token-tile width TN (the MMA's N) for a problem: 256, 128 or 64.
-int pick_token_tile(int64_t m_cnt, int64_t n_cnt, int num_sms);
-cudaError_t launch_gemm(const GemmMaps& maps, const GemmArgs& a, int tn, bool debug, cudaStream_t s);
+// Persistent launch over ceil(M/128) x ceil(N/128) output tiles on at most `num_sms` CTAs.
+cudaError_t launch_gemm(const GemmArgs& a, bool debug, int num_sms, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace w4a8
