@@ -150,6 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Launched as a programmatic dependent of the previous kernel in the stream (normally the
+    // pre-pass that wrote the operand records): the set-up above overlaps its tail, and no
+    // global memory is touched before it has completed.
+    griddep_wait();
 
     if (warp < 4) {
         regs_dec<kRegsLow>();
@@ -359,8 +363,17 @@ cudaError_t run(const GemmArgs& a, int num_sms, cudaStream_t s) {
     }
     const int64_t tiles = ((a.M + kTileT - 1) / kTileT) * ((a.N + kTileW - 1) / kTileW);
     const int64_t grid = tiles < num_sms ? tiles : num_sms;
-    gemm_kernel<DEBUG><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<DEBUG>, a);
 }
 
 }  // namespace

@@ -81,36 +81,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
-// ---------------------------------------------------------------- shared-memory counters
-// A monotonic counter in shared memory as a lighter signal than an mbarrier: producers add
-// with release semantics, a consumer polls with acquire loads until the count is reached.
-__device__ __forceinline__ void smem_add_release(uint32_t* p, uint32_t v) {
-    asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t smem_ld_acquire(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-    return v;
-}
-
-// Wait until the counter at p reaches `target` (counts stay below 2^31), bounded like mbar_wait.
-__device__ __forceinline__ bool counter_wait(const uint32_t* p, uint32_t target, const WaitCtl& ctl) {
-    if (static_cast<int32_t>(smem_ld_acquire(p) - target) >= 0) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (static_cast<int32_t>(smem_ld_acquire(p) - target) >= 0) return true;
-        if (i > 64u) __nanosleep(32);
-        if ((i & 31u) == 0u) {
-            if (*ctl.abort) return false;
-            if (globaltimer_ns() - t0 > ctl.limit_ns) {
-                *ctl.abort = 1u;
-                atomicOr(ctl.status, kStatusTimeout);
-                return false;
-            }
-        }
-    }
-}
-
 // ---------------------------------------------------------------- register split
 // Per-warpgroup register re-allocation.  The totals over the CTA must stay within the
 // registers the CTA was launched with (threads x registers per thread at launch).
@@ -122,6 +92,11 @@ template <int N>
 __device__ __forceinline__ void regs_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// Blocks until the grids this one depends on have completed and their memory is visible
+// (returns at once for a grid launched without a programmatic dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------- proxy fences
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy
