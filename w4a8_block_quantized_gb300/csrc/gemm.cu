@@ -93,6 +93,25 @@ __device__ __forceinline__ void tile_at(int64_t t, int64_t tiles_t, int64_t tile
     tw = r / gsz;
 }
 
+// Named barrier 1 over the 16 epilogue warps (barrier 0 is __syncthreads).  Every epilogue
+// warp reaches each of these at the same point of the same loop: a wait that fails is voted
+// on with epi_all() first, so either all epilogue warps go on or all unwind together.
+__device__ __forceinline__ void epi_bar_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+}
+__device__ __forceinline__ bool epi_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "n"(kEpiWarps * 32)
+        : "memory");
+    return r != 0;
+}
+
 // Bounded wait that ignores the abort flag: used while unwinding to let copies and MMAs
 // already in flight land before the CTA's shared memory and TMEM are released.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -129,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1 + kEpiWarps);
+            mbar_init(&full[s], 2);  // the producer and one epilogue thread
             mbar_init(&empty[s], 1);
         }
         for (int i = 0; i < 2; ++i) mbar_init(&tfull[i], 2);  // one commit per block slot
@@ -245,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = q * 32 + lane;                // this thread's weight row in the tile
         const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 32);
         // the TMEM buffers start free: release the first two stages
-        if (lane == 0)
+        if (warp == 4 && lane == 0)
             for (uint32_t q0 = 0; q0 < 2 && q0 < total; ++q0) mbar_arrive(&full[q0]);
         uint32_t j = 0;  // stage counter of this CTA
         bool ok = true;
@@ -273,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ns1 = 2 * p + 3 < nb ? __ldg(sct + (2 * p + 3) * kTileW) : 0.0f;
                 }
                 const uint32_t pair = j & 1u, b0 = 2 * pair, b1 = b0 + 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(&tfull[pair], (j >> 1) & 1, ctl))) {
+                if (!epi_all(mbar_wait(&tfull[pair], (j >> 1) & 1, ctl))) {
                     ok = false;
                     break;
                 }
@@ -289,9 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_ld();
                 // the accumulators are in registers: the buffers are free for the stage two later
+                // (the epilogue warps meet on a named barrier, then one thread arrives: sixteen
+                // arrivals on one mbarrier word would serialise)
                 tc_fence_before();
-                __syncwarp();
-                if (lane == 0 && j + 2 < total) mbar_arrive(&full[(j + 2) % kStages]);
+                epi_bar_sync();
+                if (warp == 4 && lane == 0 && j + 2 < total) mbar_arrive(&full[(j + 2) % kStages]);
                 if (DEBUG) {
                     if (n < args.N) {
 #pragma unroll

@@ -191,15 +191,15 @@ __device__ void weights_job(const PrepArgs& a, int64_t cta, int64_t ctas) {
 
 // Register-resident pre-pass: G warps per row, V float4 per lane (row length K <= 128*G*V).
 // With V <= 8 the next iteration's row is loaded while the current one is quantized.
-template <int G, int V, bool PLANES>
-__global__ void __launch_bounds__(256, 2) quant_kernel(const PrepArgs a, int row_ctas) {
+template <int G, int V, bool PLANES, int NW>
+__global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) quant_kernel(const PrepArgs a, int row_ctas) {
     if (static_cast<int>(blockIdx.x) >= row_ctas) {
         if (a.wrec) weights_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
         return;
     }
     constexpr bool kPrefetch = V <= 8;
-    __shared__ float red[2][8];
-    constexpr int RPC = 8 / G;  // rows per CTA iteration
+    __shared__ float red[2][NW];
+    constexpr int RPC = NW / G;  // rows per CTA iteration
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wg = warp % G, rsub = warp / G;
     const int64_t K = a.K, n4 = K / 4, nb = K / kBlock;
@@ -412,13 +412,17 @@ int weight_ctas(const PrepArgs& a) {
     return static_cast<int>(c < 152 * 8 ? c : 152 * 8);
 }
 
-template <int G, int V, bool PLANES>
+template <int G, int V, bool PLANES, int NW = 8>
 cudaError_t run_quant(const PrepArgs& a, cudaStream_t s) {
-    constexpr int RPC = 8 / G;
+    constexpr int RPC = NW / G;
     const int64_t need = (a.M + RPC - 1) / RPC;
-    const int row_ctas = static_cast<int>(need < 152 * 8 ? need : 152 * 8);
+    // as many row CTAs as fit on the GPU at once (two 256-thread or one 512-thread CTA per
+    // SM), with the rows spread evenly: each CTA walks its rows with the next one in flight
+    constexpr int64_t cap = NW == 8 ? 152 * 2 : 152;
+    const int64_t iters = (need + cap - 1) / cap;
+    const int row_ctas = static_cast<int>(iters > 0 ? (need + iters - 1) / iters : 1);
     const int grid = row_ctas + weight_ctas(a);
-    quant_kernel<G, V, PLANES><<<grid, 256, 0, s>>>(a, row_ctas);
+    quant_kernel<G, V, PLANES, NW><<<grid, NW * 32, 0, s>>>(a, row_ctas);
     return cudaGetLastError();
 }
 
@@ -426,14 +430,15 @@ template <bool PLANES>
 cudaError_t dispatch_quant(const PrepArgs& a, cudaStream_t s) {
     const int64_t n4 = a.K / 4;
     // smallest warp group G whose lanes hold the row in at most 8 float4 each (so the next
-    // row can be prefetched), then 16 float4 without prefetch, then the two-pass kernel
+    // row can be prefetched): 1-8 warps of a 256-thread CTA, then the 16 warps of a 512-thread
+    // CTA; past that, the two-pass kernel
     if (n4 <= 32 * 2) return run_quant<1, 2, PLANES>(a, s);
     if (n4 <= 32 * 4) return run_quant<1, 4, PLANES>(a, s);
     if (n4 <= 32 * 8) return run_quant<1, 8, PLANES>(a, s);
     if (n4 <= 64 * 8) return run_quant<2, 8, PLANES>(a, s);
     if (n4 <= 128 * 8) return run_quant<4, 8, PLANES>(a, s);
     if (n4 <= 256 * 8) return run_quant<8, 8, PLANES>(a, s);
-    if (n4 <= 256 * 16) return run_quant<8, 16, PLANES>(a, s);
+    if (n4 <= 512 * 8) return run_quant<16, 8, PLANES, 16>(a, s);  // 512-thread CTAs, one row each
     const int row_ctas = static_cast<int>(a.M < 152 * 4 ? a.M : 152 * 4);
     quant_long_kernel<PLANES><<<row_ctas + weight_ctas(a), 256, 0, s>>>(a, row_ctas);
     return cudaGetLastError();
