@@ -123,6 +123,23 @@ def test_linear_small_shapes(M, K, N, bias):
     assert torch.equal(y_fused, y_sep), "fused and separate calls differ"
 
 
+@pytest.mark.parametrize("M,K,N,bias", [(4096, 512, 256, True), (4100, 1024, 300, False), (4352, 128, 1000, True),
+                                        (4097, 2048, 129, True)])
+def test_linear_wide_token_tiles(M, K, N, bias):
+    """M >= 4096 takes the 256-token records and the N = 256 contraction: ragged token and
+    weight tails, every output against the oracle, the fused call against the separate and
+    the prepared calls bit for bit."""
+    d = synth.random_small(M, K, N, seed=M + 3 * K + N, bias=bias)
+    y_fused, y_sep = _run_both(d)
+    y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
+    check_y(y_fused, y_ref, bound, f"wide {M}x{K}->{N}")
+    assert torch.equal(y_fused, y_sep), "fused and separate calls differ"
+    g = inputs_to_dev(d)
+    act = B().prepare_activations(g["x"])
+    pw = B().prepare_weights(g["wq"], g["s_w"], g["z_w"])
+    assert torch.equal(B().linear_prepared(act, pw, M, N, K, bias=g["bias"]), y_fused), "prepared call differs"
+
+
 @pytest.mark.parametrize("key", ["c0", "c1", "c2", "c3"])
 def test_workloads_full(key):
     _, specs = synth.workload(key)

@@ -48,7 +48,7 @@ def up_to_date() -> bool:
 # Kernels that re-split registers between warpgroups (setmaxnreg) need exactly this many
 # registers per thread at launch: the split in gemm.cu is sized against it, and a smaller
 # launch allocation would leave setmaxnreg.inc waiting for registers that never come.
-REGISTER_SPLIT_KERNELS = {"gemm_kernel": 96}
+REGISTER_SPLIT_KERNELS = {"gemm_kernel": 96, "gemm_wide_kernel": 96}
 
 
 def check_register_split(ptxas_log: str) -> None:

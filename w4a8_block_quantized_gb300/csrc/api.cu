@@ -74,7 +74,7 @@ struct CallLayout {
 
 CallLayout call_layout(int64_t M, int64_t N, int64_t K, bool with_sa) {
     CallLayout c;
-    c.act = act_layout(M, K, with_sa);
+    c.act = act_layout(M, K, with_sa, token_tile(M));
     c.w = w_layout(N, K);
     c.w_off = c.act.total;
     c.total = c.w_off + c.w.total;
@@ -90,6 +90,7 @@ int run_linear(const uint8_t* trec, const float* s_a, const uint8_t* pw, const f
     g.N = N;
     g.K = K;
     g.trec = trec;
+    g.tw = token_tile(M);
     g.wrec = pw;
     g.sc = reinterpret_cast<const float*>(pw + W.sc);
     g.s_a = s_a;
@@ -150,13 +151,13 @@ size_t w4a8_prefill_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 
 size_t w4a8_debug_workspace_bytes(int64_t m_cnt, int64_t n_cnt, int64_t K) {
     if (check_shape(m_cnt, n_cnt, K) != W4A8_OK || m_cnt == 0 || n_cnt == 0) return static_cast<size_t>(-1);
-    return act_layout(m_cnt, K, false).total + w_layout(n_cnt, K).total;
+    return act_layout(m_cnt, K, false, kTileT).total + w_layout(n_cnt, K).total;
 }
 
 size_t w4a8_prepared_activations_bytes(int64_t M, int64_t K) {
     if (check_shape(M, 1, K) != W4A8_OK) return static_cast<size_t>(-1);
     if (M == 0) return 0;
-    return act_layout(M, K, true).total;
+    return act_layout(M, K, true, token_tile(M)).total;
 }
 
 size_t w4a8_prepared_weights_bytes(int64_t N, int64_t K) {
@@ -206,6 +207,7 @@ int w4a8_linear(const int8_t* a_q, const float* a_scale, const int32_t* rowsum, 
     p.rs_in = rowsum;
     p.M = M;
     p.trec = ws + L.act.rec;
+    p.tw = L.act.tw;
     set_weight_job(&p, wq, w_scale, w_zero, N, K, ws + L.w_off);
     if (launch_pack(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
     return run_linear(ws + L.act.rec, a_scale, ws + L.w_off, bias, y, M, N, K, *d, st);
@@ -234,6 +236,7 @@ int w4a8_prefill_linear(const float* x, const uint8_t* wq, const uint16_t* w_sca
     p.M = M;
     p.s_a_out = s_a;
     p.trec = ws + L.act.rec;
+    p.tw = L.act.tw;
     set_weight_job(&p, wq, w_scale, w_zero, N, K, ws + L.w_off);
     if (launch_quant(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
     return run_linear(ws + L.act.rec, s_a, ws + L.w_off, bias, y, M, N, K, *d, st);
@@ -245,7 +248,7 @@ int w4a8_prepare_activations(const float* x, int64_t M, int64_t K, void* act, si
     if (M == 0) return W4A8_OK;
     if (!x || !act) return W4A8_ERR_ARG;
     if (!aligned(x, 16) || !aligned(act, 16)) return W4A8_ERR_ALIGN;
-    const ActLayout A = act_layout(M, K, true);
+    const ActLayout A = act_layout(M, K, true, token_tile(M));
     if (act_bytes < A.total) return W4A8_ERR_WORKSPACE;
     DeviceInfo* d = nullptr;
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
@@ -256,6 +259,7 @@ int w4a8_prepare_activations(const float* x, int64_t M, int64_t K, void* act, si
     p.K = K;
     p.s_a_out = reinterpret_cast<float*>(a + A.s_a);
     p.trec = a + A.rec;
+    p.tw = A.tw;
     return launch_quant(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
 }
 
@@ -285,7 +289,7 @@ int w4a8_linear_prepared(const void* act, const void* pw, const float* bias, flo
     if (!aligned(act, 16) || !aligned(pw, 16) || !aligned(y, 16) || (bias && !aligned(bias, 4))) return W4A8_ERR_ALIGN;
     DeviceInfo* d = nullptr;
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
-    const ActLayout A = act_layout(M, K, true);
+    const ActLayout A = act_layout(M, K, true, token_tile(M));
     const uint8_t* a = static_cast<const uint8_t*>(act);
     return run_linear(a + A.rec, reinterpret_cast<const float*>(a + A.s_a), static_cast<const uint8_t*>(pw), bias, y,
                       M, N, K, *d, static_cast<cudaStream_t>(stream));
@@ -299,7 +303,7 @@ int w4a8_debug_block_acc(const int8_t* a_q, const uint8_t* wq, int64_t M, int64_
     if (!a_q || !wq || !acc) return W4A8_ERR_ARG;
     if (m0 < 0 || n0 < 0 || m_cnt <= 0 || n_cnt <= 0 || m0 + m_cnt > M || n0 + n_cnt > N) return W4A8_ERR_SHAPE;
     if (!aligned(a_q, 16) || !aligned(wq, 16) || !aligned(acc, 4)) return W4A8_ERR_ALIGN;
-    const ActLayout L = act_layout(m_cnt, K, false);
+    const ActLayout L = act_layout(m_cnt, K, false, kTileT);
     const WLayout W = w_layout(n_cnt, K);
     if (!workspace || workspace_bytes < L.total + W.total) return W4A8_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return W4A8_ERR_ALIGN;

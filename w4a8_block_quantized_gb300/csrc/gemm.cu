@@ -357,6 +357,208 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------- 256-token tiles
+// The large-M variant.  One MMA covers 128 weights x 256 tokens (N = 256), so the SM issues
+// half as many tcgen05.mma instructions per unit of work as with 128-token tiles (the MMA
+// issue rate of an SM, one instruction per ~50-90 cycles, is what bounds the 128-token
+// kernel).  Two TMEM buffers of 256 columns; one block per shared-memory stage, filled by two
+// bulk copies (a 256-token record and a weight record).  Roles, barriers and bounded waits
+// follow gemm_kernel; an epilogue thread owns one weight row and 64 token columns, drained
+// 32 at a time.
+namespace wide {
+constexpr int kTN = 256;
+constexpr int kStages = 4;
+constexpr int kNBuf = 2;
+constexpr int kTok = 144 * kTN;                 // token record of one block
+constexpr int kStageBytes = kTok + kWRec;
+constexpr int kOffZero = kStages * kStageBytes;
+constexpr int kOffBar = kOffZero + kZeroBytes;
+constexpr int kNumBars = 2 * kStages + kNBuf + kIssuers;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+static_assert(kTok % 1024 == 0 && kStageBytes % 1024 == 0, "swizzled operand tiles must stay 1024-aligned");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kNBuf * kTN == 512, "TMEM allocation");
+static_assert(kNBuf <= kStages, "a stage barrier carries a buffer release only after its previous phase");
+static_assert(kZeroBytes >= kTN * 16, "zero half of the token-side zero-point operand");
+}  // namespace wide
+
+__global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs args) {
+    namespace W = wide;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + W::kOffBar);
+    uint64_t* empty = full + W::kStages;
+    uint64_t* tfull = empty + W::kStages;
+    uint64_t* drain = tfull + W::kNBuf;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + W::kOffMisc);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t tiles_t = (args.M + W::kTN - 1) / W::kTN;
+    const int64_t tiles_w = (args.N + kTileW - 1) / kTileW;
+    const int64_t ntiles = tiles_t * tiles_w;
+    const int64_t first = blockIdx.x;
+    // the host keeps ntiles * K/64 below 2^31, so the block counters below fit 32 bits
+    const uint32_t my_tiles = ntiles > first ? static_cast<uint32_t>((ntiles - 1 - first) / gridDim.x + 1) : 0u;
+    const uint32_t nb = static_cast<uint32_t>(args.K / kBlock);
+    const uint32_t total = my_tiles * nb;  // blocks of this CTA, counted across its tiles
+    const WaitCtl ctl{abort_flag, args.status, args.wait_limit_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < W::kStages; ++s) {
+            mbar_init(&full[s], 2);  // the producer and one epilogue thread
+            mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < W::kNBuf; ++i) mbar_init(&tfull[i], 1);
+        for (int i = 0; i < kIssuers; ++i) mbar_init(&drain[i], 1);
+        *abort_flag = 0u;
+        fence_barrier_init();
+    }
+    for (int i = threadIdx.x; i < kZeroBytes / 16; i += kThreads)
+        reinterpret_cast<uint4*>(smem + W::kOffZero)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    griddep_wait();
+
+    if (warp < 4) {
+        regs_dec<kRegsLow>();
+        if (warp == 0) {
+            // -------------------------------------------------------- producer
+            if (lane == 0) {
+                uint32_t g = 0, issued = 0;
+                bool ok = true;
+                for (uint32_t i = 0; ok && i < my_tiles; ++i) {
+                    int64_t tt, tw;
+                    tile_at(first + static_cast<int64_t>(i) * gridDim.x, tiles_t, tiles_w, tt, tw);
+                    const uint8_t* tsrc = args.trec + static_cast<int64_t>(tt) * nb * W::kTok;
+                    const uint8_t* wsrc = args.wrec + static_cast<int64_t>(tw) * nb * kWRec;
+                    for (uint32_t b = 0; b < nb; ++b, ++g) {
+                        const int s = static_cast<int>(g % W::kStages);
+                        const uint32_t k = g / W::kStages;
+                        if (k > 0 && !mbar_wait(&empty[s], (k - 1) & 1, ctl)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t* st = smem + s * W::kStageBytes;
+                        mbar_arrive_expect_tx(&full[s], W::kTok + kWRec);
+                        bulk_load(st, tsrc + static_cast<int64_t>(b) * W::kTok, W::kTok, &full[s]);
+                        bulk_load(st + W::kTok, wsrc + static_cast<int64_t>(b) * kWRec, kWRec, &full[s]);
+                        issued = g + 1;
+                    }
+                }
+                if (*abort_flag) {
+                    for (uint32_t q = (issued > W::kStages ? issued - W::kStages : 0); q < issued; ++q)
+                        drain_wait(&full[q % W::kStages], (q / W::kStages) & 1, 100000000ull);
+                }
+            }
+        } else {
+            // -------------------------------------------------------- MMA issue (warps 1-3)
+            const int iw = warp - 1;
+            constexpr uint32_t idesc = idesc_e4m3_f32(kTileW, W::kTN);
+            const uint32_t zr = smem_u32(smem + W::kOffZero);
+            const uint32_t t0a = smem_u32(smem), w0a = smem_u32(smem + W::kTok);
+            const uint64_t dT0 = smem_desc(t0a, 1024, kLayoutSw128);
+            const uint64_t dW0 = smem_desc(w0a, 512, kLayoutSw64);
+            const uint64_t dBx0 = smem_desc(t0a + 128 * W::kTN, 128, 0, zr - (t0a + 128 * W::kTN));
+            const uint64_t dAx0 = smem_desc(w0a + kWZx, 128, 0, zr - (w0a + kWZx));
+            for (uint32_t g = iw; g < total; g += kIssuers) {
+                const int s = static_cast<int>(g % W::kStages);
+                const uint32_t buf = g & 1u;
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (g / W::kStages) & 1, ctl))) break;
+                tc_fence_after();
+                if (elect_one()) {
+                    const uint32_t d = tmem_base + buf * W::kTN;
+                    const uint64_t o = static_cast<uint64_t>((s * W::kStageBytes) >> 4);
+                    const uint64_t dT = dT0 + o, dW = dW0 + o;
+                    mma_f8f6f4(d, dW, dT, idesc, 0u);
+                    mma_f8f6f4(d, dW + 2, dT + 2, idesc, 1u);
+                    mma_f8f6f4(d, dW, dT + 4, idesc, 1u);
+                    mma_f8f6f4(d, dW + 2, dT + 6, idesc, 1u);
+                    mma_f16(d, dAx0 + o - (o << 16), dBx0 + o - (o << 16), idesc, 1u);
+                    mma_commit(&tfull[buf]);
+                }
+                __syncwarp();
+            }
+            if (elect_one()) mma_commit(&drain[iw]);
+            __syncwarp();
+            drain_wait(&drain[iw], 0, 100000000ull);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        regs_inc<kRegsHigh>();
+        const int q = warp & 3, h = (warp - 4) >> 2;  // TMEM lane quarter, 64-column quarter
+        const int row = q * 32 + lane;
+        const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 64);
+        if (warp == 4 && lane == 0)
+            for (uint32_t q0 = 0; q0 < W::kNBuf && q0 < total; ++q0) mbar_arrive(&full[q0]);
+        uint32_t g = 0;
+        bool ok = true;
+        for (uint32_t i = 0; ok && i < my_tiles; ++i) {
+            int64_t tt, tw;
+            tile_at(first + static_cast<int64_t>(i) * gridDim.x, tiles_t, tiles_w, tt, tw);
+            const int64_t mt0 = tt * W::kTN + h * 64;
+            const int64_t n = tw * kTileW + row;
+            const float* sct = args.sc + static_cast<int64_t>(tw) * nb * kTileW + row;
+            float ns = __ldg(sct);
+            float y[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) y[c] = 0.0f;
+            for (uint32_t b = 0; b < nb; ++b, ++g) {
+                const float sb = ns;
+                if (b + 1 < nb) ns = __ldg(sct + (b + 1) * kTileW);
+                const uint32_t buf = g & 1u;
+                if (!epi_all(mbar_wait(&tfull[buf], (g >> 1) & 1, ctl))) {
+                    ok = false;
+                    break;
+                }
+                if (warp == 4 && lane == 0) mbar_arrive(&empty[g % W::kStages]);
+                tc_fence_after();
+                const uint32_t tb = tl + buf * W::kTN;
+                uint32_t v[32];
+                tmem_ld_32x32b_x16(tb, v);
+                tmem_ld_32x32b_x16(tb + 16, v + 16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) y[c] = fmaf(sb, __uint_as_float(v[c]), y[c]);
+                tmem_ld_32x32b_x16(tb + 32, v);
+                tmem_ld_32x32b_x16(tb + 48, v + 16);
+                tmem_wait_ld();
+                // the accumulator is in registers: the buffer is free for block g + 2
+                tc_fence_before();
+                epi_bar_sync();
+                if (warp == 4 && lane == 0 && g + W::kNBuf < total) mbar_arrive(&full[(g + W::kNBuf) % W::kStages]);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) y[32 + c] = fmaf(sb, __uint_as_float(v[c]), y[32 + c]);
+            }
+            if (!ok) break;
+            if (n < args.N) {
+                const float bn = args.bias ? args.bias[n] : 0.0f;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const int64_t m = mt0 + c;
+                    if (m < args.M) args.y[m * args.N + n] = fmaf(args.s_a[m], y[c], bn);
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
 // A CTA that waits on a barrier nothing completes, to exercise the bounded-wait path.
 __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
     __shared__ uint64_t bar;
@@ -372,36 +574,43 @@ __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
     __syncthreads();
 }
 
-template <bool DEBUG>
-cudaError_t run(const GemmArgs& a, int num_sms, cudaStream_t s) {
-    static bool attr_done[64] = {};
+template <typename Kernel>
+cudaError_t launch(Kernel kernel, int smem_bytes, bool* attr_done, int64_t tiles, const GemmArgs& a, int num_sms,
+                   cudaStream_t s) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<DEBUG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    const int64_t tiles = ((a.M + kTileT - 1) / kTileT) * ((a.N + kTileW - 1) / kTileW);
     const int64_t grid = tiles < num_sms ? tiles : num_sms;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<DEBUG>, a);
+    return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& a, bool debug, int num_sms, cudaStream_t s) {
+    static bool attr_done[3][64] = {};
     if (num_sms < 1) return cudaErrorInvalidValue;
-    return debug ? run<true>(a, num_sms, s) : run<false>(a, num_sms, s);
+    const int64_t tiles_w = (a.N + kTileW - 1) / kTileW;
+    if (a.tw == wide::kTN && !debug)
+        return launch(gemm_wide_kernel, wide::kSmemBytes, attr_done[2], ((a.M + wide::kTN - 1) / wide::kTN) * tiles_w, a,
+                      num_sms, s);
+    if (a.tw != kTileT) return cudaErrorInvalidValue;
+    const int64_t tiles = ((a.M + kTileT - 1) / kTileT) * tiles_w;
+    return debug ? launch(gemm_kernel<true>, kSmemBytes, attr_done[1], tiles, a, num_sms, s)
+                 : launch(gemm_kernel<false>, kSmemBytes, attr_done[0], tiles, a, num_sms, s);
 }
 
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s) {

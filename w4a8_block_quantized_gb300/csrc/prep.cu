@@ -47,9 +47,9 @@ __device__ __forceinline__ uint4 rx_entry(int rs) {
     return make_uint4(*reinterpret_cast<const uint32_t*>(&p), 0u, 0u, 0u);
 }
 
-// Token record of row m, block b (the layout in w4a8_internal.h).
-__device__ __forceinline__ uint8_t* token_rec(uint8_t* trec, int64_t m, int64_t b, int64_t nb) {
-    return trec + ((m >> 7) * nb + b) * kTokRec;
+// Token record of row m, block b, for records of 2^ts tokens (the layout in w4a8_internal.h).
+__device__ __forceinline__ uint8_t* token_rec(uint8_t* trec, int64_t m, int64_t b, int64_t nb, int ts) {
+    return trec + ((m >> ts) * nb + b) * (static_cast<int64_t>(144) << ts);
 }
 
 // Byte offset, inside a token record, of the 4 codes k = 4j .. 4j+3 of the block (j < 16) of
@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) quant_kernel(const P
         return;
     }
     constexpr bool kPrefetch = V <= 8;
+    const int ts = a.tw == 256 ? 8 : 7;  // token record width 2^ts
     __shared__ float red[2][NW];
     constexpr int RPC = NW / G;  // rows per CTA iteration
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -262,8 +263,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) quant_kernel(const P
                     if (PLANES) {
                         uint32_t hi, lo;
                         planes4f(q[j], hi, lo);
-                        uint8_t* rec = token_rec(a.trec, m, f >> 4, nb);
-                        const int row = static_cast<int>(m & 127), j = static_cast<int>(f & 15);
+                        uint8_t* rec = token_rec(a.trec, m, f >> 4, nb, ts);
+                        const int row = static_cast<int>(m & ((1 << ts) - 1)), j = static_cast<int>(f & 15);
                         *reinterpret_cast<uint32_t*>(rec + plane_off(row, j, 0)) = hi;
                         *reinterpret_cast<uint32_t*>(rec + plane_off(row, j, 1)) = lo;
                     } else {
@@ -283,7 +284,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) quant_kernel(const P
                         const int64_t b = f >> 4;
                         const int rs = static_cast<int>(part[j]);
                         if (PLANES)
-                            *reinterpret_cast<uint4*>(token_rec(a.trec, m, b, nb) + kTokRx + (m & 127) * 16) = rx_entry(rs);
+                            *reinterpret_cast<uint4*>(token_rec(a.trec, m, b, nb, ts) + (128 << ts) + (m & ((1 << ts) - 1)) * 16) =
+                                rx_entry(rs);
                         else a.rs_out[m * nb + b] = rs;
                     }
                 }
@@ -309,6 +311,7 @@ __global__ void __launch_bounds__(256) quant_long_kernel(const PrepArgs a, int r
     __shared__ float red[8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t K = a.K, n4 = K / 4, nb = K / kBlock;
+    const int ts = a.tw == 256 ? 8 : 7;  // token record width 2^ts
     for (int64_t m = blockIdx.x; m < a.M; m += row_ctas) {
         const float4* xr = reinterpret_cast<const float4*>(a.x) + (a.row0 + m) * n4;
         float amax = 0.0f;
@@ -349,11 +352,11 @@ __global__ void __launch_bounds__(256) quant_long_kernel(const PrepArgs a, int r
                 if (PLANES) {
                     uint32_t hi, lo;
                     planes4(c0, c1, c2, c3, hi, lo);
-                    uint8_t* rec = token_rec(a.trec, m, b, nb);
-                    const int r = static_cast<int>(m & 127), j = static_cast<int>(f & 15);
+                    uint8_t* rec = token_rec(a.trec, m, b, nb, ts);
+                    const int r = static_cast<int>(m & ((1 << ts) - 1)), j = static_cast<int>(f & 15);
                     *reinterpret_cast<uint32_t*>(rec + plane_off(r, j, 0)) = hi;
                     *reinterpret_cast<uint32_t*>(rec + plane_off(r, j, 1)) = lo;
-                    if ((lane & 15) == 0) *reinterpret_cast<uint4*>(rec + kTokRx + r * 16) = rx_entry(part);
+                    if ((lane & 15) == 0) *reinterpret_cast<uint4*>(rec + (128 << ts) + r * 16) = rx_entry(part);
                 } else {
                     const uint32_t w = (c0 & 0xff) | ((c1 & 0xff) << 8) | ((c2 & 0xff) << 16) |
                                        (static_cast<uint32_t>(c3 & 0xff) << 24);
@@ -374,6 +377,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const PrepArgs a, int row_cta
     }
     const int64_t K = a.K, nb = K / kBlock, c16 = K / 16;
     const int64_t total = a.M * c16;
+    const int ts = a.tw == 256 ? 8 : 7;  // token record width 2^ts
     const int64_t stride = static_cast<int64_t>(row_ctas) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
         const int64_t m = i / c16, c = i - m * c16;
@@ -387,8 +391,8 @@ __global__ void __launch_bounds__(256) pack_kernel(const PrepArgs a, int row_cta
             planes4(static_cast<int8_t>(u & 0xff), static_cast<int8_t>((u >> 8) & 0xff),
                     static_cast<int8_t>((u >> 16) & 0xff), static_cast<int8_t>(u >> 24), hi[j], lo[j]);
         }
-        uint8_t* rec = token_rec(a.trec, m, c >> 2, nb);
-        const int r = static_cast<int>(m & 127), j4 = static_cast<int>(c & 3);
+        uint8_t* rec = token_rec(a.trec, m, c >> 2, nb, ts);
+        const int r = static_cast<int>(m & ((1 << ts) - 1)), j4 = static_cast<int>(c & 3);
         *reinterpret_cast<uint4*>(rec + r * 128 + ((j4 ^ (r & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(rec + r * 128 + (((j4 + 4) ^ (r & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
@@ -396,7 +400,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const PrepArgs a, int row_cta
         const int64_t tot = a.M * nb;
         for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < tot; i += stride) {
             const int64_t m = i / nb, b = i - m * nb;
-            *reinterpret_cast<uint4*>(token_rec(a.trec, m, b, nb) + kTokRx + (m & 127) * 16) =
+            *reinterpret_cast<uint4*>(token_rec(a.trec, m, b, nb, ts) + (128 << ts) + (m & ((1 << ts) - 1)) * 16) =
                 rx_entry(a.rs_in[(a.row0 + m) * nb + b]);
         }
     }

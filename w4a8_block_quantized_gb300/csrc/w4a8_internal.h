@@ -22,14 +22,16 @@ inline size_t align_ws(size_t v) { return (v + 255) & ~static_cast<size_t>(255);
 // Operand records: the GEMM moves each (tile, 64-block) operand with one bulk copy, so the
 // producers write it in shared-memory order.
 //
-// Token record (kTokRec bytes) for tokens 128t .. 128t+127 and block b, row r = m % 128:
-//   [0, 16384)      the two e4m3 nibble planes of section 3 eq. (3) in the 128-byte-swizzled
-//                   K-major layout: row r at 128 r; its 16-byte chunk c (c < 4: e4m3(16*(a>>4))
-//                   for k = 16c .. 16c+15 of the block, c >= 4: e4m3(a & 15) for k = 16(c-4) ..)
-//                   stored at chunk position c ^ (r % 8)
-//   [16384, 18432)  row r at 16384 + 16 r: the block row sum rs = 64*rh + rl (rh = rs >> 6,
-//                   rl = rs & 63) as the fp16 pair {rh / 8, rl / 512} then 12 zero bytes, the
-//                   token side of the zero-point MMA (exact: |rh| <= 127, 0 <= rl <= 63)
+// Token record (144 TW bytes) for tokens TW t .. TW t + TW - 1 and block b, row r = m % TW:
+//   [0, 128 TW)         the two e4m3 nibble planes of section 3 eq. (3) in the 128-byte-swizzled
+//                       K-major layout: row r at 128 r; its 16-byte chunk c (c < 4: e4m3(16*(a>>4))
+//                       for k = 16c .. 16c+15 of the block, c >= 4: e4m3(a & 15) for k = 16(c-4) ..)
+//                       stored at chunk position c ^ (r % 8)
+//   [128 TW, 144 TW)    row r at 128 TW + 16 r: the block row sum rs = 64*rh + rl (rh = rs >> 6,
+//                       rl = rs & 63) as the fp16 pair {rh / 8, rl / 512} then 12 zero bytes, the
+//                       token side of the zero-point MMA (exact: |rh| <= 127, 0 <= rl <= 63)
+// The record width TW is a function of M alone (token_tile), so the pre-pass and the GEMM
+// agree on it without knowing each other's other dimensions.
 // Weight record (kWRec bytes) for weight rows 128t .. 128t+127 and block b, row r = n % 128:
 //   [0, 8192)       the e4m3 weight operand in the 64-byte-swizzled K-major layout: row r at
 //                   64 r, its 16-byte chunk c (k = 16c .. 16c+15) at chunk position c ^ ((r/2) % 4);
@@ -40,22 +42,27 @@ inline size_t align_ws(size_t v) { return (v + 255) & ~static_cast<size_t>(255);
 // Weight scales (read by the epilogue straight from memory): fp32 512 s_w[n,b] (the power
 // of two undoes the 2^-9) at [tile][b][r].
 // Rows past M or N are not read into any stored output; the weight side writes them as 0.
-constexpr int kTokRec = 18432;
-constexpr int kTokRx = 16384;
+constexpr int kTokRec = 18432;    // a 128-token record
+constexpr int kTokRx = 16384;     // its zero-point rows
+
+// Token tile width: 256 for the large-M contraction (N = 256 MMAs), 128 otherwise.
+inline int token_tile(int64_t M) { return M >= 4096 ? 256 : 128; }
 constexpr int kWRec = 10240;
 constexpr int kWZx = 8192;
 
-// Prepared activations (a caller-owned buffer): token records [ceil(M/128)][K/64], then
+// Prepared activations (a caller-owned buffer): token records [ceil(M/TW)][K/64], then
 // s_a fp32 [M] (omitted when the caller passes s_a).
 struct ActLayout {
     size_t rec = 0, s_a = 0, total = 0;
     int64_t tiles = 0;
+    int tw = 128;
 };
 
-inline ActLayout act_layout(int64_t M, int64_t K, bool with_sa) {
+inline ActLayout act_layout(int64_t M, int64_t K, bool with_sa, int tw) {
     ActLayout L;
-    L.tiles = (M + kTileT - 1) / kTileT;
-    size_t off = align_ws(static_cast<size_t>(L.tiles) * static_cast<size_t>(K / kBlock) * kTokRec);
+    L.tw = tw;
+    L.tiles = (M + tw - 1) / tw;
+    size_t off = align_ws(static_cast<size_t>(L.tiles) * static_cast<size_t>(K / kBlock) * 144u * static_cast<size_t>(tw));
     if (with_sa) {
         L.s_a = off;
         off = align_ws(off + static_cast<size_t>(M) * 4);
@@ -92,8 +99,9 @@ struct PrepArgs {
     int8_t* a_q_out = nullptr;
     float* s_a_out = nullptr;
     int32_t* rs_out = nullptr;
-    // GEMM-layout output: token records
+    // GEMM-layout output: token records of width tw
     uint8_t* trec = nullptr;
+    int tw = 128;
     // weight job (skipped when wrec == nullptr): rows n_first .. n_first + N - 1 of wq into
     // weight records; the zero-point rows and the scales (sc) only when s_w != nullptr
     const uint8_t* wq = nullptr;
@@ -111,7 +119,8 @@ cudaError_t launch_pack(const PrepArgs& a, cudaStream_t s);   // a_q -> token re
 // ---------------------------------------------------------------- GEMM
 struct GemmArgs {
     int64_t M = 0, N = 0, K = 0;       // output rows / columns (row stride N) and depth
-    const uint8_t* trec = nullptr;      // token records [ceil(M/128)][K/64]
+    const uint8_t* trec = nullptr;      // token records [ceil(M/tw)][K/64]
+    int tw = 128;                       // token tile (record width): 128 or 256
     const uint8_t* wrec = nullptr;      // weight records [ceil(N/128)][K/64]
     const float* sc = nullptr;          // weight scales [ceil(N/128)][K/64][128]
     const float* s_a = nullptr;
@@ -122,7 +131,7 @@ struct GemmArgs {
     uint64_t wait_limit_ns = 1000000000ull;
 };
 
-// Persistent launch over ceil(M/128) x ceil(N/128) output tiles on at most `num_sms` CTAs.
+// Persistent launch over ceil(M/tw) x ceil(N/128) output tiles on at most `num_sms` CTAs.
 cudaError_t launch_gemm(const GemmArgs& a, bool debug, int num_sms, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
 
