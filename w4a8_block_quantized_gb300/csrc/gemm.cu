@@ -79,6 +79,12 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kTmemCols == 512, "TMEM allocation");
 static_assert(kNBuf / 2 <= kStages, "a stage barrier carries a buffer release only after its previous phase");
 static_assert(kZeroBytes >= kTileW * 16 && kZeroBytes >= kTileT * 16, "zero half of the zero-point operands");
+// An mbarrier wait on parity P returns at once while the phase before P is still open, so a
+// warp that waits for phase k + 1 of a stage must itself have seen phase k complete.  With
+// the work items 2j + k dealt round-robin to the issuers, the issuer of a stage's slot k is
+// the same warp at every phase of that stage only if the issuer count divides the number of
+// slots per round of the stages.
+static_assert((2 * kStages) % kIssuers == 0, "each stage slot must have one issuer warp at every phase");
 
 // Grouped raster over the output tiles: groups of kGroup token tiles, the token tile
 // varying fastest inside a group, so the CTAs running at one time share token and weight
@@ -369,6 +375,7 @@ namespace wide {
 constexpr int kTN = 256;
 constexpr int kStages = 4;
 constexpr int kNBuf = 2;
+constexpr int kIssuers = 2;  // warps 1-2; each owns every other stage (warp 3 idles)
 constexpr int kTok = 144 * kTN;                 // token record of one block
 constexpr int kStageBytes = kTok + kWRec;
 constexpr int kOffZero = kStages * kStageBytes;
@@ -381,6 +388,8 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kNBuf * kTN == 512, "TMEM allocation");
 static_assert(kNBuf <= kStages, "a stage barrier carries a buffer release only after its previous phase");
 static_assert(kZeroBytes >= kTN * 16, "zero half of the token-side zero-point operand");
+// block g goes to issuer g % kIssuers: the same warp waits every phase of a stage, in order
+static_assert(kStages % kIssuers == 0 && kIssuers <= 3, "each stage must have one issuer warp at every phase");
 }  // namespace wide
 
 __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs args) {
@@ -411,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
             mbar_init(&empty[s], 1);
         }
         for (int i = 0; i < W::kNBuf; ++i) mbar_init(&tfull[i], 1);
-        for (int i = 0; i < kIssuers; ++i) mbar_init(&drain[i], 1);
+        for (int i = 0; i < W::kIssuers; ++i) mbar_init(&drain[i], 1);
         *abort_flag = 0u;
         fence_barrier_init();
     }
@@ -459,8 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
                         drain_wait(&full[q % W::kStages], (q / W::kStages) & 1, 100000000ull);
                 }
             }
-        } else {
-            // -------------------------------------------------------- MMA issue (warps 1-3)
+        } else if (warp <= W::kIssuers) {
+            // -------------------------------------------------------- MMA issue (warps 1-2)
             const int iw = warp - 1;
             constexpr uint32_t idesc = idesc_e4m3_f32(kTileW, W::kTN);
             const uint32_t zr = smem_u32(smem + W::kOffZero);
@@ -469,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
             const uint64_t dW0 = smem_desc(w0a, 512, kLayoutSw64);
             const uint64_t dBx0 = smem_desc(t0a + 128 * W::kTN, 128, 0, zr - (t0a + 128 * W::kTN));
             const uint64_t dAx0 = smem_desc(w0a + kWZx, 128, 0, zr - (w0a + kWZx));
-            for (uint32_t g = iw; g < total; g += kIssuers) {
+            for (uint32_t g = iw; g < total; g += W::kIssuers) {
                 const int s = static_cast<int>(g % W::kStages);
                 const uint32_t buf = g & 1u;
                 if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (g / W::kStages) & 1, ctl))) break;
