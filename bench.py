@@ -3,7 +3,7 @@
 
 A step is one pass of the whole hot path over one batch: for every linear of the
 workload, the fused call w4a8_prefill_linear (activation pre-pass + tensor-core
-contraction + epilogue), inputs resident in HBM.  L2 is flushed (256 MiB written)
+contraction + epilogue), inputs resident in HBM.  L2 is flushed (256 MiB written, then read back)
 before every timed step, outside the timed events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c1] [--impl ours|reference]
@@ -30,6 +30,7 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "W4A8 block64 prefill linear: effective TOPS & tok/s at M=512; % of INT8 peak"
+DECODE_METRIC = "W4A8 block64 decode linear: tokens/s at M=1 (weights streamed at 4.5 bits each); % of HBM"
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -38,7 +39,7 @@ def parse_args(argv=None):
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=20)
-    p.add_argument("--workload", default="c1", choices=["c0", "c1", "c2", "c3", "c4"])
+    p.add_argument("--workload", default="c1", choices=["c0", "c1", "c2", "c3", "c4", "d1", "d3", "d4"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
@@ -216,7 +217,19 @@ def run_bench(args):
     M = specs[0].M
     ops_per_step = sum(s.ops for s in specs)
     stream = torch.cuda.current_stream(device)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush_sink = torch.zeros((), dtype=torch.float32, device=device)
+
+    class _Flush:
+        @staticmethod
+        def zero_():
+            # write a buffer twice the size of L2, then read it back: the read evicts the
+            # written lines, so their write-back to HBM happens here and not inside the
+            # next timed kernel
+            flush_buf.zero_()
+            torch.sum(flush_buf.view(torch.float32), dim=0, out=flush_sink)
+
+    flush = _Flush()
 
     def step():
         for t in lin:
@@ -261,26 +274,50 @@ def run_bench(args):
                               "step_ms": [round(v, 4) for v in step_ms[:20]]}), flush=True)
         return
 
-    # ---------------- kernel-level timing (same stream, CUDA events): the GEMM alone
-    # through the split calls, and the pre-pass alone, each after an L2 flush.
+    # ---------------- kernel-level timing (same stream, CUDA events), each after an L2
+    # flush: the pre-pass alone, then the contraction alone -- through the split calls
+    # (prepared operands, tensor-core GEMM) or, for the few-token form, quant_pack +
+    # w4a8_linear (the weight-streaming kernel).
+    from w4a8_block_quantized_gb300 import synth
+    decode = M <= synth.DECODE_MAX_M
+    # few tokens of moderate depth: the fused call is one launch (the kernel quantizes)
+    one_launch = decode and all(binding.prefill_workspace_bytes(s.M, s.N, s.K) == 0 for s in specs)
     gemm_ms, prep_ms = [], []
     prepared = []
     for t in lin:
         s = t["spec"]
-        act = binding.prepare_activations(t["x"], stream=stream)
-        pw = binding.prepare_weights(t["wq"], t["s_w"], t["z_w"], stream=stream)
-        prepared.append((act, pw))
+        if one_launch:
+            prepared.append(None)
+        elif decode:
+            prepared.append(binding.quant_pack(t["x"], stream=stream) +
+                            (binding.workspace(0, device),))
+        else:
+            act = binding.prepare_activations(t["x"], stream=stream)
+            pw = binding.prepare_weights(t["wq"], t["s_w"], t["z_w"], stream=stream)
+            prepared.append((act, pw))
     kreps = max(20, min(args.steps, 200))
     for _ in range(kreps):
         g_ms = p_ms = 0.0
-        for t, (act, pw) in zip(lin, prepared):
+        for t, pre in zip(lin, prepared):
             s = t["spec"]
             e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             flush.zero_()
             e0.record(stream)
-            binding.prepare_activations(t["x"], act=act, stream=stream)
-            e1.record(stream)
-            binding.linear_prepared(act, pw, s.M, s.N, s.K, bias=t["bias"], y=t["y"], stream=stream)
+            if one_launch:
+                e1.record(stream)
+                binding.prefill_linear(t["x"], t["wq"], t["s_w"], t["z_w"], t["bias"], y=t["y"], ws=t["ws"],
+                                       stream=stream)
+            elif decode:
+                a_q, s_a, rs, ws0 = pre
+                binding.quant_pack(t["x"], a_q=a_q, a_scale=s_a, rowsum=rs, stream=stream)
+                e1.record(stream)
+                binding.linear(a_q, s_a, rs, t["wq"], t["s_w"], t["z_w"], t["bias"], y=t["y"], ws=ws0,
+                               stream=stream)
+            else:
+                act, pw = pre
+                binding.prepare_activations(t["x"], act=act, stream=stream)
+                e1.record(stream)
+                binding.linear_prepared(act, pw, s.M, s.N, s.K, bias=t["bias"], y=t["y"], stream=stream)
             e2.record(stream)
             e2.synchronize()
             p_ms += e0.elapsed_time(e1)
@@ -296,8 +333,18 @@ def run_bench(args):
     tensor_peak = bf16_tf * 2.0 / 2.0
     gemm_ops = ops_per_step / len(lin)
     gemm_tops = gemm_ops / (gemm_avg * 1e-3) / 1e12
-    # x read, two e4m3 planes written, s_a, and one 16-byte zero-point operand entry per 64-block
-    prep_bytes = sum(s.M * s.K * 4 + s.M * s.K * 2 + s.M * 4 + s.M * (s.K // 64) * 16 for s in specs) / len(lin)
+    if decode:
+        # x read; a_q, s_a and the int32 row sums written (API layout)
+        prep_bytes = sum(s.M * s.K * 4 + s.M * s.K + s.M * 4 + s.M * (s.K // 64) * 4 for s in specs) / len(lin)
+        # packed weights + s_w + z_w, the activations (x when the kernel quantizes, else the
+        # codes, row sums and scales), bias and y
+        gemv_bytes = sum(synth.weight_bytes(s) + (4 * s.M * s.K if one_launch else
+                                                  s.M * s.K + s.M * (s.K // 64) * 4 + s.M * 4) +
+                         (4 * s.N if s.bias else 0) + 4 * s.M * s.N for s in specs) / len(lin)
+        gemv_gbs = gemv_bytes / (gemm_avg * 1e-3) / 1e9
+    else:
+        # x read, two e4m3 planes written, s_a, and one 16-byte zero-point operand entry per 64-block
+        prep_bytes = sum(s.M * s.K * 4 + s.M * s.K * 2 + s.M * 4 + s.M * (s.K // 64) * 16 for s in specs) / len(lin)
     prep_gbs = prep_bytes / (prep_avg * 1e-3) / 1e9
 
     # ---------------- end to end through the C ABI with host buffers
@@ -327,11 +374,35 @@ def run_bench(args):
         cpu = cpu_baseline(lin, specs, args.cpu_seconds)
 
     clocks = clk.summary(t_start, t_end)
+    if decode:
+        roofline = {"bound": "hbm", "kernel": "gemv_kernel (packed u4 weights streamed, dp4a blocks + f32 epilogue)",
+                    "achieved": round(gemv_gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
+                    "frac": round(gemv_gbs / hbm_gbs, 4), "traffic": None, "peak_source": peak_src,
+                    "bytes_per_launch": int(gemv_bytes), "gemv_us_per_launch": round(gemm_avg * 1e3, 3)}
+    else:
+        roofline = {"bound": "tensor", "kernel": "gemm_kernel (tcgen05 kind::f8f6f4 + epilogue)",
+                    "achieved": round(gemm_tops, 2), "peak": round(tensor_peak, 1), "unit": "TOPS",
+                    "frac": round(gemm_tops / tensor_peak, 4),
+                    "traffic": None if args.shape else recorded_traffic(args.workload),
+                    "peak_source": f"{peak_src} bf16 burst x2 (fp8 nominal ratio) /2 (two e4m3 MACs per int8 MAC)",
+                    "gemm_us_per_launch": round(gemm_avg * 1e3, 3)}
+    e2e_tops = whole_job_rate(ops_per_step * e2e_steps, world, e2e_s) / 1e12
+    if decode:
+        # a decode step is one token (per sequence of the batch) through every linear:
+        # the headline is tokens per second, the TOPS ride along
+        metric, unit, value, e2e_value = DECODE_METRIC, "tok/s", round(tok_s, 1), \
+            round(whole_job_rate(M * e2e_steps, world, e2e_s), 1)
+        if cpu is not None:
+            cpu = dict(cpu, value=round(cpu["value"] * 1e12 / (ops_per_step / M), 3), unit="tok/s",
+                       tops=cpu["value"])
+    else:
+        metric, unit, value, e2e_value = METRIC, "TOPS", round(value_tops, 3), round(e2e_tops, 3)
     out = {
-        "metric": METRIC,
-        "value": round(value_tops, 3),
-        "unit": "TOPS",
+        "metric": metric,
+        "value": value,
+        "unit": unit,
         "tok_s": round(tok_s, 1),
+        "tops": round(value_tops, 4),
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -339,26 +410,24 @@ def run_bench(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3xe4m3->f32 (exact int8 x u4 blocks), f32 epilogue",
+        "dtype": ("int8 x u4 dp4a -> exact int32 blocks, f32 epilogue" if decode else
+                  "e4m3xe4m3->f32 (exact int8 x u4 blocks), f32 epilogue"),
         "data": "synthetic (seeded Philox; no model weights)",
         "config": {"workload": f"{args.workload}: {title}",
                    "linears": [{"name": s.name, "M": s.M, "K": s.K, "N": s.N, "bias": s.bias} for s in specs],
                    "tokens_per_step": M, "ops_per_step": ops_per_step,
-                   "l2": "flushed before every timed step (256 MiB memset, outside the timed events)",
+                   "l2": "flushed before every timed step (256 MiB written, then read back; outside the timed events)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "kernel": "gemm_kernel (tcgen05 kind::f8f6f4 + epilogue)",
-                     "achieved": round(gemm_tops, 2), "peak": round(tensor_peak, 1), "unit": "TOPS",
-                     "frac": round(gemm_tops / tensor_peak, 4),
-                     "traffic": None if args.shape else recorded_traffic(args.workload),
-                     "peak_source": f"{peak_src} bf16 burst x2 (fp8 nominal ratio) /2 (two e4m3 MACs per int8 MAC)",
-                     "gemm_us_per_launch": round(gemm_avg * 1e3, 3)},
-        "prepass": {"bound": "hbm", "achieved": round(prep_gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
-                    "frac": round(prep_gbs / hbm_gbs, 4), "us_per_launch": round(prep_avg * 1e3, 3),
-                    "peak_source": peak_src},
-        "e2e": {"value": round(whole_job_rate(ops_per_step * e2e_steps, world, e2e_s) / 1e12, 3), "unit": "TOPS",
+        "roofline": roofline,
+        "prepass": ({"fused": "the few-token kernel quantizes the rows itself (one launch per linear)"}
+                    if one_launch else
+                    {"bound": "hbm", "achieved": round(prep_gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": round(prep_gbs / hbm_gbs, 4), "us_per_launch": round(prep_avg * 1e3, 3),
+                     "peak_source": peak_src}),
+        "e2e": {"value": e2e_value, "unit": unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3 / e2e_steps, 4)},
-        "gpu_launches": args.steps * 2 * len(lin),
+        "gpu_launches": args.steps * (1 if one_launch else 2) * len(lin),
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
@@ -432,16 +501,19 @@ def run_reference(args):
     value = ops / dt / 1e12
     toks = args.steps * sum(len(r) for r in rows) / len(rows) / dt
     sample = "; ".join(f"{s.name}: {len(r)}/{s.M} evenly spaced rows" for s, r in zip(specs, rows))
+    metric, unit = METRIC, "TOPS"
+    if specs[0].M <= synth.DECODE_MAX_M:
+        metric, unit, value = DECODE_METRIC, "tok/s", toks
     out = {
-        "metric": METRIC, "value": round(value, 6), "unit": "TOPS", "tok_s": round(toks, 2), "impl": "reference",
+        "metric": metric, "value": round(value, 6), "unit": unit, "tok_s": round(toks, 2), "impl": "reference",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int32/int64 blocks, f64 output", "data": "synthetic (seeded Philox)",
         "config": {"workload": f"{args.workload}: {title}",
                    "linears": [{"name": s.name, "M": s.M, "K": s.K, "N": s.N, "bias": s.bias} for s in specs]},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TOPS", "cores": oracle.num_threads(), "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": sample},
-        "e2e": {"value": round(value, 6), "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
 

@@ -66,11 +66,20 @@ typedef enum {
 int w4a8_quant_pack(const float *x, int64_t M, int64_t K,
                     int8_t *a_q, float *a_scale, int32_t *rowsum, void *stream);
 
+/* Few-token (decode) form.  For M <= W4A8_DECODE_MAX_M, w4a8_linear and
+ * w4a8_prefill_linear stream the packed weights once (wq, w_scale and w_zero as given:
+ * 4.5 bits per weight) and form each block's exact integer product on the CUDA cores
+ * (section 4's decode discussion: a decode step costs one read of the weights).  The
+ * result obeys the same definition and tolerance as the tensor-core form; the fp32 sums
+ * are taken in a different order, so the two forms need not agree bit for bit. */
+#define W4A8_DECODE_MAX_M 8
+
 /* Quantized linear from pre-quantized activations (section 3 eq. (2), section 4
  * steps 2-3): block-64 integer contraction on the tensor cores, then the scale /
  * zero-point / bias epilogue writing fp32 y [M][N] directly.
  * workspace: at least w4a8_linear_workspace_bytes(M, N, K) bytes (the activation
- * operand re-encoded for the tensor cores). */
+ * operand re-encoded for the tensor cores).  For M <= W4A8_DECODE_MAX_M that size is 0
+ * and `workspace` may be NULL. */
 int w4a8_linear(const int8_t *a_q, const float *a_scale, const int32_t *rowsum,
                 const uint8_t *wq, const uint16_t *w_scale, const uint16_t *w_zero,
                 const float *bias, float *y, int64_t M, int64_t N, int64_t K,
@@ -79,6 +88,10 @@ int w4a8_linear(const int8_t *a_q, const float *a_scale, const int32_t *rowsum,
 /* Fused prefill linear: the pre-pass writes the tensor-core operand, the activation
  * scales and the row sums straight into the workspace (no int8 a_q array), then
  * the linear runs.  Same result, bit for bit, as w4a8_quant_pack + w4a8_linear.
+ * For M <= W4A8_DECODE_MAX_M the few-token form runs: with M * K <= 16384 in one launch
+ * that quantizes the rows itself (workspace size 0, `workspace` may be NULL), otherwise
+ * after the pre-pass, whose outputs (a_q, a_scale, rowsum in the API layout) the workspace
+ * holds.
  * workspace: at least w4a8_prefill_workspace_bytes(M, N, K) bytes. */
 int w4a8_prefill_linear(const float *x, const uint8_t *wq, const uint16_t *w_scale,
                         const uint16_t *w_zero, const float *bias, float *y,
@@ -98,7 +111,8 @@ int w4a8_prefill_linear(const float *x, const uint8_t *wq, const uint16_t *w_sca
  * The buffers are opaque; their contents are only valid for the same M / N / K.  wq, the
  * scales and the zeros are not read again after w4a8_prepare_weights.
  * prepare_activations + prepare_weights + linear_prepared equals w4a8_prefill_linear
- * bit for bit. */
+ * bit for bit for M > W4A8_DECODE_MAX_M; for fewer tokens linear_prepared still runs the
+ * tensor-core form (the prepared weights hold no packed copy to stream). */
 int w4a8_prepare_activations(const float *x, int64_t M, int64_t K, void *act, size_t act_bytes,
                              void *stream);
 int w4a8_prepare_weights(const uint8_t *wq, const uint16_t *w_scale, const uint16_t *w_zero,

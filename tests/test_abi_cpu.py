@@ -44,7 +44,7 @@ def test_status_strings(lib):
         s = b.status_string(code)
         assert s and s != "unknown status"
     assert b.status_string(12345) == "unknown status"
-    assert lib.w4a8_abi_version() == 200
+    assert lib.w4a8_abi_version() == 201
 
 
 def test_shape_checks_need_no_gpu(lib):
@@ -63,9 +63,12 @@ def test_shape_checks_need_no_gpu(lib):
     assert lib.w4a8_linear(dummy, dummy, dummy, dummy, dummy, dummy, None, dummy, 8, 8, 96, dummy, 1 << 20,
                            None) == b.W4A8_ERR_SHAPE
     # workspace too small is reported before any launch
-    need = lib.w4a8_prefill_workspace_bytes(8, 8, 64)
-    assert lib.w4a8_prefill_linear(dummy, dummy, P(32), P(32), None, dummy, 8, 8, 64, dummy, need - 1,
-                                   None) == b.W4A8_ERR_WORKSPACE
+    # (the tensor-core form, and the few-token form after a separate pre-pass)
+    for M, N, K in ((16, 8, 64), (8, 8, 4096)):
+        need = lib.w4a8_prefill_workspace_bytes(M, N, K)
+        assert need > 0
+        assert lib.w4a8_prefill_linear(dummy, dummy, P(32), P(32), None, dummy, M, N, K, dummy, need - 1,
+                                       None) == b.W4A8_ERR_WORKSPACE
     # debug window outside the problem
     assert lib.w4a8_debug_block_acc(dummy, dummy, 8, 8, 64, 4, 8, 0, 8, dummy, dummy, 1 << 20,
                                     None) == b.W4A8_ERR_SHAPE
@@ -83,3 +86,21 @@ def test_workspace_sizes(lib):
     assert lib.w4a8_linear_workspace_bytes(0, N, K) == 0
     assert lib.w4a8_linear_workspace_bytes(M, N, 100) == ctypes.c_size_t(-1).value
     assert lib.w4a8_debug_workspace_bytes(7, 9, 128) >= 7 * 256 + 9 * 128
+
+
+def test_few_token_workspace_sizes(lib):
+    """Up to W4A8_DECODE_MAX_M tokens the linear needs no scratch; the fused call none when
+    the kernel quantizes the rows itself (M * K <= 16384), else the pre-pass outputs in the
+    API layout; one token more switches to the tensor-core form."""
+    N = 3072
+    for M in range(1, 9):
+        for K in (1024, 2048, 4096, 16384):
+            nb = K // 64
+            assert lib.w4a8_linear_workspace_bytes(M, N, K) == 0
+            pre = lib.w4a8_prefill_workspace_bytes(M, N, K)
+            if M * K <= 16384:
+                assert pre == 0
+            else:
+                assert M * K + 4 * M + 4 * M * nb <= pre <= M * K + 4 * M + 4 * M * nb + 3 * 256
+    assert lib.w4a8_linear_workspace_bytes(9, N, 1024) >= N * 1024
+    assert lib.w4a8_prefill_workspace_bytes(9, N, 1024) >= N * 1024

@@ -335,3 +335,55 @@ def test_repeated_launches_complete_and_identical(M, K, N, launches):
     rows = np.linspace(0, M - 1, 6).astype(np.int64)
     y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"][rows], d["wq"], d["s_w"], d["z_w"], d["bias"])
     check_y(y0[torch.from_numpy(rows).to(dev())], y_ref, bound, f"rows of {M}x{K}x{N}")
+
+
+# ------------------------------------------------------------------ few-token (decode) form
+@pytest.mark.parametrize("M,K,N,bias", [(1, 64, 1, True), (1, 1024, 3072, True), (1, 1088, 257, False),
+                                        (2, 2048, 1023, True), (3, 6144, 2048, False), (4, 192, 5, True),
+                                        (5, 3136, 130, False), (6, 4096, 64, True), (7, 16384, 33, True),
+                                        (8, 2048, 6144, False), (1, 20480, 3, True), (8, 64, 2, False)])
+def test_decode_shapes(M, K, N, bias):
+    """M <= 8 streams the packed weights: K chunk tails (K % 1024 != 0), odd N (the last row
+    pair half empty), N below a CTA's rows, every token count; every output against the
+    oracle, the fused call equal to quant_pack + linear bit for bit, and w4a8_linear with no
+    workspace at all."""
+    b = B()
+    d = synth.random_small(M, K, N, seed=11 * M + K + N, bias=bias)
+    g = inputs_to_dev(d)
+    y_fused = b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"])
+    a_q, s_a, rs = b.quant_pack(g["x"])
+    y_sep = torch.empty_like(y_fused)
+    rc = b.load().w4a8_linear(b._ptr(a_q), b._ptr(s_a), b._ptr(rs), b._ptr(g["wq"]), b._ptr(g["s_w"]),
+                              b._ptr(g["z_w"]), b._ptr(g["bias"]), b._ptr(y_sep), M, N, K, None, 0,
+                              b._stream(None))
+    assert rc == 0
+    y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
+    check_y(y_fused, y_ref, bound, f"decode {M}x{K}->{N}")
+    assert torch.equal(y_fused, y_sep), "fused and separate calls differ"
+    assert b.sync_status() == 0
+
+
+@pytest.mark.parametrize("K,N", [(4096, 14336), (14336, 4096), (2048, 6144), (6144, 2048)])
+def test_decode_model_shapes_full(K, N):
+    """One token through the 7B- and 1.7B-class projections, every output against the oracle;
+    the no-alloc entry point gives the same bits."""
+    b = B()
+    d = synth.make_linear(synth.LinearSpec("decode", 1, K, N, True))
+    g = inputs_to_dev(d)
+    y = b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"])
+    y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
+    check_y(y, y_ref, bound, f"decode 1x{K}->{N}")
+    assert torch.equal(b.prefill_linear_noalloc(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"]), y)
+
+
+def test_decode_boundary_tokens():
+    """8 tokens take the weight-streaming form, 9 the tensor-core form: both within the
+    tolerance of the same definition on the same rows."""
+    b = B()
+    d = synth.random_small(9, 2048, 777, seed=99, bias=True)
+    g = inputs_to_dev(d)
+    y9 = b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"])
+    y8 = b.prefill_linear(g["x"][:8].contiguous(), g["wq"], g["s_w"], g["z_w"], g["bias"])
+    y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
+    check_y(y9, y_ref, bound, "9 tokens")
+    check_y(y8, y_ref[:8], bound[:8], "8 tokens")

@@ -113,6 +113,39 @@ void set_weight_job(PrepArgs* p, const uint8_t* wq, const uint16_t* w_scale, con
     p->sc = reinterpret_cast<float*>(wrec + w_layout(N, K).sc);
 }
 
+// Scratch bytes of the two workspace-taking entry points.  The few-token form needs none
+// for w4a8_linear, and for the fused call none when the kernel quantizes the rows itself,
+// else the pre-pass outputs; the tensor-core form needs the re-encoded activations and the
+// prepared weights.
+bool few_tokens(int64_t M, int64_t K) { return M <= kGemvMaxM && gemv_supported(M, K); }
+size_t linear_ws(int64_t M, int64_t N, int64_t K) {
+    return few_tokens(M, K) ? 0 : call_layout(M, N, K, false).total;
+}
+size_t prefill_ws(int64_t M, int64_t N, int64_t K) {
+    if (few_tokens(M, K)) return gemv_quantizes(M, K) ? 0 : decode_layout(M, K).total;
+    return call_layout(M, N, K, true).total;
+}
+
+// The few-token kernel from x (it quantizes) or from the pre-pass outputs.
+int run_gemv(const float* x, const int8_t* a_q, const float* s_a, const int32_t* rs, const uint8_t* wq,
+             const uint16_t* w_scale, const uint16_t* w_zero, const float* bias, float* y, int64_t M, int64_t N,
+             int64_t K, const DeviceInfo& d, cudaStream_t st) {
+    GemvArgs g;
+    g.x = x;
+    g.a_q = a_q;
+    g.s_a = s_a;
+    g.rs = rs;
+    g.wq = wq;
+    g.s_w = w_scale;
+    g.z_w = w_zero;
+    g.bias = bias;
+    g.y = y;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    return launch_gemv(g, d.num_sms, d.status, st) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace w4a8
 
@@ -120,7 +153,7 @@ using namespace w4a8;
 
 extern "C" {
 
-int w4a8_abi_version(void) { return 200; }
+int w4a8_abi_version(void) { return 201; }
 
 const char* w4a8_status_string(int status) {
     switch (status) {
@@ -140,13 +173,13 @@ const char* w4a8_status_string(int status) {
 size_t w4a8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (check_shape(M, N, K) != W4A8_OK) return static_cast<size_t>(-1);
     if (M == 0 || N == 0) return 0;
-    return call_layout(M, N, K, false).total;
+    return linear_ws(M, N, K);
 }
 
 size_t w4a8_prefill_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (check_shape(M, N, K) != W4A8_OK) return static_cast<size_t>(-1);
     if (M == 0 || N == 0) return 0;
-    return call_layout(M, N, K, true).total;
+    return prefill_ws(M, N, K);
 }
 
 size_t w4a8_debug_workspace_bytes(int64_t m_cnt, int64_t n_cnt, int64_t K) {
@@ -195,12 +228,17 @@ int w4a8_linear(const int8_t* a_q, const float* a_scale, const int32_t* rowsum, 
     if (!aligned(a_q, 16) || !aligned(wq, 16) || !aligned(y, 16) || !aligned(a_scale, 4) || !aligned(rowsum, 4) ||
         !aligned(w_scale, 2) || !aligned(w_zero, 2) || (bias && !aligned(bias, 4)))
         return W4A8_ERR_ALIGN;
+    DeviceInfo* d = nullptr;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (few_tokens(M, K)) {
+        // few-token form: no scratch, the workspace is not touched
+        if ((rc = current_device(&d)) != W4A8_OK) return rc;
+        return run_gemv(nullptr, a_q, a_scale, rowsum, wq, w_scale, w_zero, bias, y, M, N, K, *d, st);
+    }
     const CallLayout L = call_layout(M, N, K, false);
     if (!workspace || workspace_bytes < L.total) return W4A8_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return W4A8_ERR_ALIGN;
-    DeviceInfo* d = nullptr;
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     PrepArgs p;
     p.a_q_in = a_q;
@@ -223,13 +261,31 @@ int w4a8_prefill_linear(const float* x, const uint8_t* wq, const uint16_t* w_sca
     if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(y, 16) || !aligned(w_scale, 2) || !aligned(w_zero, 2) ||
         (bias && !aligned(bias, 4)))
         return W4A8_ERR_ALIGN;
-    const CallLayout L = call_layout(M, N, K, true);
-    if (!workspace || workspace_bytes < L.total) return W4A8_ERR_WORKSPACE;
-    if (!aligned(workspace, 16)) return W4A8_ERR_ALIGN;
+    const size_t need = prefill_ws(M, N, K);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return W4A8_ERR_WORKSPACE;
+    if (need > 0 && !aligned(workspace, 16)) return W4A8_ERR_ALIGN;
     DeviceInfo* d = nullptr;
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (few_tokens(M, K) && gemv_quantizes(M, K)) {
+        // few-token form, one launch: the weight-streaming kernel quantizes x itself
+        return run_gemv(x, nullptr, nullptr, nullptr, wq, w_scale, w_zero, bias, y, M, N, K, *d, st);
+    }
+    if (few_tokens(M, K)) {
+        // few-token form: the pre-pass in the API layout, then the weight-streaming kernel
+        const DecodeLayout D = decode_layout(M, K);
+        PrepArgs p;
+        p.x = x;
+        p.M = M;
+        p.K = K;
+        p.a_q_out = reinterpret_cast<int8_t*>(ws + D.a_q);
+        p.s_a_out = reinterpret_cast<float*>(ws + D.s_a);
+        p.rs_out = reinterpret_cast<int32_t*>(ws + D.rs);
+        if (launch_quant(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
+        return run_gemv(nullptr, p.a_q_out, p.s_a_out, p.rs_out, wq, w_scale, w_zero, bias, y, M, N, K, *d, st);
+    }
+    const CallLayout L = call_layout(M, N, K, true);
     float* s_a = reinterpret_cast<float*>(ws + L.act.s_a);
     PrepArgs p;
     p.x = x;
@@ -396,8 +452,7 @@ int w4a8_prefill_linear_noalloc(const float* x, const uint8_t* wq, const uint16_
     int rc = check_shape(M, N, K);
     if (rc != W4A8_OK) return rc;
     if (M == 0 || N == 0) return W4A8_OK;
-    const size_t need = call_layout(M, N, K, true).total;
-    if (need > W4A8_NOALLOC_SCRATCH_BYTES) return W4A8_ERR_SCRATCH_LIMIT;
+    if (prefill_ws(M, N, K) > W4A8_NOALLOC_SCRATCH_BYTES) return W4A8_ERR_SCRATCH_LIMIT;
     DeviceInfo* d = nullptr;
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
     uint8_t* scratch = nullptr;

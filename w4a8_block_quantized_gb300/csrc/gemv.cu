@@ -1,0 +1,526 @@
+// gemv.cu -- the few-token (decode) form of the block-64 W4A8 linear.
+//
+// "MNN LLM inference on the SpacemiT K3", section 3 eqs. (2)-(3) for the arithmetic; section
+// 4's decode discussion for the shape of the work: one token per step, so the cost is one
+// read of the packed weights with their block scales and zeros (tokens/s = bandwidth /
+// weight bytes), streamed through a small on-chip buffer in ping-pong fashion while the
+// previous piece is reduced, and the output written directly in fp32.
+//
+// With M <= kGemvMaxM tokens the contraction has no reuse worth a tensor-core tile: every
+// weight is read once from HBM and used M times.  The weights are streamed as given (4 bits
+// per weight + one fp16 s_w and one fp16 z_w per 64 weights = 4.5 bits per weight).
+//
+// Persistent CTAs, one per SM, each walking row tiles t = blockIdx.x, blockIdx.x + grid, ...
+//   warp 8       producer: per tile three bulk copies into a ring of shared-memory stages --
+//                the tile's packed rows (contiguous: rows are K/2 bytes apart) and the
+//                16-byte-aligned spans of memory holding its s_w and z_w rows (a span may
+//                start and end up to 15 bytes outside the rows; a 16-byte granule of device
+//                memory never straddles a page, so those bytes are always readable and are
+//                simply not used).
+//   warps 0-7    consumers.  A tile of TR >= 8 rows gives each warp TR/8 rows; a tile of
+//                TR < 8 rows gives each row 8/TR warps that split its K chunks.  A lane owns
+//                one 64-block of a row in every chunk of 32 blocks (2048 weights).
+// The activations are staged once per CTA in shared memory, per token and chunk as four
+// planes of 16 bytes per lane (plane p: codes 16p .. 16p+15 of the lane's block, each group
+// of 8 codes as its even-k bytes then its odd-k bytes -- the order of the packed weight
+// nibbles), with the block row sums as floats.  Either the CTA quantizes the rows itself
+// from x (few tokens of moderate depth: the pre-pass's quantizer, quant_math.cuh, so the
+// codes equal the pre-pass's bit for bit; the producer's first bulk copy brings x in, ahead
+// of the weights) or it reads the pre-pass's outputs.  Per weight
+// word: the low nibbles masked give the even codes for a signed dp4a; the high nibbles
+// masked (16 q, kept unshifted) go through an unsigned x signed dp4a, the sum shifted right
+// by 4 once per block; four independent accumulators.  A block's int32 product is exact;
+// the epilogue forms t = acc - z_w rs with one fma and adds s_w t.  Sums: lane, then warp,
+// then (split rows) the row's warps in a fixed order; y = s_a sum + bias.
+//
+// Every wait is bounded; a CTA that gives up records a timeout and unwinds.
+#include <cuda_fp16.h>
+
+#include "quant_math.cuh"
+#include "sm103_ptx.cuh"
+#include "w4a8_internal.h"
+
+namespace w4a8 {
+namespace {
+
+constexpr int kCW = 8;                     // consumer warps
+constexpr int kGThreads = (kCW + 1) * 32;  // + the producer warp
+constexpr int kChunkBlocks = 32;           // 64-blocks per row per warp step (one per lane)
+constexpr int kChunkAct = kChunkBlocks * 64;  // staged activation bytes per token and chunk
+constexpr int kMaxStages = 8;
+constexpr int kSmemCap = 226 * 1024;  // dynamic; the static arrays fit in the last KiB
+constexpr int kBarStage = 9;          // named barrier: the consumers while staging
+// named barriers 1..4: the warps sharing one row of a tile of fewer than 8 rows
+
+// Shared-memory plan of one launch (computed on the host; identical for every CTA).
+struct GemvPlan {
+    int tr = 8;               // rows per tile
+    int wpr = 1;              // warps per row (tr < 8)
+    int ns = 2;               // stages
+    int chunks = 1;           // ceil(K / 2048)
+    uint32_t act_stride = 0;  // staged activation bytes per token (chunks * 2048)
+    uint32_t rs_off = 0, x_off = 0, bar_off = 0, stage_off = 0;  // x_off: the fp32 rows (quantizing kernel)
+    uint32_t stage_bytes = 0, w_bytes = 0, sz_bytes = 0;  // a stage; its weight part; one s_w / z_w slot
+    uint32_t smem = 0;
+    int64_t tiles = 0;
+    int grid = 0;
+};
+
+constexpr uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+bool make_plan(int64_t M, int64_t N, int64_t K, bool quantize, int num_sms, GemvPlan* out) {
+    GemvPlan best;
+    int64_t best_cost = -1;
+    const int64_t nb = K / kBlock;
+    const int chunks = static_cast<int>((nb + kChunkBlocks - 1) / kChunkBlocks);
+    const int64_t act_stride = static_cast<int64_t>(chunks) * kChunkAct;
+    const int64_t act = M * act_stride, rs = M * nb * 4, xb = quantize ? M * K * 4 : 0;
+    if (act + rs + xb > kSmemCap) return false;
+    const uint32_t rs_off = align_up(static_cast<uint32_t>(act), 128);
+    const uint32_t x_off = align_up(rs_off + static_cast<uint32_t>(rs), 128);
+    const uint32_t bar_off = align_up(x_off + static_cast<uint32_t>(xb), 128);
+    const uint32_t stage_off = align_up(bar_off + (2 * kMaxStages + 1) * 8 + 16, 1024);
+    for (int tr : {32, 16, 8, 4, 2, 1}) {
+        if (tr > 8 && M > 2) continue;  // more rows per warp only for one or two tokens
+        const uint32_t wb = align_up(static_cast<uint32_t>(tr * K / 2), 16);
+        const uint32_t sz = align_up(static_cast<uint32_t>(tr * nb * 2 + 32), 16);
+        const uint32_t stage = align_up(wb + 2 * sz, 128);
+        const int64_t room = kSmemCap - 1024 - static_cast<int64_t>(stage_off);
+        int64_t ns = room / stage;
+        if (ns > kMaxStages) ns = kMaxStages;
+        if (ns < 2) continue;
+        const int64_t tiles = (N + tr - 1) / tr;
+        const int64_t grid = tiles < num_sms ? tiles : num_sms;
+        const int64_t waves = (tiles + grid - 1) / grid;
+        // bytes streamed by the busiest CTA, plus a fixed cost per tile (barriers, sums)
+        const int64_t cost = waves * (static_cast<int64_t>(stage) + 4096);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best.tr = tr;
+            best.wpr = tr >= 8 ? 1 : 8 / tr;
+            best.ns = static_cast<int>(ns);
+            best.chunks = chunks;
+            best.act_stride = static_cast<uint32_t>(act_stride);
+            best.rs_off = rs_off;
+            best.x_off = x_off;
+            best.bar_off = bar_off;
+            best.stage_off = stage_off;
+            best.stage_bytes = stage;
+            best.w_bytes = wb;
+            best.sz_bytes = sz;
+            best.smem = stage_off + static_cast<uint32_t>(ns) * stage + 1024;  // + base alignment slack
+            best.tiles = tiles;
+            best.grid = static_cast<int>(grid);
+        }
+    }
+    if (best_cost < 0) return false;
+    *out = best;
+    return true;
+}
+
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+    return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
+}
+// unsigned bytes of a x signed bytes of b
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint16_t lds16(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+// The 16-byte-aligned span of device memory holding elements [e0, e1) of a fp16 array: its
+// start, its length and the offset of element e0 inside it.
+__device__ __forceinline__ void half_span(const uint16_t* base, int64_t e0, int64_t e1, const uint8_t*& src,
+                                          uint32_t& bytes, uint32_t& skew) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(base + e0), a1 = reinterpret_cast<uintptr_t>(base + e1);
+    const uintptr_t s0 = a0 & ~uintptr_t(15), s1 = (a1 + 15) & ~uintptr_t(15);
+    src = reinterpret_cast<const uint8_t*>(s0);
+    bytes = static_cast<uint32_t>(s1 - s0);
+    skew = static_cast<uint32_t>(a0 - s0);
+}
+
+// Low bytes of four int codes, c0 in byte 0.
+__device__ __forceinline__ uint32_t pack4(int c0, int c1, int c2, int c3) {
+    return __byte_perm(__byte_perm(c0, c1, 0x0040), __byte_perm(c2, c3, 0x0040), 0x5410);
+}
+
+// Staged plane of 16 codes k = 16p .. 16p+15 of a block: {E, O} of codes 0-7 then of 8-15
+// (E: the even codes of the group of 8, O: the odd ones), from four words of codes in k order.
+__device__ __forceinline__ uint4 plane_of(uint32_t n0, uint32_t n1, uint32_t n2, uint32_t n3) {
+    return make_uint4(__byte_perm(n0, n1, 0x6420), __byte_perm(n0, n1, 0x7531), __byte_perm(n2, n3, 0x6420),
+                      __byte_perm(n2, n3, 0x7531));
+}
+
+// Exact product of one block: W0 / W1 the block's 32 packed bytes (codes 0-31 / 32-63 of
+// the block, even k in the low nibbles), P the four staged planes of the token.
+__device__ __forceinline__ int block_dot(const uint4& W0, const uint4& W1, const uint4 (&P)[4]) {
+    constexpr uint32_t kLo = 0x0F0F0F0Fu, kHi = 0xF0F0F0F0u;
+    int la = dp4a_ss(W0.x & kLo, P[0].x, 0), ha = dp4a_us(W0.x & kHi, P[0].y, 0);
+    int lb = dp4a_ss(W0.y & kLo, P[0].z, 0), hb = dp4a_us(W0.y & kHi, P[0].w, 0);
+    la = dp4a_ss(W0.z & kLo, P[1].x, la);
+    ha = dp4a_us(W0.z & kHi, P[1].y, ha);
+    lb = dp4a_ss(W0.w & kLo, P[1].z, lb);
+    hb = dp4a_us(W0.w & kHi, P[1].w, hb);
+    la = dp4a_ss(W1.x & kLo, P[2].x, la);
+    ha = dp4a_us(W1.x & kHi, P[2].y, ha);
+    lb = dp4a_ss(W1.y & kLo, P[2].z, lb);
+    hb = dp4a_us(W1.y & kHi, P[2].w, hb);
+    la = dp4a_ss(W1.z & kLo, P[3].x, la);
+    ha = dp4a_us(W1.z & kHi, P[3].y, ha);
+    lb = dp4a_ss(W1.w & kLo, P[3].z, lb);
+    hb = dp4a_us(W1.w & kHi, P[3].w, hb);
+    return (la + lb) + ((ha + hb) >> 4);  // the high sums are 16 x (odd-code products), exact
+}
+
+template <int MT, int RW>
+__global__ void __launch_bounds__(kGThreads, 1)
+    gemv_kernel(const GemvArgs a, const GemvPlan P, uint32_t* status, uint64_t wait_limit_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + P.bar_off);
+    uint64_t* empty = full + kMaxStages;
+    uint64_t* xbar = empty + kMaxStages;  // the fp32 rows (quantizing kernel)
+    volatile uint32_t* abort_flag = reinterpret_cast<uint32_t*>(xbar + 1);
+    __shared__ float red[2][kCW][MT];
+    __shared__ float amax_red[2][kCW];
+    __shared__ float sa_sm[MT];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t K = a.K, N = a.N, nb = K / kBlock;
+    const int ns = P.ns, tr = P.tr;
+    const uint32_t my_tiles =
+        P.tiles > blockIdx.x ? static_cast<uint32_t>((P.tiles - 1 - blockIdx.x) / gridDim.x + 1) : 0u;
+    const WaitCtl ctl{abort_flag, status, wait_limit_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ns; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCW);
+        }
+        mbar_init(xbar, 1);
+        *abort_flag = 0u;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kCW) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            auto tile_src = [&](uint32_t i, const uint8_t*& w, uint32_t& wbytes, const uint8_t*& ss, uint32_t& sbytes,
+                                const uint8_t*& zs, uint32_t& zbytes) {
+                const int64_t n0 = (blockIdx.x + static_cast<int64_t>(i) * gridDim.x) * tr;
+                const int64_t rows = N - n0 < tr ? N - n0 : tr;
+                uint32_t skew;
+                w = a.wq + n0 * (K / 2);
+                wbytes = static_cast<uint32_t>(rows * (K / 2));
+                half_span(a.s_w, n0 * nb, (n0 + rows) * nb, ss, sbytes, skew);
+                half_span(a.z_w, n0 * nb, (n0 + rows) * nb, zs, zbytes, skew);
+            };
+            const uint8_t *w, *ss, *zs;
+            uint32_t wbytes, sbytes, zbytes;
+            griddep_wait();
+            if (a.x) {
+                // the rows to quantize go first: every CTA reads them, ahead of its weights
+                const uint32_t xbytes = static_cast<uint32_t>(MT * K * 4);
+                mbar_arrive_expect_tx(xbar, xbytes);
+                bulk_load(smem + P.x_off, a.x, xbytes, xbar);
+            }
+            uint32_t i = 0;
+            bool ok = true;
+            for (; i < my_tiles; ++i) {
+                const int s = static_cast<int>(i % ns);
+                const uint32_t k = i / ns;
+                if (k > 0 && !mbar_wait(&empty[s], (k - 1) & 1, ctl)) {
+                    ok = false;
+                    break;
+                }
+                tile_src(i, w, wbytes, ss, sbytes, zs, zbytes);
+                uint8_t* st = smem + P.stage_off + s * P.stage_bytes;
+                mbar_arrive_expect_tx(&full[s], wbytes + sbytes + zbytes);
+                bulk_load(st, w, wbytes, &full[s]);
+                bulk_load(st + P.w_bytes, ss, sbytes, &full[s]);
+                bulk_load(st + P.w_bytes + P.sz_bytes, zs, zbytes, &full[s]);
+            }
+            if (!ok || *abort_flag) {
+                // let the copies already issued land before the CTA exits
+                for (uint32_t q = (i > static_cast<uint32_t>(ns) ? i - ns : 0); q < i; ++q) {
+                    const uint32_t bar = smem_u32(&full[q % ns]), par = (q / ns) & 1;
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait(bar, par) && globaltimer_ns() - t0 < 100000000ull) {
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        griddep_wait();
+        // Stage the activations: token m, block b = 32 c + l -> four 16-byte planes at
+        // m * act_stride + 2048 c + 512 p + 16 l; the block row sums as floats; s_a.
+        float* rsf_sm = reinterpret_cast<float*>(smem + P.rs_off);
+        auto plane_addr = [&](int64_t m, int64_t b, int p) {
+            return smem + m * P.act_stride + (b >> 5) * kChunkAct + p * 512 + (b & 31) * 16;
+        };
+        if (a.x) {
+            // Quantize here, from the rows the producer copied in (nb <= 256).  The units are
+            // 16 codes (a block's plane): lane group 4b .. 4b+3 of a warp holds block b.
+            const bool got = __all_sync(0xffffffffu, mbar_wait(xbar, 0, ctl));
+            const uint32_t xs_base = smem_u32(smem + P.x_off);
+            for (int m = 0; m < MT; ++m) {
+                const uint32_t xr = xs_base + static_cast<uint32_t>(m * K * 4);
+                float amax = 0.0f;
+                for (int64_t f = threadIdx.x; got && f < K / 4; f += kCW * 32) {
+                    const uint4 v = lds128(xr + static_cast<uint32_t>(f * 16));
+                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(__uint_as_float(v.x)), fabsf(__uint_as_float(v.y))),
+                                             fmaxf(fabsf(__uint_as_float(v.z)), fabsf(__uint_as_float(v.w)))));
+                }
+#pragma unroll
+                for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                if (lane == 0) amax_red[m & 1][warp] = amax;
+                named_bar_sync(kBarStage, kCW * 32);
+                amax = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kCW; ++w) amax = fmaxf(amax, amax_red[m & 1][w]);
+                const float s = __fdiv_rn(amax, 127.0f);
+                const float r = __frcp_rn(s);
+                if (threadIdx.x == 0) sa_sm[m] = s;
+                const int units = static_cast<int>(4 * nb);
+                for (int u0 = warp * 32; u0 < units; u0 += kCW * 32) {  // warp-uniform trip count
+                    const int u = u0 + lane, b = u >> 2, p = u & 3;
+                    const bool on = got && u < units;
+                    float4 xs[4], q[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint4 v = on ? lds128(xr + static_cast<uint32_t>((64 * b + 16 * p + 4 * j) * 4))
+                                           : make_uint4(0, 0, 0, 0);
+                        xs[j] = make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                                            __uint_as_float(v.w));
+                    }
+                    if (amax > 0.0f) {
+                        quant_lane<4>(xs, q, s, r);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) q[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                    uint32_t n[4];
+                    float part = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        part += (q[j].x + q[j].y) + (q[j].z + q[j].w);  // exact
+                        n[j] = pack4(__float2int_rn(q[j].x), __float2int_rn(q[j].y), __float2int_rn(q[j].z),
+                                     __float2int_rn(q[j].w));
+                    }
+                    if (on) *reinterpret_cast<uint4*>(plane_addr(m, b, p)) = plane_of(n[0], n[1], n[2], n[3]);
+                    part += __shfl_xor_sync(0xffffffffu, part, 1);
+                    part += __shfl_xor_sync(0xffffffffu, part, 2);
+                    if (on && p == 0) rsf_sm[m * nb + b] = part;
+                }
+            }
+        } else {
+            for (int64_t u = threadIdx.x; u < MT * nb; u += kCW * 32) {
+                const int64_t m = u / nb, b = u - m * nb;
+                const int4* src = reinterpret_cast<const int4*>(a.a_q + m * K + 64 * b);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const int4 v = __ldg(src + p);
+                    *reinterpret_cast<uint4*>(plane_addr(m, b, p)) =
+                        plane_of(static_cast<uint32_t>(v.x), static_cast<uint32_t>(v.y), static_cast<uint32_t>(v.z),
+                                 static_cast<uint32_t>(v.w));
+                }
+                rsf_sm[u] = static_cast<float>(__ldg(a.rs + u));
+            }
+            if (threadIdx.x < MT) sa_sm[threadIdx.x] = __ldg(a.s_a + threadIdx.x);
+        }
+        named_bar_sync(kBarStage, kCW * 32);
+        // the next kernel in the stream may start its prologue as this CTA's SM frees up; it
+        // still waits for this whole grid (and its memory) before it touches data
+        griddep_launch_dependents();
+
+        const int wpr = P.wpr;
+        const int rslot = warp / wpr, sidx = warp - rslot * wpr;
+        const uint32_t act_base = smem_u32(smem), rs_base = smem_u32(rsf_sm);
+        const uint32_t krow = static_cast<uint32_t>(K / 2), nbu = static_cast<uint32_t>(nb);
+        for (uint32_t i = 0; i < my_tiles; ++i) {
+            const int s = static_cast<int>(i % ns);
+            const int64_t n0 = (blockIdx.x + static_cast<int64_t>(i) * gridDim.x) * tr;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (i / ns) & 1, ctl));
+            const uint32_t st = smem_u32(smem + P.stage_off + s * P.stage_bytes);
+            const uint8_t* src;
+            uint32_t bytes, sskew, zskew;
+            half_span(a.s_w, n0 * nb, n0 * nb + 1, src, bytes, sskew);
+            half_span(a.z_w, n0 * nb, n0 * nb + 1, src, bytes, zskew);
+            const uint32_t swb = st + P.w_bytes + sskew, zwb = st + P.w_bytes + P.sz_bytes + zskew;
+            // the rows of this warp in the tile: r_j = warp + 8 j (tr >= 8) or rslot (tr < 8)
+            int rrow[RW];
+            bool rok[RW];
+#pragma unroll
+            for (int j = 0; j < RW; ++j) {
+                rrow[j] = tr >= 8 ? warp + 8 * j : rslot;
+                rok[j] = ok && rrow[j] < tr && n0 + rrow[j] < N;
+            }
+            float sum[RW][MT];
+#pragma unroll
+            for (int j = 0; j < RW; ++j)
+#pragma unroll
+                for (int m = 0; m < MT; ++m) sum[j][m] = 0.0f;
+            if (ok) {
+                for (int c = sidx; c < P.chunks; c += wpr) {
+                    const uint32_t b = static_cast<uint32_t>(c * kChunkBlocks + lane);
+                    const bool live = b < nbu;
+                    uint4 W0[RW], W1[RW];
+                    float sw[RW], nz[RW];
+#pragma unroll
+                    for (int j = 0; j < RW; ++j) {
+                        const bool on = rok[j] && live;
+                        const uint32_t wa = st + rrow[j] * krow + b * 32;
+                        W0[j] = on ? lds128(wa) : make_uint4(0, 0, 0, 0);
+                        W1[j] = on ? lds128(wa + 16) : make_uint4(0, 0, 0, 0);
+                        const uint32_t e = (rrow[j] * nbu + b) * 2;
+                        sw[j] = on ? half_bits_to_float(lds16(swb + e)) : 0.0f;
+                        nz[j] = on ? -half_bits_to_float(lds16(zwb + e)) : 0.0f;
+                    }
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        uint4 Pl[4];
+                        const uint32_t ad = act_base + m * P.act_stride + c * kChunkAct + 16 * lane;
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) Pl[p] = lds128(ad + p * 512);
+                        const float rsf = live ? lds_f32(rs_base + (m * nbu + b) * 4) : 0.0f;
+#pragma unroll
+                        for (int j = 0; j < RW; ++j) {
+                            const int acc = block_dot(W0[j], W1[j], Pl);
+                            sum[j][m] = fmaf(sw[j], fmaf(nz[j], rsf, static_cast<float>(acc)), sum[j][m]);
+                        }
+                    }
+                }
+            }
+            // the stage has been read
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            // the warp sums (a full butterfly: every lane ends with the total; lane m stores token m)
+#pragma unroll
+            for (int j = 0; j < RW; ++j)
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    float v = sum[j][m];
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    sum[j][m] = v;
+                }
+            if (wpr == 1) {
+#pragma unroll
+                for (int j = 0; j < RW; ++j) {
+                    const int64_t n = n0 + rrow[j];
+                    float v = sum[j][0];
+#pragma unroll
+                    for (int m = 1; m < MT; ++m)
+                        if (lane == m) v = sum[j][m];
+                    if (rok[j] && lane < MT)
+                        a.y[static_cast<int64_t>(lane) * N + n] = fmaf(sa_sm[lane], v, a.bias ? a.bias[n] : 0.0f);
+                }
+            } else {
+                // the row's warps meet (every warp meets once per tile, whatever its waits gave)
+                if (lane == 0)
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) red[i & 1][warp][m] = sum[0][m];
+                named_bar_sync(1 + rslot, wpr * 32);
+                const int64_t n = n0 + rslot;
+                if (sidx == 0 && rok[0] && lane < MT) {
+                    float v = 0.0f;
+                    for (int q = 0; q < wpr; ++q) v += red[i & 1][rslot * wpr + q][lane];
+                    a.y[static_cast<int64_t>(lane) * N + n] = fmaf(sa_sm[lane], v, a.bias ? a.bias[n] : 0.0f);
+                }
+            }
+        }
+    }
+    __syncthreads();
+}
+
+template <int MT, int RW>
+cudaError_t launch_one(const GemvArgs& a, const GemvPlan& P, uint32_t* status, cudaStream_t s) {
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_done[dev]) {
+        cudaError_t e =
+            cudaFuncSetAttribute(gemv_kernel<MT, RW>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(P.grid));
+    cfg.blockDim = dim3(kGThreads);
+    cfg.dynamicSmemBytes = P.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, RW>, a, P, status, uint64_t(1000000000ull));
+}
+
+template <int MT>
+cudaError_t launch_mt(const GemvArgs& a, const GemvPlan& P, uint32_t* status, cudaStream_t s) {
+    if constexpr (MT <= 2) {
+        if (P.tr == 32) return launch_one<MT, 4>(a, P, status, s);
+        if (P.tr == 16) return launch_one<MT, 2>(a, P, status, s);
+    }
+    return launch_one<MT, 1>(a, P, status, s);
+}
+
+}  // namespace
+
+bool gemv_supported(int64_t M, int64_t K) {
+    GemvPlan P;
+    return M >= 1 && M <= kGemvMaxM && K >= kBlock && make_plan(M, 1, K, false, 1, &P);
+}
+
+bool gemv_quantizes(int64_t M, int64_t K) {
+    GemvPlan P;
+    return M * K <= kGemvFuseElems && gemv_supported(M, K) && make_plan(M, 1, K, true, 1, &P);
+}
+
+cudaError_t launch_gemv(const GemvArgs& a, int num_sms, uint32_t* status, cudaStream_t s) {
+    GemvPlan P;
+    if (a.M < 1 || a.M > kGemvMaxM || a.N < 1 || (a.x && !gemv_quantizes(a.M, a.K)) ||
+        !make_plan(a.M, a.N, a.K, a.x != nullptr, num_sms, &P))
+        return cudaErrorInvalidValue;
+    switch (a.M) {
+        case 1: return launch_mt<1>(a, P, status, s);
+        case 2: return launch_mt<2>(a, P, status, s);
+        case 3: return launch_mt<3>(a, P, status, s);
+        case 4: return launch_mt<4>(a, P, status, s);
+        case 5: return launch_mt<5>(a, P, status, s);
+        case 6: return launch_mt<6>(a, P, status, s);
+        case 7: return launch_mt<7>(a, P, status, s);
+        default: return launch_mt<8>(a, P, status, s);
+    }
+}
+
+}  // namespace w4a8

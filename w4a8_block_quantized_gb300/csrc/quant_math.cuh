@@ -1,0 +1,66 @@
+// quant_math.cuh -- the activation quantizer shared by the pre-pass (prep.cu) and the
+// few-token kernel (gemv.cu), so that both produce the same codes bit for bit.
+//
+// "MNN LLM inference on the SpacemiT K3", section 4 step 1 (dynamic per-row INT8):
+// s = absmax / 127 (fp32 IEEE division), code = clamp(round_half_away(x / s), -127, 127).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace w4a8 {
+
+// INT8 code of one activation: clamp(round_half_away(x / s), -127, 127), fp32 IEEE division.
+__device__ __forceinline__ int quant1(float x, float s) {
+    float r = roundf(__fdiv_rn(x, s));
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return static_cast<int>(r);
+}
+
+// The same code, as a float, without a division in the common case.  With r = RN(1/s),
+// t = RN(x * r) lies within |x/s| * (2^-23 + 2^-48) of x/s, and the IEEE quotient
+// RN(x/s) within |x/s| * 2^-24; for |x/s| <= 127.5 the two differ by less than 2^-15.  So
+// unless t is within 2^-15 of a half-integer, round_half_away(t) equals round_half_away of
+// the IEEE quotient.  near_tie() flags the rest, which are recomputed with the division.
+__device__ __forceinline__ bool near_tie(float t) {
+    const float a = fabsf(t);
+    return fabsf((a - truncf(a)) - 0.5f) <= 0x1p-15f;
+}
+
+// t rounded to the nearest integer (ties to even), and whether t lies within 2^-15 of a
+// half-integer.  |t - rint(t)| is exact (the two are within a factor two of each other, or
+// the integer is 0) and equals the distance of frac(|t|) from the nearer integer, so the
+// flag is the near_tie() test.  Away from the flagged values round-to-even and
+// round-half-away agree; the flagged ones are recomputed by the caller.
+__device__ __forceinline__ float rint_flag(float t, bool& tie) {
+    const float q = rintf(t);
+    tie |= fabsf(t - q) >= 0.5f - 0x1p-15f;
+    return q;
+}
+
+// Quantize one lane's V float4 of a row to float codes.  No clamp is applied: for finite
+// inputs |x| <= absmax and s = RN(absmax/127), so |x/s| <= 127 (1 + 2^-24) and no code can
+// exceed 127 in magnitude, exactly as the clamped definition gives.  The rare near-tie
+// elements of the warp are recomputed with the IEEE division (warp-uniform branch).
+template <int V>
+__device__ __forceinline__ void quant_lane(const float4 (&x)[V], float4 (&q)[V], float s, float r) {
+    bool tie = false;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+        q[i].x = rint_flag(x[i].x * r, tie);
+        q[i].y = rint_flag(x[i].y * r, tie);
+        q[i].z = rint_flag(x[i].z * r, tie);
+        q[i].w = rint_flag(x[i].w * r, tie);
+    }
+    if (__any_sync(0xffffffffu, tie)) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            if (near_tie(x[i].x * r)) q[i].x = roundf(__fdiv_rn(x[i].x, s));
+            if (near_tie(x[i].y * r)) q[i].y = roundf(__fdiv_rn(x[i].y, s));
+            if (near_tie(x[i].z * r)) q[i].z = roundf(__fdiv_rn(x[i].z, s));
+            if (near_tie(x[i].w * r)) q[i].w = roundf(__fdiv_rn(x[i].w, s));
+        }
+    }
+}
+
+}  // namespace w4a8

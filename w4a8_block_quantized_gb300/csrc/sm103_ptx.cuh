@@ -97,6 +97,10 @@ __device__ __forceinline__ void regs_inc() {
 // Blocks until the grids this one depends on have completed and their memory is visible
 // (returns at once for a grid launched without a programmatic dependency).
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allows the next programmatic-dependent grid to be scheduled before this one completes.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- proxy fences
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy

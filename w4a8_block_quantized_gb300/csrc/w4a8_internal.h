@@ -133,6 +133,47 @@ struct GemmArgs {
 
 // Persistent launch over ceil(M/tw) x ceil(N/128) output tiles on at most `num_sms` CTAs.
 cudaError_t launch_gemm(const GemmArgs& a, bool debug, int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------- few-token (decode) form
+// Up to kGemvMaxM tokens (and a K whose staged activations fit on chip): the packed weights
+// streamed once, integer dot products on the CUDA cores (gemv.cu), activations in the API
+// layout (a_q [M][K], s_a [M], rs [M][K/64]).
+constexpr int64_t kGemvMaxM = 8;
+
+struct GemvArgs {
+    const float* x = nullptr;           // fp32 [M][K]: quantize in the kernel (gemv_quantizes), or
+    const int8_t* a_q = nullptr;        // the pre-pass outputs a_q / s_a / rs
+    const float* s_a = nullptr;
+    const int32_t* rs = nullptr;
+    const uint8_t* wq = nullptr;        // [N][K/2]
+    const uint16_t* s_w = nullptr;      // fp16 bits [N][K/64]
+    const uint16_t* z_w = nullptr;
+    const float* bias = nullptr;
+    float* y = nullptr;                 // [M][N]
+    int64_t M = 0, N = 0, K = 0;
+};
+
+// Scratch of the fused few-token call: the pre-pass outputs in the API layout.
+struct DecodeLayout {
+    size_t a_q = 0, s_a = 0, rs = 0, total = 0;
+};
+
+inline DecodeLayout decode_layout(int64_t M, int64_t K) {
+    DecodeLayout L;
+    L.s_a = align_ws(static_cast<size_t>(M) * static_cast<size_t>(K));
+    L.rs = align_ws(L.s_a + static_cast<size_t>(M) * 4);
+    L.total = align_ws(L.rs + static_cast<size_t>(M) * static_cast<size_t>(K / kBlock) * 4);
+    return L;
+}
+
+// Whether M tokens of depth K fit the weight-streaming kernel (its staged activations and
+// at least two weight stages must fit in one CTA's shared memory), and whether it can also
+// quantize them itself (every CTA re-reads x from L2, so only for small M * K).
+constexpr int64_t kGemvFuseElems = 16384;
+bool gemv_supported(int64_t M, int64_t K);
+bool gemv_quantizes(int64_t M, int64_t K);
+
+cudaError_t launch_gemv(const GemvArgs& a, int num_sms, uint32_t* status, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace w4a8

@@ -68,7 +68,28 @@ WORKLOADS: dict[str, tuple[str, tuple[LinearSpec, ...]]] = {
     "c4": _cfg("7B-class prefill M8192: K4096->N14336 then K14336->N4096", [
         ("up", 8192, 4096, 14336, False, 20.0, 0, 0),
         ("down", 8192, 14336, 4096, False, 20.0, 0, 1)]),
+    # One-token decode steps through the same projections (the few-token form).
+    "d1": _cfg("decode 1 token, M1 K1024 N3072 +bias (0.6B-class MLP up-projection)", [
+        ("up", 1, 1024, 3072, True, 20.0, 0, 0)]),
+    "d3": _cfg("decode 1 token through the decoder-layer linear set, hidden 2048 (q,k,v,o,gate,up,down)", [
+        ("q", 1, 2048, 2048, False, 20.0, 1000, 0),
+        ("k", 1, 2048, 1024, False, 20.0, 1001, 0),
+        ("v", 1, 2048, 1024, False, 20.0, 1002, 0),
+        ("o", 1, 2048, 2048, False, 20.0, 1003, 0),
+        ("gate", 1, 2048, 6144, False, 20.0, 1004, 0),
+        ("up", 1, 2048, 6144, False, 20.0, 1005, 0),
+        ("down", 1, 6144, 2048, False, 20.0, 1006, 0)]),
+    "d4": _cfg("decode 1 token, 7B-class: K4096->N14336 then K14336->N4096", [
+        ("up", 1, 4096, 14336, False, 20.0, 0, 0),
+        ("down", 1, 14336, 4096, False, 20.0, 0, 1)]),
 }
+
+DECODE_MAX_M = 8  # token counts the library runs in its weight-streaming (decode) form
+
+
+def weight_bytes(spec: LinearSpec) -> int:
+    """Bytes of one linear's weights as streamed: packed u4 codes + fp16 s_w and z_w."""
+    return spec.N * spec.K // 2 + 2 * 2 * spec.N * (spec.K // BLOCK)
 
 
 def workload(key: str) -> tuple[str, tuple[LinearSpec, ...]]:
