@@ -122,6 +122,30 @@ int w4a8_linear_prepared(const void *act, const void *pw, const float *bias, flo
 size_t w4a8_prepared_activations_bytes(int64_t M, int64_t K);
 size_t w4a8_prepared_weights_bytes(int64_t N, int64_t K);
 
+/* Epilogue variants ("MNN LLM inference on the SpacemiT K3", section 4 step 3: the direct
+ * epilogue adds the bias and may clamp).  The *_ex calls equal their plain counterparts
+ * except for the store of y:
+ *   y[m,n] = clamp(s_a[m] * sum_b (...) + bias[n], clamp_lo, clamp_hi)
+ * stored as fp32 (out_dtype W4A8_OUT_F32) or as bf16, round to nearest even
+ * (W4A8_OUT_BF16; y then holds M*N 16-bit values, still 16-byte aligned).  clamp_lo =
+ * -INFINITY and clamp_hi = +INFINITY store the value unchanged, so the plain calls are the
+ * *_ex calls with W4A8_OUT_F32 and those bounds, bit for bit.  An unknown out_dtype or
+ * clamp_lo > clamp_hi (or either NaN) returns W4A8_ERR_ARG and launches nothing. */
+#define W4A8_OUT_F32 0
+#define W4A8_OUT_BF16 1
+int w4a8_prefill_linear_ex(const float *x, const uint8_t *wq, const uint16_t *w_scale,
+                           const uint16_t *w_zero, const float *bias, void *y, int out_dtype,
+                           float clamp_lo, float clamp_hi, int64_t M, int64_t N, int64_t K,
+                           void *workspace, size_t workspace_bytes, void *stream);
+int w4a8_linear_ex(const int8_t *a_q, const float *a_scale, const int32_t *rowsum,
+                   const uint8_t *wq, const uint16_t *w_scale, const uint16_t *w_zero,
+                   const float *bias, void *y, int out_dtype, float clamp_lo, float clamp_hi,
+                   int64_t M, int64_t N, int64_t K, void *workspace, size_t workspace_bytes,
+                   void *stream);
+int w4a8_linear_prepared_ex(const void *act, const void *pw, const float *bias, void *y,
+                            int out_dtype, float clamp_lo, float clamp_hi, int64_t M, int64_t N,
+                            int64_t K, void *stream);
+
 /* w4a8_prefill_linear for callers that cannot allocate device memory (no counterpart in
  * the paper; it exists for integration only).  Some callers have no way to hand the
  * library a workspace: code that runs where cudaMalloc is not allowed or not wanted (an

@@ -170,3 +170,27 @@ def prefill_linear(x, wq, s_w, z_w, bias=None, rows=None, tag: str = "oracle"):
 
 def num_threads(tag: str = "oracle") -> int:
     return int(lib(tag).oracle_num_threads())
+
+
+def bf16_round(v) -> np.ndarray:
+    """Nearest value with an 8-bit significand (bfloat16: 1 implicit + 7 stored bits, the
+    fp32 exponent range), ties to the even significand; returned as float64.  Written from
+    the definition: v = f * 2^e with 1/2 <= |f| < 1, f * 2^8 rounded half-to-even, scaled
+    back.  Below the normal range (|v| < 2^-126) the step is fixed at 2^-133."""
+    v = np.asarray(v, dtype=np.float64)
+    f, e = np.frexp(v)
+    e = np.maximum(e, -125)                 # 2^-126 = 0.5 * 2^-125: subnormal step 2^-133
+    out = np.rint(np.ldexp(v, 8 - e))       # np.rint rounds half to even
+    return np.ldexp(out, e - 8)
+
+
+def epilogue(y, clamp_lo=-np.inf, clamp_hi=np.inf, out_dtype: str = "f32") -> np.ndarray:
+    """Section 4 step 3's store of the output: clamp to [clamp_lo, clamp_hi], then the
+    value the output type holds (fp32: IEEE round to nearest even; bf16: bf16_round).
+    y is the exact (fp64) result; returns float64."""
+    v = np.clip(np.asarray(y, dtype=np.float64), clamp_lo, clamp_hi)
+    if out_dtype == "f32":
+        return v.astype(np.float32).astype(np.float64)
+    if out_dtype == "bf16":
+        return bf16_round(v)
+    raise ValueError(out_dtype)

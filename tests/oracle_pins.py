@@ -198,6 +198,42 @@ def pin_special_cases(tag):
     assert np.allclose(y3[0], exp, rtol=1e-13, atol=0.0)
 
 
+def pin_epilogue_store(tag):
+    """The epilogue's store (section 4 step 3: clamp, then the output type).  bf16 rounding
+    against hand-worked values (ties to the even significand) and, on random values, against
+    the nearer of the two bf16 neighbours built from their bit patterns (numpy's float32 view
+    of a 16-bit pattern shifted left by 16); the clamp against its closed form; fp32 against
+    numpy's own float32 cast."""
+    r = oracle.bf16_round
+    assert r(1.0) == 1.0 and r(-3.0) == -3.0 and r(0.0) == 0.0
+    assert r(1.0 + 2.0 ** -8) == 1.0                        # tie, even neighbour below
+    assert r(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6        # tie, even neighbour above
+    assert r(1.0 + 2.0 ** -8 + 2.0 ** -20) == 1.0 + 2.0 ** -7
+    assert r(-(1.0 + 2.0 ** -8 + 2.0 ** -20)) == -(1.0 + 2.0 ** -7)
+    assert r(1.0 / 3.0) == 0.333984375                      # 0x3EAB
+    assert r(255.5) == 256.0 and r(254.5) == 254.0          # step 2 in [128, 256): 255.5 -> 256
+    rng = np.random.default_rng(17)
+    v = rng.standard_normal(4000) * np.exp2(rng.integers(-30, 30, 4000))
+    got = r(v)
+    # neighbours from bit patterns: truncate the float32 of v toward zero to a bf16 pattern
+    f32 = v.astype(np.float32)
+    hi16 = (f32.view(np.uint32) >> 16).astype(np.uint32)
+    lo = (hi16 << 16).view(np.float32).astype(np.float64)
+    nxt = ((hi16 + 1) << 16).view(np.float32).astype(np.float64)
+    for val, a, b, g in zip(v, lo, nxt, got):
+        lo_, hi_ = min(a, b), max(a, b)
+        if not (lo_ <= val <= hi_):                         # the float32 cast crossed a neighbour
+            continue
+        da, db = abs(val - lo_), abs(hi_ - val)
+        assert g in (lo_, hi_)
+        if da != db:
+            assert g == (lo_ if da < db else hi_)
+    y = np.array([-2.0, -0.5, 0.1, 0.75, 3.0])
+    assert np.array_equal(oracle.epilogue(y, -0.5, 0.75, "f32"), [-0.5, -0.5, np.float64(np.float32(0.1)), 0.75, 0.75])
+    assert np.array_equal(oracle.epilogue(y, out_dtype="f32"), y.astype(np.float32).astype(np.float64))
+    assert np.array_equal(oracle.epilogue(y, -1.0, 1.0, "bf16"), r(np.clip(y, -1.0, 1.0)))
+
+
 ALL_PINS = [
     pin_half_decode,
     pin_quant_golden,
@@ -209,4 +245,5 @@ ALL_PINS = [
     pin_bruteforce_fp64,
     pin_linear_golden,
     pin_special_cases,
+    pin_epilogue_store,
 ]

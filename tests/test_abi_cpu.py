@@ -44,7 +44,7 @@ def test_status_strings(lib):
         s = b.status_string(code)
         assert s and s != "unknown status"
     assert b.status_string(12345) == "unknown status"
-    assert lib.w4a8_abi_version() == 201
+    assert lib.w4a8_abi_version() == 202
 
 
 def test_shape_checks_need_no_gpu(lib):
@@ -104,3 +104,15 @@ def test_few_token_workspace_sizes(lib):
                 assert M * K + 4 * M + 4 * M * nb <= pre <= M * K + 4 * M + 4 * M * nb + 3 * 256
     assert lib.w4a8_linear_workspace_bytes(9, N, 1024) >= N * 1024
     assert lib.w4a8_prefill_workspace_bytes(9, N, 1024) >= N * 1024
+
+
+def test_epilogue_arguments_rejected_before_launch(lib):
+    """The *_ex calls reject an unknown output type and clamp bounds with lo > hi or a NaN
+    before touching the device."""
+    import math
+    from w4a8_block_quantized_gb300 import binding as b
+    d = ctypes.c_void_p(1 << 20)
+    for dt, lo, hi in ((2, -1.0, 1.0), (-1, -1.0, 1.0), (0, 1.0, -1.0), (1, math.nan, 1.0), (0, -1.0, math.nan)):
+        assert lib.w4a8_prefill_linear_ex(d, d, d, d, None, d, dt, lo, hi, 4, 8, 64, None, 0, None) == b.W4A8_ERR_ARG
+        assert lib.w4a8_linear_ex(d, d, d, d, d, d, None, d, dt, lo, hi, 4, 8, 64, None, 0, None) == b.W4A8_ERR_ARG
+        assert lib.w4a8_linear_prepared_ex(d, d, None, d, dt, lo, hi, 4, 8, 64, None) == b.W4A8_ERR_ARG

@@ -387,3 +387,58 @@ def test_decode_boundary_tokens():
     y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
     check_y(y9, y_ref, bound, "9 tokens")
     check_y(y8, y_ref[:8], bound[:8], "8 tokens")
+
+
+# ------------------------------------------------------------------ epilogue variants
+@pytest.mark.parametrize("M,K,N", [(300, 1024, 700), (4100, 512, 300), (1, 2048, 1000), (5, 4096, 777),
+                                   (2, 1024, 129)])
+def test_epilogue_clamp_and_bf16(M, K, N):
+    """The *_ex calls: fp32 with the default bounds equals the plain call bit for bit; the
+    clamp against the clamped oracle output; bf16 within the fp32 tolerance plus half a bf16
+    step; the split and prepared forms give the fused form's bits.  Covers the 128- and
+    256-token contractions and both few-token paths (in-kernel and separate pre-pass)."""
+    from gpu_util import ABS_TOL, REL_TOL
+    b = B()
+    d = synth.random_small(M, K, N, seed=3 * M + K + 7 * N, bias=True)
+    g = inputs_to_dev(d)
+    y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
+    lo, hi = (float(v) for v in np.quantile(y_ref, [0.2, 0.85]))
+    y_plain = b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"])
+    assert torch.equal(b.prefill_linear_ex(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"]), y_plain)
+    clipped = np.clip(y_ref, lo, hi)
+    yc = b.prefill_linear_ex(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"], clamp=(lo, hi))
+    check_y(yc, clipped, bound, f"clamp {M}x{K}->{N}")
+    assert float(yc.min()) >= np.float32(lo) and float(yc.max()) <= np.float32(hi)
+    yb = b.prefill_linear_ex(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"], out_dtype=torch.bfloat16,
+                             clamp=(lo, hi))
+    assert yb.dtype == torch.bfloat16
+    got = yb.float().cpu().numpy().astype(np.float64)
+    allowed = REL_TOL * bound + ABS_TOL
+    allowed = allowed + 2.0 ** -8 * (np.abs(clipped) + allowed)
+    err = np.abs(got - clipped)
+    assert np.all(err <= allowed), f"bf16: {int((err > allowed).sum())} outputs outside tolerance"
+    e_ref = oracle.epilogue(y_ref, lo, hi, "bf16")
+    assert np.mean(got == e_ref) > 0.95  # the same bf16 value except next to rounding boundaries
+    a_q, s_a, rs = b.quant_pack(g["x"])
+    ys = b.linear_ex(a_q, s_a, rs, g["wq"], g["s_w"], g["z_w"], g["bias"], out_dtype=torch.bfloat16, clamp=(lo, hi))
+    assert torch.equal(ys, yb), "split form differs"
+    if M > 8:
+        act = b.prepare_activations(g["x"])
+        pw = b.prepare_weights(g["wq"], g["s_w"], g["z_w"])
+        yp = b.linear_prepared_ex(act, pw, M, N, K, bias=g["bias"], out_dtype=torch.bfloat16, clamp=(lo, hi))
+        assert torch.equal(yp, yb), "prepared form differs"
+    assert b.sync_status() == 0
+
+
+def test_epilogue_argument_checks():
+    b = B()
+    d = synth.random_small(4, 64, 8, seed=1, bias=False)
+    g = inputs_to_dev(d)
+    y = torch.empty((4, 8), device=dev())
+    lib = b.load()
+    args = (b._ptr(g["x"]), b._ptr(g["wq"]), b._ptr(g["s_w"]), b._ptr(g["z_w"]), None, b._ptr(y))
+    assert lib.w4a8_prefill_linear_ex(*args, 7, -1.0, 1.0, 4, 8, 64, None, 0, b._stream(None)) == b.W4A8_ERR_ARG
+    assert lib.w4a8_prefill_linear_ex(*args, 0, 1.0, -1.0, 4, 8, 64, None, 0, b._stream(None)) == b.W4A8_ERR_ARG
+    assert lib.w4a8_prefill_linear_ex(*args, 0, float("nan"), 1.0, 4, 8, 64, None, 0, b._stream(None)) == \
+        b.W4A8_ERR_ARG
+    assert b.sync_status() == 0

@@ -7,6 +7,7 @@ fallback: if the library is missing or the GPU is not an sm_103 part, calls rais
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 
 import torch
@@ -24,6 +25,9 @@ W4A8_ERR_WORKSPACE = -6
 W4A8_ERR_DEVICE = -7
 W4A8_ERR_SCRATCH_LIMIT = -8
 NOALLOC_SCRATCH_BYTES = 16 << 20
+OUT_F32 = 0
+OUT_BF16 = 1
+_OUT_DTYPES = {torch.float32: OUT_F32, torch.bfloat16: OUT_BF16}
 
 # name -> (restype, argtypes); every symbol include/w4a8.h declares
 _P = ctypes.c_void_p
@@ -37,6 +41,12 @@ SIGNATURES = {
     "w4a8_prepare_activations": (ctypes.c_int, [_P, _I64, _I64, _P, _SZ, _P]),
     "w4a8_prepare_weights": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _SZ, _P]),
     "w4a8_linear_prepared": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "w4a8_prefill_linear_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                              _I64, _I64, _I64, _P, _SZ, _P]),
+    "w4a8_linear_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                      _I64, _I64, _I64, _P, _SZ, _P]),
+    "w4a8_linear_prepared_ex": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                               _I64, _I64, _I64, _P]),
     "w4a8_prepared_activations_bytes": (_SZ, [_I64, _I64]),
     "w4a8_prepared_weights_bytes": (_SZ, [_I64, _I64]),
     "w4a8_linear_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
@@ -208,6 +218,60 @@ def prepare_weights(wq, w_scale, w_zero, pw=None, stream=None):
                                      _stream(stream))
     _check(rc, "w4a8_prepare_weights")
     return pw
+
+
+def _out(y, shape, device, out_dtype):
+    dt = torch.float32 if out_dtype is None else out_dtype
+    if dt not in _OUT_DTYPES:
+        raise TypeError(f"y: unsupported output dtype {dt}")
+    y = torch.empty(shape, dtype=dt, device=device) if y is None else y
+    if y.dtype != dt or not y.is_contiguous() or tuple(y.shape) != tuple(shape):
+        raise ValueError(f"y: want a contiguous {dt} tensor of shape {tuple(shape)}")
+    return y, _OUT_DTYPES[dt]
+
+
+def prefill_linear_ex(x, wq, w_scale, w_zero, bias=None, y=None, out_dtype=None, clamp=(-math.inf, math.inf),
+                      ws=None, stream=None):
+    """w4a8_prefill_linear_ex: the fused call with the epilogue clamp and an fp32 or bf16 y."""
+    _want(x, torch.float32, "x")
+    _want(wq, torch.uint8, "wq")
+    M, K = x.shape
+    N = wq.shape[0]
+    y, code = _out(y, (M, N), x.device, out_dtype if y is None else y.dtype)
+    if ws is None:
+        ws = workspace(prefill_workspace_bytes(M, N, K), x.device)
+    rc = load().w4a8_prefill_linear_ex(_ptr(x), _ptr(wq), _ptr(w_scale), _ptr(w_zero), _ptr(bias), _ptr(y), code,
+                                       float(clamp[0]), float(clamp[1]), M, N, K, _ptr(ws), ws.numel(),
+                                       _stream(stream))
+    _check(rc, "w4a8_prefill_linear_ex")
+    return y
+
+
+def linear_ex(a_q, a_scale, rowsum, wq, w_scale, w_zero, bias=None, y=None, out_dtype=None,
+              clamp=(-math.inf, math.inf), ws=None, stream=None):
+    """w4a8_linear_ex: pre-quantized activations, epilogue clamp, fp32 or bf16 y."""
+    _want(a_q, torch.int8, "a_q")
+    _want(wq, torch.uint8, "wq")
+    M, K = a_q.shape
+    N = wq.shape[0]
+    y, code = _out(y, (M, N), a_q.device, out_dtype if y is None else y.dtype)
+    if ws is None:
+        ws = workspace(linear_workspace_bytes(M, N, K), a_q.device)
+    rc = load().w4a8_linear_ex(_ptr(a_q), _ptr(a_scale), _ptr(rowsum), _ptr(wq), _ptr(w_scale), _ptr(w_zero),
+                               _ptr(bias), _ptr(y), code, float(clamp[0]), float(clamp[1]), M, N, K, _ptr(ws),
+                               ws.numel(), _stream(stream))
+    _check(rc, "w4a8_linear_ex")
+    return y
+
+
+def linear_prepared_ex(act, pw, M: int, N: int, K: int, bias=None, y=None, out_dtype=None,
+                       clamp=(-math.inf, math.inf), stream=None):
+    """w4a8_linear_prepared_ex: prepared operands, epilogue clamp, fp32 or bf16 y."""
+    y, code = _out(y, (M, N), act.device, out_dtype if y is None else y.dtype)
+    rc = load().w4a8_linear_prepared_ex(_ptr(act), _ptr(pw), _ptr(bias), _ptr(y), code, float(clamp[0]),
+                                        float(clamp[1]), M, N, K, _stream(stream))
+    _check(rc, "w4a8_linear_prepared_ex")
+    return y
 
 
 def linear_prepared(act, pw, M: int, N: int, K: int, bias=None, y=None, stream=None):

@@ -82,8 +82,8 @@ CallLayout call_layout(int64_t M, int64_t N, int64_t K, bool with_sa) {
 }
 
 // GEMM + epilogue from prepared activations (token records) and prepared weights.
-int run_linear(const uint8_t* trec, const float* s_a, const uint8_t* pw, const float* bias, float* y, int64_t M,
-               int64_t N, int64_t K, const DeviceInfo& d, cudaStream_t st) {
+int run_linear(const uint8_t* trec, const float* s_a, const uint8_t* pw, const float* bias, const OutSpec& out,
+               int64_t M, int64_t N, int64_t K, const DeviceInfo& d, cudaStream_t st) {
     const WLayout W = w_layout(N, K);
     GemmArgs g;
     g.M = M;
@@ -95,7 +95,7 @@ int run_linear(const uint8_t* trec, const float* s_a, const uint8_t* pw, const f
     g.sc = reinterpret_cast<const float*>(pw + W.sc);
     g.s_a = s_a;
     g.bias = bias;
-    g.y = y;
+    g.out = out;
     g.status = d.status;
     return launch_gemm(g, false, d.num_sms, st) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
 }
@@ -128,8 +128,8 @@ size_t prefill_ws(int64_t M, int64_t N, int64_t K) {
 
 // The few-token kernel from x (it quantizes) or from the pre-pass outputs.
 int run_gemv(const float* x, const int8_t* a_q, const float* s_a, const int32_t* rs, const uint8_t* wq,
-             const uint16_t* w_scale, const uint16_t* w_zero, const float* bias, float* y, int64_t M, int64_t N,
-             int64_t K, const DeviceInfo& d, cudaStream_t st) {
+             const uint16_t* w_scale, const uint16_t* w_zero, const float* bias, const OutSpec& out, int64_t M,
+             int64_t N, int64_t K, const DeviceInfo& d, cudaStream_t st) {
     GemvArgs g;
     g.x = x;
     g.a_q = a_q;
@@ -139,12 +139,38 @@ int run_gemv(const float* x, const int8_t* a_q, const float* s_a, const int32_t*
     g.s_w = w_scale;
     g.z_w = w_zero;
     g.bias = bias;
-    g.y = y;
+    g.out = out;
     g.M = M;
     g.N = N;
     g.K = K;
     return launch_gemv(g, d.num_sms, d.status, st) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
 }
+
+OutSpec f32_out(float* y) {
+    OutSpec o;
+    o.y = y;
+    return o;
+}
+
+// The output spec of the *_ex entry points: a known dtype and lo <= hi (no NaN).
+int make_out(void* y, int out_dtype, float lo, float hi, OutSpec* o) {
+    if (out_dtype != W4A8_OUT_F32 && out_dtype != W4A8_OUT_BF16) return W4A8_ERR_ARG;
+    if (!(lo <= hi)) return W4A8_ERR_ARG;
+    o->y = y;
+    o->bf16 = out_dtype == W4A8_OUT_BF16;
+    o->lo = lo;
+    o->hi = hi;
+    return W4A8_OK;
+}
+
+int linear_impl(const int8_t* a_q, const float* a_scale, const int32_t* rowsum, const uint8_t* wq,
+                const uint16_t* w_scale, const uint16_t* w_zero, const float* bias, const OutSpec& out, int64_t M,
+                int64_t N, int64_t K, void* workspace, size_t workspace_bytes, void* stream);
+int prefill_impl(const float* x, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero,
+                 const float* bias, const OutSpec& out, int64_t M, int64_t N, int64_t K, void* workspace,
+                 size_t workspace_bytes, void* stream);
+int linear_prepared_impl(const void* act, const void* pw, const float* bias, const OutSpec& out, int64_t M,
+                         int64_t N, int64_t K, void* stream);
 
 }  // namespace
 }  // namespace w4a8
@@ -153,7 +179,7 @@ using namespace w4a8;
 
 extern "C" {
 
-int w4a8_abi_version(void) { return 201; }
+int w4a8_abi_version(void) { return 202; }
 
 const char* w4a8_status_string(int status) {
     switch (status) {
@@ -221,11 +247,34 @@ int w4a8_quant_pack(const float* x, int64_t M, int64_t K, int8_t* a_q, float* a_
 int w4a8_linear(const int8_t* a_q, const float* a_scale, const int32_t* rowsum, const uint8_t* wq,
                 const uint16_t* w_scale, const uint16_t* w_zero, const float* bias, float* y, int64_t M, int64_t N,
                 int64_t K, void* workspace, size_t workspace_bytes, void* stream) {
+    return linear_impl(a_q, a_scale, rowsum, wq, w_scale, w_zero, bias, f32_out(y), M, N, K, workspace,
+                       workspace_bytes, stream);
+}
+
+int w4a8_linear_ex(const int8_t* a_q, const float* a_scale, const int32_t* rowsum, const uint8_t* wq,
+                   const uint16_t* w_scale, const uint16_t* w_zero, const float* bias, void* y, int out_dtype,
+                   float clamp_lo, float clamp_hi, int64_t M, int64_t N, int64_t K, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+    OutSpec o;
+    const int rc = make_out(y, out_dtype, clamp_lo, clamp_hi, &o);
+    if (rc != W4A8_OK) return rc;
+    return linear_impl(a_q, a_scale, rowsum, wq, w_scale, w_zero, bias, o, M, N, K, workspace, workspace_bytes,
+                       stream);
+}
+
+}  // extern "C"
+
+namespace w4a8 {
+namespace {
+
+int linear_impl(const int8_t* a_q, const float* a_scale, const int32_t* rowsum, const uint8_t* wq,
+                const uint16_t* w_scale, const uint16_t* w_zero, const float* bias, const OutSpec& out, int64_t M,
+                int64_t N, int64_t K, void* workspace, size_t workspace_bytes, void* stream) {
     int rc = check_shape(M, N, K);
     if (rc != W4A8_OK) return rc;
     if (M == 0 || N == 0) return W4A8_OK;
-    if (!a_q || !a_scale || !rowsum || !wq || !w_scale || !w_zero || !y) return W4A8_ERR_ARG;
-    if (!aligned(a_q, 16) || !aligned(wq, 16) || !aligned(y, 16) || !aligned(a_scale, 4) || !aligned(rowsum, 4) ||
+    if (!a_q || !a_scale || !rowsum || !wq || !w_scale || !w_zero || !out.y) return W4A8_ERR_ARG;
+    if (!aligned(a_q, 16) || !aligned(wq, 16) || !aligned(out.y, 16) || !aligned(a_scale, 4) || !aligned(rowsum, 4) ||
         !aligned(w_scale, 2) || !aligned(w_zero, 2) || (bias && !aligned(bias, 4)))
         return W4A8_ERR_ALIGN;
     DeviceInfo* d = nullptr;
@@ -233,7 +282,7 @@ int w4a8_linear(const int8_t* a_q, const float* a_scale, const int32_t* rowsum, 
     if (few_tokens(M, K)) {
         // few-token form: no scratch, the workspace is not touched
         if ((rc = current_device(&d)) != W4A8_OK) return rc;
-        return run_gemv(nullptr, a_q, a_scale, rowsum, wq, w_scale, w_zero, bias, y, M, N, K, *d, st);
+        return run_gemv(nullptr, a_q, a_scale, rowsum, wq, w_scale, w_zero, bias, out, M, N, K, *d, st);
     }
     const CallLayout L = call_layout(M, N, K, false);
     if (!workspace || workspace_bytes < L.total) return W4A8_ERR_WORKSPACE;
@@ -248,17 +297,17 @@ int w4a8_linear(const int8_t* a_q, const float* a_scale, const int32_t* rowsum, 
     p.tw = L.act.tw;
     set_weight_job(&p, wq, w_scale, w_zero, N, K, ws + L.w_off);
     if (launch_pack(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
-    return run_linear(ws + L.act.rec, a_scale, ws + L.w_off, bias, y, M, N, K, *d, st);
+    return run_linear(ws + L.act.rec, a_scale, ws + L.w_off, bias, out, M, N, K, *d, st);
 }
 
-int w4a8_prefill_linear(const float* x, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero,
-                        const float* bias, float* y, int64_t M, int64_t N, int64_t K, void* workspace,
-                        size_t workspace_bytes, void* stream) {
+int prefill_impl(const float* x, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero,
+                 const float* bias, const OutSpec& out, int64_t M, int64_t N, int64_t K, void* workspace,
+                 size_t workspace_bytes, void* stream) {
     int rc = check_shape(M, N, K);
     if (rc != W4A8_OK) return rc;
     if (M == 0 || N == 0) return W4A8_OK;
-    if (!x || !wq || !w_scale || !w_zero || !y) return W4A8_ERR_ARG;
-    if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(y, 16) || !aligned(w_scale, 2) || !aligned(w_zero, 2) ||
+    if (!x || !wq || !w_scale || !w_zero || !out.y) return W4A8_ERR_ARG;
+    if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(out.y, 16) || !aligned(w_scale, 2) || !aligned(w_zero, 2) ||
         (bias && !aligned(bias, 4)))
         return W4A8_ERR_ALIGN;
     const size_t need = prefill_ws(M, N, K);
@@ -270,7 +319,7 @@ int w4a8_prefill_linear(const float* x, const uint8_t* wq, const uint16_t* w_sca
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     if (few_tokens(M, K) && gemv_quantizes(M, K)) {
         // few-token form, one launch: the weight-streaming kernel quantizes x itself
-        return run_gemv(x, nullptr, nullptr, nullptr, wq, w_scale, w_zero, bias, y, M, N, K, *d, st);
+        return run_gemv(x, nullptr, nullptr, nullptr, wq, w_scale, w_zero, bias, out, M, N, K, *d, st);
     }
     if (few_tokens(M, K)) {
         // few-token form: the pre-pass in the API layout, then the weight-streaming kernel
@@ -283,7 +332,7 @@ int w4a8_prefill_linear(const float* x, const uint8_t* wq, const uint16_t* w_sca
         p.s_a_out = reinterpret_cast<float*>(ws + D.s_a);
         p.rs_out = reinterpret_cast<int32_t*>(ws + D.rs);
         if (launch_quant(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
-        return run_gemv(nullptr, p.a_q_out, p.s_a_out, p.rs_out, wq, w_scale, w_zero, bias, y, M, N, K, *d, st);
+        return run_gemv(nullptr, p.a_q_out, p.s_a_out, p.rs_out, wq, w_scale, w_zero, bias, out, M, N, K, *d, st);
     }
     const CallLayout L = call_layout(M, N, K, true);
     float* s_a = reinterpret_cast<float*>(ws + L.act.s_a);
@@ -295,7 +344,43 @@ int w4a8_prefill_linear(const float* x, const uint8_t* wq, const uint16_t* w_sca
     p.tw = L.act.tw;
     set_weight_job(&p, wq, w_scale, w_zero, N, K, ws + L.w_off);
     if (launch_quant(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
-    return run_linear(ws + L.act.rec, s_a, ws + L.w_off, bias, y, M, N, K, *d, st);
+    return run_linear(ws + L.act.rec, s_a, ws + L.w_off, bias, out, M, N, K, *d, st);
+}
+
+int linear_prepared_impl(const void* act, const void* pw, const float* bias, const OutSpec& out, int64_t M,
+                         int64_t N, int64_t K, void* stream) {
+    int rc = check_shape(M, N, K);
+    if (rc != W4A8_OK) return rc;
+    if (M == 0 || N == 0) return W4A8_OK;
+    if (!act || !pw || !out.y) return W4A8_ERR_ARG;
+    if (!aligned(act, 16) || !aligned(pw, 16) || !aligned(out.y, 16) || (bias && !aligned(bias, 4)))
+        return W4A8_ERR_ALIGN;
+    DeviceInfo* d = nullptr;
+    if ((rc = current_device(&d)) != W4A8_OK) return rc;
+    const ActLayout A = act_layout(M, K, true, token_tile(M));
+    const uint8_t* a = static_cast<const uint8_t*>(act);
+    return run_linear(a + A.rec, reinterpret_cast<const float*>(a + A.s_a), static_cast<const uint8_t*>(pw), bias,
+                      out, M, N, K, *d, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace w4a8
+
+extern "C" {
+
+int w4a8_prefill_linear(const float* x, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero,
+                        const float* bias, float* y, int64_t M, int64_t N, int64_t K, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    return prefill_impl(x, wq, w_scale, w_zero, bias, f32_out(y), M, N, K, workspace, workspace_bytes, stream);
+}
+
+int w4a8_prefill_linear_ex(const float* x, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero,
+                           const float* bias, void* y, int out_dtype, float clamp_lo, float clamp_hi, int64_t M,
+                           int64_t N, int64_t K, void* workspace, size_t workspace_bytes, void* stream) {
+    OutSpec o;
+    const int rc = make_out(y, out_dtype, clamp_lo, clamp_hi, &o);
+    if (rc != W4A8_OK) return rc;
+    return prefill_impl(x, wq, w_scale, w_zero, bias, o, M, N, K, workspace, workspace_bytes, stream);
 }
 
 int w4a8_prepare_activations(const float* x, int64_t M, int64_t K, void* act, size_t act_bytes, void* stream) {
@@ -338,17 +423,15 @@ int w4a8_prepare_weights(const uint8_t* wq, const uint16_t* w_scale, const uint1
 
 int w4a8_linear_prepared(const void* act, const void* pw, const float* bias, float* y, int64_t M, int64_t N,
                          int64_t K, void* stream) {
-    int rc = check_shape(M, N, K);
+    return linear_prepared_impl(act, pw, bias, f32_out(y), M, N, K, stream);
+}
+
+int w4a8_linear_prepared_ex(const void* act, const void* pw, const float* bias, void* y, int out_dtype,
+                            float clamp_lo, float clamp_hi, int64_t M, int64_t N, int64_t K, void* stream) {
+    OutSpec o;
+    const int rc = make_out(y, out_dtype, clamp_lo, clamp_hi, &o);
     if (rc != W4A8_OK) return rc;
-    if (M == 0 || N == 0) return W4A8_OK;
-    if (!act || !pw || !y) return W4A8_ERR_ARG;
-    if (!aligned(act, 16) || !aligned(pw, 16) || !aligned(y, 16) || (bias && !aligned(bias, 4))) return W4A8_ERR_ALIGN;
-    DeviceInfo* d = nullptr;
-    if ((rc = current_device(&d)) != W4A8_OK) return rc;
-    const ActLayout A = act_layout(M, K, true, token_tile(M));
-    const uint8_t* a = static_cast<const uint8_t*>(act);
-    return run_linear(a + A.rec, reinterpret_cast<const float*>(a + A.s_a), static_cast<const uint8_t*>(pw), bias, y,
-                      M, N, K, *d, static_cast<cudaStream_t>(stream));
+    return linear_prepared_impl(act, pw, bias, o, M, N, K, stream);
 }
 
 int w4a8_debug_block_acc(const int8_t* a_q, const uint8_t* wq, int64_t M, int64_t N, int64_t K, int64_t m0,

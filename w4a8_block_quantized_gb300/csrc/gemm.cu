@@ -48,6 +48,7 @@
 // wait), releases their buffers as soon as the accumulators are in registers, then folds
 // them into y; it frees a stage once its accumulators are complete.  Every wait is bounded (WaitCtl); a CTA
 // that gives up records a timeout and unwinds.
+#include "epilogue.cuh"
 #include "sm103_ptx.cuh"
 #include "w4a8_internal.h"
 
@@ -348,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     const int64_t m = mt0 + c;
-                    if (m < args.M) args.y[m * args.N + n] = fmaf(args.s_a[m], y[c], bn);
+                    if (m < args.M) store_y(args.out, m * args.N + n, fmaf(args.s_a[m], y[c], bn));
                 }
             }
         }
@@ -553,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const int64_t m = mt0 + c;
-                    if (m < args.M) args.y[m * args.N + n] = fmaf(args.s_a[m], y[c], bn);
+                    if (m < args.M) store_y(args.out, m * args.N + n, fmaf(args.s_a[m], y[c], bn));
                 }
             }
         }

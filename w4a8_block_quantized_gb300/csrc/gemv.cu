@@ -36,6 +36,7 @@
 // Every wait is bounded; a CTA that gives up records a timeout and unwinds.
 #include <cuda_fp16.h>
 
+#include "epilogue.cuh"
 #include "quant_math.cuh"
 #include "sm103_ptx.cuh"
 #include "w4a8_internal.h"
@@ -441,7 +442,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     for (int m = 1; m < MT; ++m)
                         if (lane == m) v = sum[j][m];
                     if (rok[j] && lane < MT)
-                        a.y[static_cast<int64_t>(lane) * N + n] = fmaf(sa_sm[lane], v, a.bias ? a.bias[n] : 0.0f);
+                        store_y(a.out, static_cast<int64_t>(lane) * N + n, fmaf(sa_sm[lane], v, a.bias ? a.bias[n] : 0.0f));
                 }
             } else {
                 // the row's warps meet (every warp meets once per tile, whatever its waits gave)
@@ -453,7 +454,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 if (sidx == 0 && rok[0] && lane < MT) {
                     float v = 0.0f;
                     for (int q = 0; q < wpr; ++q) v += red[i & 1][rslot * wpr + q][lane];
-                    a.y[static_cast<int64_t>(lane) * N + n] = fmaf(sa_sm[lane], v, a.bias ? a.bias[n] : 0.0f);
+                    store_y(a.out, static_cast<int64_t>(lane) * N + n, fmaf(sa_sm[lane], v, a.bias ? a.bias[n] : 0.0f));
                 }
             }
         }

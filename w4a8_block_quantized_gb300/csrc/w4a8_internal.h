@@ -9,6 +9,14 @@
 
 namespace w4a8 {
 
+// Where and how an epilogue stores y: clamp(s_a * sum + bias, lo, hi) as fp32 or bf16
+// (round to nearest even).  lo = -inf, hi = +inf store the value unchanged.
+struct OutSpec {
+    void* y = nullptr;  // [M][N] fp32 or bf16
+    int bf16 = 0;
+    float lo = -__builtin_huge_valf(), hi = __builtin_huge_valf();
+};
+
 // Bits of the per-device status word (a kernel ORs them in; the host reads and clears).
 constexpr uint32_t kStatusTimeout = 1u;
 
@@ -125,7 +133,7 @@ struct GemmArgs {
     const float* sc = nullptr;          // weight scales [ceil(N/128)][K/64][128]
     const float* s_a = nullptr;
     const float* bias = nullptr;
-    float* y = nullptr;                 // [M][N]
+    OutSpec out;                        // y [M][N]
     int32_t* acc = nullptr;             // debug: [M][N][K/64]
     uint32_t* status = nullptr;
     uint64_t wait_limit_ns = 1000000000ull;
@@ -149,7 +157,7 @@ struct GemvArgs {
     const uint16_t* s_w = nullptr;      // fp16 bits [N][K/64]
     const uint16_t* z_w = nullptr;
     const float* bias = nullptr;
-    float* y = nullptr;                 // [M][N]
+    OutSpec out;                        // y [M][N]
     int64_t M = 0, N = 0, K = 0;
 };
 
