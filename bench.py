@@ -369,6 +369,10 @@ def run_bench(args):
     h2d = sum(s.M * s.K * 4 for s in specs)
     d2h = sum(s.M * s.N * 4 for s in specs)
 
+    layer = None
+    if args.workload in ("c3", "d3") and not args.shape:
+        layer = layer_step(lin, specs, stream, flush, max(20, min(args.steps, 200)), decode)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(lin, specs, args.cpu_seconds)
@@ -431,11 +435,94 @@ def run_bench(args):
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
+    if layer is not None:
+        out["layer"] = layer
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ decoder layer as a layer
+# Inputs a real decoder layer shares: q, k, v read one activation, gate and up another.  A
+# layer stores each such group's weights with their rows concatenated (one linear of
+# N = sum of the group's N), so the shared input is quantized once and contracted in one call.
+LAYER_GROUPS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
+
+
+def layer_step(lin, specs, stream, flush, reps, decode):
+    """The 7-linear set run the way a decoder layer runs it: q/k/v and gate/up as
+    row-concatenated groups on their shared inputs (4 linears).  Prefill: weights prepared
+    once at load time, per step one pre-pass and one contraction per group; decode: one
+    few-token call per group (one launch each).  Timed per step (L2 flushed before each,
+    outside the events) as eager calls and replayed from a command tape."""
+    from w4a8_block_quantized_gb300 import binding
+    by = {t["spec"].name: t for t in lin}
+    M = specs[0].M
+    dev = lin[0]["x"].device
+    calls = []
+    for grp in LAYER_GROUPS:
+        ts = [by[nm] for nm in grp]
+        K = ts[0]["spec"].K
+        N = sum(t["spec"].N for t in ts)
+        x = ts[0]["x"]
+        wq = torch.cat([t["wq"] for t in ts]).contiguous()
+        s_w = torch.cat([t["s_w"] for t in ts]).contiguous()
+        z_w = torch.cat([t["z_w"] for t in ts]).contiguous()
+        bias = None
+        if any(t["bias"] is not None for t in ts):
+            bias = torch.cat([t["bias"] if t["bias"] is not None else torch.zeros(t["spec"].N, device=dev)
+                              for t in ts]).contiguous()
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        if decode:
+            ws = binding.workspace(binding.prefill_workspace_bytes(M, N, K), dev)
+            calls.append(lambda s, x=x, wq=wq, s_w=s_w, z_w=z_w, bias=bias, y=y, ws=ws: binding.prefill_linear(
+                x, wq, s_w, z_w, bias, y=y, ws=ws, stream=s))
+        else:
+            act = binding.workspace(binding.prepared_activations_bytes(M, K), dev)
+            pw = binding.prepare_weights(wq, s_w, z_w, stream=stream)
+            calls.append(lambda s, x=x, act=act: binding.prepare_activations(x, act=act, stream=s))
+            calls.append(lambda s, act=act, pw=pw, N=N, K=K, bias=bias, y=y: binding.linear_prepared(
+                act, pw, M, N, K, bias=bias, y=y, stream=s))
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for c in calls:
+            c(side)                      # one ordinary call of each before recording
+        with binding.Tape(side) as tape:
+            for c in calls:
+                c(side)
+    side.synchronize()
+
+    def timed(run):
+        ms = []
+        for i in range(reps + 3):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(side)
+            run()
+            b.record(side)
+            b.synchronize()
+            if i >= 3:
+                ms.append(a.elapsed_time(b))
+        return statistics.fmean(ms)
+
+    with torch.cuda.stream(side):
+        side.wait_stream(torch.cuda.current_stream())
+        t_eager = timed(lambda: [c(side) for c in calls])
+        t_tape = timed(lambda: tape.replay(side))
+    if binding.sync_status(side) != 0:
+        raise RuntimeError("device status reported a timeout in the layer step")
+    tape.free()
+    ops = sum(s.ops for s in specs)
+    return {"mode": ("q/k/v and gate/up as row-concatenated groups on shared inputs (4 linears); " +
+                     ("one few-token launch per group" if decode else
+                      "weights prepared at load, per group one pre-pass + one contraction")),
+            "launches_per_step": len(calls),
+            "ms_per_step_eager": round(t_eager, 5), "ms_per_step_tape": round(t_tape, 5),
+            "tok_s_tape": round(M / (t_tape * 1e-3), 1), "tops_tape": round(ops / (t_tape * 1e-3) / 1e12, 3),
+            "l2": "flushed before every step (outside the events)"}
 
 
 # ------------------------------------------------------------------ CPU oracle legs

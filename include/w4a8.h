@@ -23,7 +23,8 @@
  *
  * Conventions for every call below:
  *   - Every array pointer is a DEVICE pointer owned by the caller; the library never
- *     allocates, frees or retains memory.  Scratch comes from the caller's `workspace`.
+ *     allocates, frees or retains memory (command tapes, below, are the one exception).
+ *     Scratch comes from the caller's `workspace`.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
  *     asynchronous: W4A8_OK means the work was validated and enqueued.
  *   - Shapes: K must be a positive multiple of 64; M >= 0 and N >= 0 (M == 0 or
@@ -181,6 +182,24 @@ size_t w4a8_debug_workspace_bytes(int64_t m_cnt, int64_t n_cnt, int64_t K);
 int w4a8_debug_block_acc(const int8_t *a_q, const uint8_t *wq, int64_t M, int64_t N, int64_t K,
                          int64_t m0, int64_t m_cnt, int64_t n0, int64_t n_cnt, int32_t *acc,
                          void *workspace, size_t workspace_bytes, void *stream);
+
+/* Command tapes (the XNet-DNN GPU inference article, section 2.3 "RCI Command Tape": a
+ * frame's kernel queue is recorded once and replayed).  Between w4a8_tape_begin(stream)
+ * and w4a8_tape_end(stream, &tape), the w4a8_* calls enqueued on `stream` are recorded, not
+ * run; w4a8_tape_replay(tape, s) then runs the whole sequence with one launch on any
+ * stream of the same device.  A replay reads and writes the very buffers the recorded calls
+ * named: their contents may change between replays, their addresses and sizes must stay
+ * valid until w4a8_tape_free.  Recording goes through CUDA stream capture (thread-local
+ * mode), so `stream` must be a non-default stream that is not already capturing
+ * (W4A8_ERR_ARG otherwise), and everything else enqueued on it meanwhile -- by this thread --
+ * is recorded as well.  The tape object (host memory plus the driver's executable graph) is
+ * the one resource the library allocates; w4a8_tape_free releases it.  Make one ordinary
+ * call of each shape before recording, so no one-time setup falls inside the capture. */
+typedef struct w4a8_tape w4a8_tape;
+int w4a8_tape_begin(void *stream);
+int w4a8_tape_end(void *stream, w4a8_tape **tape);
+int w4a8_tape_replay(const w4a8_tape *tape, void *stream);
+void w4a8_tape_free(w4a8_tape *tape);
 
 /* Synchronizes `stream`, then returns and clears the current device's status word:
  * W4A8_OK, W4A8_ERR_TIMEOUT if a kernel gave up on a wait since the last call, or

@@ -116,3 +116,13 @@ def test_epilogue_arguments_rejected_before_launch(lib):
         assert lib.w4a8_prefill_linear_ex(d, d, d, d, None, d, dt, lo, hi, 4, 8, 64, None, 0, None) == b.W4A8_ERR_ARG
         assert lib.w4a8_linear_ex(d, d, d, d, d, d, None, d, dt, lo, hi, 4, 8, 64, None, 0, None) == b.W4A8_ERR_ARG
         assert lib.w4a8_linear_prepared_ex(d, d, None, d, dt, lo, hi, 4, 8, 64, None) == b.W4A8_ERR_ARG
+
+
+def test_tape_arguments_rejected(lib):
+    from w4a8_block_quantized_gb300 import binding as b
+    assert lib.w4a8_tape_begin(None) == b.W4A8_ERR_ARG            # the default stream is not captured
+    h = ctypes.c_void_p()
+    assert lib.w4a8_tape_end(None, ctypes.byref(h)) == b.W4A8_ERR_ARG
+    assert lib.w4a8_tape_end(ctypes.c_void_p(1 << 20), None) == b.W4A8_ERR_ARG
+    assert lib.w4a8_tape_replay(None, None) == b.W4A8_ERR_ARG
+    lib.w4a8_tape_free(None)                                      # a no-op

@@ -442,3 +442,94 @@ def test_epilogue_argument_checks():
     assert lib.w4a8_prefill_linear_ex(*args, 0, float("nan"), 1.0, 4, 8, 64, None, 0, b._stream(None)) == \
         b.W4A8_ERR_ARG
     assert b.sync_status() == 0
+
+
+# ------------------------------------------------------------------ command tapes
+def test_tape_replays_a_mixed_sequence():
+    """A tape recording the fused call at three forms (128-token, 256-token, few-token), the
+    bf16 variant, and one pre-pass shared by two prepared linears, replays bit for bit what
+    the same calls give eagerly -- and again after the inputs change in place."""
+    b = B()
+    stream = torch.cuda.Stream()
+    shapes = [(300, 1024, 700), (4100, 512, 300), (1, 2048, 1000), (3, 4096, 200)]
+    ds = [synth.random_small(M, K, N, seed=40 + i, bias=True) for i, (M, K, N) in enumerate(shapes)]
+    gs = [inputs_to_dev(d) for d in ds]
+    outs = [torch.empty((M, N), device=dev()) for M, K, N in shapes]
+    wss = [b.workspace(b.prefill_workspace_bytes(M, N, K), dev()) for M, K, N in shapes]
+    yb = torch.empty((300, 700), dtype=torch.bfloat16, device=dev())
+    # shared pre-pass: one input, two prepared weight sets
+    dq = synth.random_small(256, 2048, 512, seed=50, bias=False)
+    dk = synth.random_small(256, 2048, 384, seed=51, bias=True)
+    xq = to_dev(dq["x"])
+    pq = b.prepare_weights(to_dev(dq["wq"]), to_dev(dq["s_w"]), to_dev(dq["z_w"]))
+    pk = b.prepare_weights(to_dev(dk["wq"]), to_dev(dk["s_w"]), to_dev(dk["z_w"]))
+    act = b.workspace(b.prepared_activations_bytes(256, 2048), dev())
+    yq = torch.empty((256, 512), device=dev())
+    yk = torch.empty((256, 384), device=dev())
+    bk = to_dev(dk["bias"])
+
+    def calls(s):
+        for g, y, ws in zip(gs, outs, wss):
+            b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"], y=y, ws=ws, stream=s)
+        b.prefill_linear_ex(gs[0]["x"], gs[0]["wq"], gs[0]["s_w"], gs[0]["z_w"], gs[0]["bias"], y=yb,
+                            clamp=(-1.0, 1.0), ws=wss[0], stream=s)
+        b.prepare_activations(xq, act=act, stream=s)
+        b.linear_prepared(act, pq, 256, 512, 2048, y=yq, stream=s)
+        b.linear_prepared(act, pk, 256, 384, 2048, bias=bk, y=yk, stream=s)
+
+    results = lambda: [o.clone() for o in outs] + [yb.clone(), yq.clone(), yk.clone()]
+    with torch.cuda.stream(stream):
+        calls(stream)
+    stream.synchronize()
+    eager = results()
+    with torch.cuda.stream(stream):
+        with b.Tape(stream) as tape:
+            calls(stream)
+    for o in outs + [yq, yk]:
+        o.fill_(float("nan"))
+    yb.fill_(float("nan"))
+    tape.replay(stream)
+    stream.synchronize()
+    for e, r in zip(eager, results()):
+        assert torch.equal(e, r)
+    # new inputs, same buffers: the replay follows them
+    for g in gs:
+        g["x"].mul_(-0.5)
+    xq.add_(0.25)
+    with torch.cuda.stream(stream):
+        calls(stream)
+    stream.synchronize()
+    eager2 = results()
+    for o in outs + [yq, yk]:
+        o.zero_()
+    tape.replay(stream)
+    stream.synchronize()
+    for e, r in zip(eager2, results()):
+        assert torch.equal(e, r)
+    assert not torch.equal(eager[0], eager2[0])
+    tape.free()
+    assert b.sync_status() == 0
+
+
+@pytest.mark.parametrize("M", [512, 1])
+def test_row_concatenated_group_equals_members(M):
+    """q/k/v stored as one row-concatenated weight matrix: one call gives each member's
+    outputs in its column range -- every output within tolerance of the oracle, and, for the
+    tensor-core form (whose per-output arithmetic does not depend on N), bit for bit the
+    separate calls' outputs."""
+    b = B()
+    Ns = (512, 256, 256)
+    K = 2048
+    ds = [synth.random_small(M, K, N, seed=60 + i, bias=True) for i, N in enumerate(Ns)]
+    x = ds[0]["x"]
+    g = {k: to_dev(np.concatenate([d[k] for d in ds])) for k in ("wq", "s_w", "z_w", "bias")}
+    y = b.prefill_linear(to_dev(x), g["wq"], g["s_w"], g["z_w"], g["bias"])
+    off = 0
+    for d, N in zip(ds, Ns):
+        gi = inputs_to_dev(d)
+        yi = b.prefill_linear(to_dev(x), gi["wq"], gi["s_w"], gi["z_w"], gi["bias"])
+        y_ref, bound, _, _, _ = oracle.prefill_linear(x, d["wq"], d["s_w"], d["z_w"], d["bias"])
+        check_y(y[:, off:off + N], y_ref, bound, f"group member N={N}")
+        if M > 8:
+            assert torch.equal(y[:, off:off + N], yi)
+        off += N

@@ -53,6 +53,10 @@ SIGNATURES = {
     "w4a8_prefill_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "w4a8_debug_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "w4a8_debug_block_acc": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P, _SZ, _P]),
+    "w4a8_tape_begin": (ctypes.c_int, [_P]),
+    "w4a8_tape_end": (ctypes.c_int, [_P, ctypes.POINTER(_P)]),
+    "w4a8_tape_replay": (ctypes.c_int, [_P, _P]),
+    "w4a8_tape_free": (None, [_P]),
     "w4a8_sync_status": (ctypes.c_int, [_P]),
     "w4a8_selftest_wait_timeout": (ctypes.c_int, [_I64, _P]),
     "w4a8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -304,3 +308,44 @@ def sync_status(stream=None) -> int:
 
 def selftest_wait_timeout(limit_us: int, stream=None) -> None:
     _check(load().w4a8_selftest_wait_timeout(int(limit_us), _stream(stream)), "w4a8_selftest_wait_timeout")
+
+
+class Tape:
+    """A recorded call sequence (w4a8_tape_*): `with Tape(stream) as t:` records the library
+    calls made on `stream` inside the block; `t.replay(stream)` runs them again with one
+    launch.  The tensors the recorded calls used must stay alive while the tape is."""
+
+    def __init__(self, stream):
+        self.stream = stream
+        self.handle = None
+
+    def __enter__(self):
+        _check(load().w4a8_tape_begin(_stream(self.stream)), "w4a8_tape_begin")
+        return self
+
+    def __exit__(self, exc_type, exc, tb):
+        h = _P()
+        rc = load().w4a8_tape_end(_stream(self.stream), ctypes.byref(h))
+        if exc_type is None:
+            _check(rc, "w4a8_tape_end")
+            self.handle = h
+        elif rc == 0 and h:
+            load().w4a8_tape_free(h)
+        return False
+
+    def replay(self, stream=None):
+        if self.handle is None:
+            raise RuntimeError("tape not recorded")
+        _check(load().w4a8_tape_replay(self.handle, _stream(stream)), "w4a8_tape_replay")
+
+    def free(self):
+        if self.handle is not None:
+            load().w4a8_tape_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
