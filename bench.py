@@ -159,20 +159,23 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ ncu traffic record
 def recorded_traffic(workload: str):
-    """DRAM bytes (read + write) per GEMM launch from the committed ncu capture of this
-    workload, or None when there is none or gemm.cu changed since it was taken."""
+    """DRAM bytes (read + write) per launch of the workload's dominant kernel from the
+    committed ncu launch list, or None when there is none or that kernel's source changed
+    since it was taken."""
     import hashlib
     rec = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "w4a8_block_quantized_gb300", "csrc", "gemm.cu")
     if not os.path.exists(rec):
         return None
     with open(rec) as f:
-        d = json.load(f)
-    with open(src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()
-    e = d.get(workload)
-    if not e or e.get("gemm_cu_sha256") != sha:
+        e = json.load(f).get(workload)
+    if not e:
         return None
+    src = os.path.join(ROOT, e.get("source", ""))
+    if not os.path.isfile(src):
+        return None
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != e.get("sha256"):
+            return None
     return e.get("dram_bytes_per_launch")
 
 
@@ -381,7 +384,8 @@ def run_bench(args):
     if decode:
         roofline = {"bound": "hbm", "kernel": "gemv_kernel (packed u4 weights streamed, dp4a blocks + f32 epilogue)",
                     "achieved": round(gemv_gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
-                    "frac": round(gemv_gbs / hbm_gbs, 4), "traffic": None, "peak_source": peak_src,
+                    "frac": round(gemv_gbs / hbm_gbs, 4),
+                    "traffic": None if args.shape else recorded_traffic(args.workload), "peak_source": peak_src,
                     "bytes_per_launch": int(gemv_bytes), "gemv_us_per_launch": round(gemm_avg * 1e3, 3)}
     else:
         roofline = {"bound": "tensor", "kernel": "gemm_kernel (tcgen05 kind::f8f6f4 + epilogue)",
