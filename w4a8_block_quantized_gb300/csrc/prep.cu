@@ -80,6 +80,41 @@ __device__ __forceinline__ uint32_t bytes4f(float4 q) {
 
 __device__ __forceinline__ float h2f(uint16_t bits) { return __half2float(__ushort_as_half(bits)); }
 
+// The sums of H values (H in {1, 2, 4}) over each 16-lane half of the warp, reduced together:
+// every halving step sends half of a lane's remaining values to its partner and keeps the
+// other half, so H sums cost log2(H) + 4 shuffle steps instead of 4 H.  Lane l then holds
+// value j = jsel(l) of its half's sums; lanes with (l & (16 / H - 1)) == 0 hold distinct j.
+// The values are exact small integers, so every order gives the same bits.
+template <int H>
+__device__ __forceinline__ float half_warp_sums(const float (&p)[H], int lane, int& j) {
+    float v;
+    if constexpr (H == 4) {
+        const bool u8 = lane & 8, u4 = lane & 4;
+        float a0 = u8 ? p[2] : p[0], a1 = u8 ? p[3] : p[1];
+        const float s0 = u8 ? p[0] : p[2], s1 = u8 ? p[1] : p[3];
+        a0 += __shfl_xor_sync(0xffffffffu, s0, 8);
+        a1 += __shfl_xor_sync(0xffffffffu, s1, 8);
+        v = u4 ? a1 : a0;
+        v += __shfl_xor_sync(0xffffffffu, u4 ? a0 : a1, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        j = (u8 ? 2 : 0) + (u4 ? 1 : 0);
+    } else if constexpr (H == 2) {
+        const bool u8 = lane & 8;
+        v = u8 ? p[1] : p[0];
+        v += __shfl_xor_sync(0xffffffffu, u8 ? p[0] : p[1], 8);
+#pragma unroll
+        for (int o = 4; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        j = u8 ? 1 : 0;
+    } else {
+        v = p[0];
+#pragma unroll
+        for (int o = 8; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        j = 0;
+    }
+    return v;
+}
+
 // u4 pairs -> bytes in k order: nibbles k0..k7 of w become bytes of (o0: k0..k3, o1: k4..k7).
 // A byte holding the code q is the e4m3 encoding of q * 2^-9, the GEMM's weight operand.
 __device__ __forceinline__ void expand8(uint32_t w, uint32_t& o0, uint32_t& o1) {
@@ -220,22 +255,17 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) quant_kernel(const P
                     }
                 }
             }
-#pragma unroll
-            for (int o = 8; o; o >>= 1)
-#pragma unroll
-                for (int j = 0; j < H; ++j) part[j] += __shfl_xor_sync(0xffffffffu, part[j], o);
-            if (active && (lane & 15) == 0) {
-#pragma unroll
-                for (int j = 0; j < H; ++j) {
-                    const int64_t f = static_cast<int64_t>((h0 + j) * G + wg) * 32 + lane;
-                    if (f < n4) {
-                        const int64_t b = f >> 4;
-                        const int rs = static_cast<int>(part[j]);
-                        if (PLANES)
-                            *reinterpret_cast<uint4*>(token_rec(a.trec, m, b, nb, ts) + (128 << ts) + (m & ((1 << ts) - 1)) * 16) =
-                                rx_entry(rs);
-                        else a.rs_out[m * nb + b] = rs;
-                    }
+            int jj;
+            const float bsum = half_warp_sums<H>(part, lane, jj);
+            if (active && (lane & (16 / H - 1)) == 0) {
+                const int64_t f = static_cast<int64_t>((h0 + jj) * G + wg) * 32 + lane;
+                if (f < n4) {
+                    const int64_t b = f >> 4;
+                    const int rs = static_cast<int>(bsum);
+                    if (PLANES)
+                        *reinterpret_cast<uint4*>(token_rec(a.trec, m, b, nb, ts) + (128 << ts) + (m & ((1 << ts) - 1)) * 16) =
+                            rx_entry(rs);
+                    else a.rs_out[m * nb + b] = rs;
                 }
             }
         }
