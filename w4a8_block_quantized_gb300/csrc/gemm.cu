@@ -76,7 +76,7 @@ constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 constexpr uint32_t kTmemCols = kNBuf * kTileT;
 static_assert(kTokRec % 1024 == 0 && kWRec % 1024 == 0 && kStageBytes % 1024 == 0,
               "swizzled operand tiles must stay 1024-aligned");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kSmemBytes + 2 * 16 * 32 * 4 <= 227 * 1024, "shared memory budget (with the static epilogue slots)");
 static_assert(kTmemCols == 512, "TMEM allocation");
 static_assert(kNBuf / 2 <= kStages, "a stage barrier carries a buffer release only after its previous phase");
 static_assert(kZeroBytes >= kTileW * 16 && kZeroBytes >= kTileT * 16, "zero half of the zero-point operands");
@@ -140,6 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* drain = tfull + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile uint32_t* abort_flag = tmem_slot + 1;
+    __shared__ float epi_sa[kEpiWarps][32];    // per epilogue warp: the tile's s_a of its columns
+    __shared__ float epi_bias[kEpiWarps][32];  // per epilogue thread: the bias of its row
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tiles_t = (args.M + kTileT - 1) / kTileT;
@@ -282,6 +284,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t n = tw * kTileW + row;       // this thread's weight row
             // this row's scales, block after block; each stage's pair is loaded one stage ahead
             const float* sct = DEBUG ? nullptr : args.sc + static_cast<int64_t>(tw) * nb * kTileW + row;
+            if (!DEBUG) {
+                // this tile's s_a and bias, loaded now into the warp's own slots so the stores at
+                // the end of the tile neither wait on memory nor hold registers through the loop
+                epi_sa[warp - 4][lane] = mt0 + lane < args.M ? __ldg(args.s_a + mt0 + lane) : 0.0f;
+                epi_bias[warp - 4][lane] = (args.bias && n < args.N) ? __ldg(args.bias + n) : 0.0f;
+            }
             float ns0 = 0.0f, ns1 = 0.0f;
             if (!DEBUG) {
                 ns0 = __ldg(sct);
@@ -344,12 +352,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) break;
+            if (!DEBUG) __syncwarp();  // every lane: the slots were written by other lanes of the warp
             if (!DEBUG && n < args.N) {
-                const float bn = args.bias ? args.bias[n] : 0.0f;
+                const float bn = epi_bias[warp - 4][lane];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     const int64_t m = mt0 + c;
-                    if (m < args.M) store_y(args.out, m * args.N + n, fmaf(args.s_a[m], y[c], bn));
+                    if (m < args.M) store_y(args.out, m * args.N + n, fmaf(epi_sa[warp - 4][c], y[c], bn));
                 }
             }
         }

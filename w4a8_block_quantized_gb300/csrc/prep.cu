@@ -176,6 +176,9 @@ __device__ void weights_job(const PrepArgs& a, int64_t cta, int64_t ctas) {
 // With V <= 8 the next iteration's row is loaded while the current one is quantized.
 template <int G, int V, bool PLANES, int NW>
 __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) quant_kernel(const PrepArgs a, int row_ctas) {
+    // the next kernel in the stream (the contraction, a programmatic dependent) may launch and
+    // run its set-up now; it waits for this whole grid to complete before reading its outputs
+    griddep_launch_dependents();
     if (static_cast<int>(blockIdx.x) >= row_ctas) {
         if (a.wrec) weights_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
         return;
@@ -282,6 +285,9 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) quant_kernel(const P
 // the row (from L2 in practice; HBM traffic stays one read).
 template <bool PLANES>
 __global__ void __launch_bounds__(256) quant_long_kernel(const PrepArgs a, int row_ctas) {
+    // the next kernel in the stream (the contraction, a programmatic dependent) may launch and
+    // run its set-up now; it waits for this whole grid to complete before reading its outputs
+    griddep_launch_dependents();
     if (static_cast<int>(blockIdx.x) >= row_ctas) {
         if (a.wrec) weights_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
         return;
@@ -349,6 +355,9 @@ __global__ void __launch_bounds__(256) quant_long_kernel(const PrepArgs a, int r
 // Pack pre-quantized int8 codes into the tensor-core planes; transpose the row sums;
 // re-lay out the weight scales.  Rows row0 .. row0 + M - 1 of a_q_in.
 __global__ void __launch_bounds__(256) pack_kernel(const PrepArgs a, int row_ctas) {
+    // the next kernel in the stream (the contraction, a programmatic dependent) may launch and
+    // run its set-up now; it waits for this whole grid to complete before reading its outputs
+    griddep_launch_dependents();
     if (static_cast<int>(blockIdx.x) >= row_ctas) {
         if (a.wrec) weights_job(a, blockIdx.x - row_ctas, gridDim.x - row_ctas);
         return;
