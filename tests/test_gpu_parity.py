@@ -533,3 +533,24 @@ def test_row_concatenated_group_equals_members(M):
         if M > 8:
             assert torch.equal(y[:, off:off + N], yi)
         off += N
+
+
+@pytest.mark.parametrize("M,K,N,launches", [(1, 4096, 14336, 300), (1, 14336, 4096, 300), (8, 4096, 3000, 200)])
+def test_decode_repeated_launches_complete_and_identical(M, K, N, launches):
+    """Back-to-back few-token calls (one launch each when the kernel quantizes, pre-pass plus
+    kernel at M = 8, K = 4096): a clean status word and the same bits every time; the first
+    output against the oracle."""
+    b = B()
+    d = synth.make_linear(synth.LinearSpec("stress", M, K, N, True))
+    g = inputs_to_dev(d)
+    y0 = b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"])
+    assert b.sync_status() == 0
+    ws = b.workspace(b.prefill_workspace_bytes(M, N, K), dev())
+    y = torch.empty_like(y0)
+    for i in range(launches):
+        b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"], y=y, ws=ws)
+        if i % 50 == 49:
+            assert b.sync_status() == 0, f"launch {i}"
+            assert torch.equal(y, y0), f"launch {i}"
+    y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
+    check_y(y0, y_ref, bound, f"decode {M}x{K}->{N}")
