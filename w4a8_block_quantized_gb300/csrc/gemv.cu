@@ -166,6 +166,11 @@ __device__ __forceinline__ void half_span(const uint16_t* base, int64_t e0, int6
     skew = static_cast<uint32_t>(a0 - s0);
 }
 
+// A float code (an exact integer in [-127, 127]) as a word whose low byte is the code in two's
+// complement: adding 1.5 * 2^23 puts the integer in the low mantissa bits.  One fp32 add, not
+// a conversion instruction.
+__device__ __forceinline__ int code_bits(float q) { return static_cast<int>(__float_as_uint(__fadd_rn(q, 12582912.0f))); }
+
 // Low bytes of four int codes, c0 in byte 0.
 __device__ __forceinline__ uint32_t pack4(int c0, int c1, int c2, int c3) {
     return __byte_perm(__byte_perm(c0, c1, 0x0040), __byte_perm(c2, c3, 0x0040), 0x5410);
@@ -314,10 +319,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 for (int u0 = warp * 32; u0 < units; u0 += kCW * 32) {  // warp-uniform trip count
                     const int u = u0 + lane, b = u >> 2, p = u & 3;
                     const bool on = got && u < units;
+                    // slot j holds float4 (j + rot) % 4 of the unit: consecutive lanes sit 64 bytes
+                    // apart, and the rotation spreads each 8-lane phase of the loads over all banks
+                    const int rot = (lane >> 1) & 3;
                     float4 xs[4], q[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const uint4 v = on ? lds128(xr + static_cast<uint32_t>((64 * b + 16 * p + 4 * j) * 4))
+                        const int jj = (j + rot) & 3;
+                        const uint4 v = on ? lds128(xr + static_cast<uint32_t>((64 * b + 16 * p + 4 * jj) * 4))
                                            : make_uint4(0, 0, 0, 0);
                         xs[j] = make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
                                             __uint_as_float(v.w));
@@ -328,14 +337,19 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 4; ++j) q[j] = make_float4(0.f, 0.f, 0.f, 0.f);
                     }
-                    uint32_t n[4];
+                    uint32_t nr[4];
                     float part = 0.0f;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         part += (q[j].x + q[j].y) + (q[j].z + q[j].w);  // exact
-                        n[j] = pack4(__float2int_rn(q[j].x), __float2int_rn(q[j].y), __float2int_rn(q[j].z),
-                                     __float2int_rn(q[j].w));
+                        nr[j] = pack4(code_bits(q[j].x), code_bits(q[j].y), code_bits(q[j].z), code_bits(q[j].w));
                     }
+                    // back to k order: n[k] = nr[(k - rot) % 4], a rotation by rot in two select steps
+                    uint32_t h[4], n[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) h[k] = (rot & 1) ? nr[(k + 3) & 3] : nr[k];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) n[k] = (rot & 2) ? h[(k + 2) & 3] : h[k];
                     if (on) *reinterpret_cast<uint4*>(plane_addr(m, b, p)) = plane_of(n[0], n[1], n[2], n[3]);
                     part += __shfl_xor_sync(0xffffffffu, part, 1);
                     part += __shfl_xor_sync(0xffffffffu, part, 2);

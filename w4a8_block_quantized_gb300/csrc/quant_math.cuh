@@ -32,8 +32,11 @@ __device__ __forceinline__ bool near_tie(float t) {
 // the integer is 0) and equals the distance of frac(|t|) from the nearer integer, so the
 // flag is the near_tie() test.  Away from the flagged values round-to-even and
 // round-half-away agree; the flagged ones are recomputed by the caller.
+// The rounding is done on the fp32 add pipe: for |t| <= 2^22, (t + 1.5 * 2^23) - 1.5 * 2^23
+// is t rounded to the nearest integer, ties to even (the sum's unit in the last place is 1
+// and the add rounds to nearest even), i.e. exactly rintf(t); |t| <= 127.5 here.
 __device__ __forceinline__ float rint_flag(float t, bool& tie) {
-    const float q = rintf(t);
+    const float q = __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f);
     tie |= fabsf(t - q) >= 0.5f - 0x1p-15f;
     return q;
 }
