@@ -41,6 +41,11 @@ __device__ __forceinline__ float rint_flag(float t, bool& tie) {
     return q;
 }
 
+// One code by the definition (IEEE division, round half away from zero), for the rare
+// elements next to a rounding boundary.  Out of line and scalar: the division's code is then
+// not repeated in every quantizing loop body.
+static __device__ __noinline__ float requant(float x, float s) { return roundf(__fdiv_rn(x, s)); }
+
 // Quantize one lane's V float4 of a row to float codes.  No clamp is applied: for finite
 // inputs |x| <= absmax and s = RN(absmax/127), so |x/s| <= 127 (1 + 2^-24) and no code can
 // exceed 127 in magnitude, exactly as the clamped definition gives.  The rare near-tie
@@ -58,10 +63,10 @@ __device__ __forceinline__ void quant_lane(const float4 (&x)[V], float4 (&q)[V],
     if (__any_sync(0xffffffffu, tie)) {
 #pragma unroll
         for (int i = 0; i < V; ++i) {
-            if (near_tie(x[i].x * r)) q[i].x = roundf(__fdiv_rn(x[i].x, s));
-            if (near_tie(x[i].y * r)) q[i].y = roundf(__fdiv_rn(x[i].y, s));
-            if (near_tie(x[i].z * r)) q[i].z = roundf(__fdiv_rn(x[i].z, s));
-            if (near_tie(x[i].w * r)) q[i].w = roundf(__fdiv_rn(x[i].w, s));
+            if (near_tie(x[i].x * r)) q[i].x = requant(x[i].x, s);
+            if (near_tie(x[i].y * r)) q[i].y = requant(x[i].y, s);
+            if (near_tie(x[i].z * r)) q[i].z = requant(x[i].z, s);
+            if (near_tie(x[i].w * r)) q[i].w = requant(x[i].w, s);
         }
     }
 }
