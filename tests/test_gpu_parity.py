@@ -554,3 +554,18 @@ def test_decode_repeated_launches_complete_and_identical(M, K, N, launches):
             assert torch.equal(y, y0), f"launch {i}"
     y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
     check_y(y0, y_ref, bound, f"decode {M}x{K}->{N}")
+
+
+@pytest.mark.parametrize("M,K,N,bias", [(4096, 64, 129, True), (4095, 64, 257, False), (4096, 1024, 1, True),
+                                        (4097, 64, 64, False), (9, 64, 1, True), (8, 16384, 7, False)])
+def test_form_boundaries(M, K, N, bias):
+    """Shapes at the routing boundaries: exactly 4096 tokens (the first 256-token-tile size)
+    and one below and above it, a single 64-block per tile (K = 64), one output column, 9
+    tokens (the smallest tensor-core call) and 8 tokens whose row does not fit the kernel's
+    own quantizer (separate pre-pass); every output against the oracle, fused = separate."""
+    d = synth.random_small(M, K, N, seed=5 * M + K + N, bias=bias)
+    y_fused, y_sep = _run_both(d)
+    y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
+    check_y(y_fused, y_ref, bound, f"boundary {M}x{K}->{N}")
+    assert torch.equal(y_fused, y_sep), "fused and separate calls differ"
+    assert B().sync_status() == 0
