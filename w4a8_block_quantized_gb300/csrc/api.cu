@@ -1,5 +1,5 @@
 // api.cu -- the C ABI declared in include/w4a8.h: argument validation, workspace
-// carving, tensor-map encoding and kernel launches.  Nothing here allocates memory.
+// carving, routing by shape and kernel launches.  Nothing here allocates memory.
 #include "../../include/w4a8.h"
 #include "w4a8_internal.h"
 
@@ -57,7 +57,7 @@ int check_shape(int64_t M, int64_t N, int64_t K) {
     if (M < 0 || N < 0) return W4A8_ERR_ARG;
     if (K <= 0 || K % kBlock != 0) return W4A8_ERR_SHAPE;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return W4A8_ERR_SHAPE;
-    // tensor-map coordinates and the weight-row byte stride stay within 32 bits
+    // the kernels' 32-bit row offsets (K/2 bytes per packed weight row) and row counts stay in range
     if (2 * K > kMaxDim || N > (int64_t(1) << 31)) return W4A8_ERR_SHAPE;
     // the GEMM counts its 64-blocks (output tiles x K/64) in 32 bits
     const int64_t tiles = ((M + kTileT - 1) / kTileT) * ((N + kTileW - 1) / kTileW);
