@@ -1,0 +1,42 @@
+"""bench.py pieces that need no GPU: the reference arm (the oracle timed on the host) prints
+one JSON line in the contract's shape, and the workload table holds what the docs state."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.mark.parametrize("workload,unit", [("c0", "TOPS"), ("d1", "tok/s")])
+def test_reference_arm_prints_one_contract_line(workload, unit):
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", workload, "--steps", "1",
+                        "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == unit and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
+    for key in ("metric", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "config", "dtype"):
+        assert key in d, key
+
+
+def test_workloads_match_the_documented_shapes():
+    sys.path.insert(0, ROOT)
+    from w4a8_block_quantized_gb300 import synth
+    shapes = {k: [(s.M, s.K, s.N) for s in synth.workload(k)[1]] for k in synth.WORKLOADS}
+    assert shapes["c0"] == [(128, 1024, 1024)]
+    assert shapes["c1"] == [(512, 1024, 3072)] and synth.workload("c1")[1][0].bias
+    assert shapes["c2"] == [(512, 2048, 6144), (512, 6144, 2048)]
+    assert shapes["c3"] == [(512, 2048, 2048), (512, 2048, 1024), (512, 2048, 1024), (512, 2048, 2048),
+                            (512, 2048, 6144), (512, 2048, 6144), (512, 6144, 2048)]
+    assert shapes["c4"] == [(8192, 4096, 14336), (8192, 14336, 4096)]
+    assert all(M == 1 for k in ("d1", "d3", "d4") for M, _, _ in shapes[k])
+    assert [(K, N) for _, K, N in shapes["d3"]] == [(K, N) for _, K, N in shapes["c3"]]
+    # the decode workloads' weights at 4.5 bits per weight
+    s = synth.workload("d4")[1][0]
+    assert synth.weight_bytes(s) == s.N * s.K // 2 + 4 * s.N * (s.K // 64)
