@@ -70,17 +70,20 @@ int w4a8_quant_pack(const float *x, int64_t M, int64_t K,
 /* Few-token (decode) form.  For M <= W4A8_DECODE_MAX_M, w4a8_linear and
  * w4a8_prefill_linear stream the packed weights once (wq, w_scale and w_zero as given:
  * 4.5 bits per weight) and form each block's exact integer product on the CUDA cores
- * (section 4's decode discussion: a decode step costs one read of the weights).  The
- * result obeys the same definition and tolerance as the tensor-core form; the fp32 sums
- * are taken in a different order, so the two forms need not agree bit for bit. */
+ * (section 4's decode discussion: a decode step costs one read of the weights).  This
+ * needs the tokens' staged codes to fit one CTA's shared memory next to two weight stages
+ * (M * K up to about 180 000); deeper rows take the tensor-core form.  The result obeys the
+ * same definition and tolerance as the tensor-core form; the fp32 sums are taken in a
+ * different order, so the two forms need not agree bit for bit.  The *_workspace_bytes
+ * calls give the size each call needs, 0 where the few-token form needs none. */
 #define W4A8_DECODE_MAX_M 8
 
 /* Quantized linear from pre-quantized activations (section 3 eq. (2), section 4
  * steps 2-3): block-64 integer contraction on the tensor cores, then the scale /
  * zero-point / bias epilogue writing fp32 y [M][N] directly.
  * workspace: at least w4a8_linear_workspace_bytes(M, N, K) bytes (the activation
- * operand re-encoded for the tensor cores).  For M <= W4A8_DECODE_MAX_M that size is 0
- * and `workspace` may be NULL. */
+ * operand re-encoded for the tensor cores).  In the few-token form that size is 0 and
+ * `workspace` may be NULL. */
 int w4a8_linear(const int8_t *a_q, const float *a_scale, const int32_t *rowsum,
                 const uint8_t *wq, const uint16_t *w_scale, const uint16_t *w_zero,
                 const float *bias, float *y, int64_t M, int64_t N, int64_t K,

@@ -126,3 +126,11 @@ def test_tape_arguments_rejected(lib):
     assert lib.w4a8_tape_end(ctypes.c_void_p(1 << 20), None) == b.W4A8_ERR_ARG
     assert lib.w4a8_tape_replay(None, None) == b.W4A8_ERR_ARG
     lib.w4a8_tape_free(None)                                      # a no-op
+
+
+def test_deep_few_token_rows_take_the_tensor_core_form(lib):
+    """Eight tokens of K = 32768 do not fit the few-token kernel's shared memory: the linear
+    then needs the tensor-core form's workspace; K = 16384 still fits."""
+    assert lib.w4a8_linear_workspace_bytes(8, 256, 16384) == 0
+    assert lib.w4a8_linear_workspace_bytes(8, 256, 32768) > 0
+    assert lib.w4a8_linear_workspace_bytes(1, 256, 32768) == 0
