@@ -134,3 +134,52 @@ def test_deep_few_token_rows_take_the_tensor_core_form(lib):
     assert lib.w4a8_linear_workspace_bytes(8, 256, 16384) == 0
     assert lib.w4a8_linear_workspace_bytes(8, 256, 32768) > 0
     assert lib.w4a8_linear_workspace_bytes(1, 256, 32768) == 0
+
+
+class _named:
+    """Adds the call's name to an assertion raised inside the block."""
+
+    def __init__(self, name):
+        self.name = name
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, et, e, tb):
+        if et is AssertionError:
+            raise AssertionError(f"{self.name}: {e}") from e
+        return False
+
+
+def test_binding_rejects_host_tensors_before_the_library():
+    """No binding call hands a host address to the library: a CPU tensor anywhere in the
+    argument list raises TypeError in the binding, before any entry point runs."""
+    import torch
+    from w4a8_block_quantized_gb300 import binding as b
+
+    M, N, K = 4, 8, 64
+    x = torch.zeros((M, K))
+    a_q = torch.zeros((M, K), dtype=torch.int8)
+    s_a = torch.zeros(M)
+    rs = torch.zeros((M, 1), dtype=torch.int32)
+    wq = torch.zeros((N, K // 2), dtype=torch.uint8)
+    sw = torch.zeros((N, 1), dtype=torch.float16)
+    buf = torch.zeros(1 << 16, dtype=torch.uint8)
+    calls = {
+        "quant_pack": lambda: b.quant_pack(x),
+        "linear": lambda: b.linear(a_q, s_a, rs, wq, sw, sw),
+        "linear_ex": lambda: b.linear_ex(a_q, s_a, rs, wq, sw, sw),
+        "prefill_linear": lambda: b.prefill_linear(x, wq, sw, sw),
+        "prefill_linear_ex": lambda: b.prefill_linear_ex(x, wq, sw, sw),
+        "prefill_linear_noalloc": lambda: b.prefill_linear_noalloc(x, wq, sw, sw),
+        "prepare_activations": lambda: b.prepare_activations(x),
+        "prepare_weights": lambda: b.prepare_weights(wq, sw, sw),
+        "linear_prepared": lambda: b.linear_prepared(buf, buf, M, N, K),
+        "linear_prepared_ex": lambda: b.linear_prepared_ex(buf, buf, M, N, K),
+        "debug_block_acc": lambda: b.debug_block_acc(a_q, wq, N),
+    }
+    for name, call in calls.items():
+        with pytest.raises(TypeError, match="CUDA tensor"), _named(name):
+            call()
+    with pytest.raises(TypeError, match="torch.Tensor"):
+        b._arg(object(), None, None, "y")

@@ -444,6 +444,48 @@ def test_epilogue_argument_checks():
     assert b.sync_status() == 0
 
 
+
+def test_binding_checks_every_tensor_before_launch():
+    """The binding checks each tensor's device, dtype, shape and (for the opaque prepared
+    buffers, which the C call receives without a length) size, so a mismatched argument
+    raises in Python and nothing is launched."""
+    b = B()
+    M, N, K = 4, 8, 128
+    d = synth.random_small(M, K, N, seed=2, bias=True)
+    g = inputs_to_dev(d)
+    x, wq, sw, zw, bias = g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"]
+    bad = {
+        "y shape": lambda: b.prefill_linear(x, wq, sw, zw, bias, y=torch.empty((M, N + 1), device=dev())),
+        "y dtype": lambda: b.prefill_linear(x, wq, sw, zw, bias, y=torch.empty((M, N), device=dev(),
+                                                                             dtype=torch.float16)),
+        "y on host": lambda: b.prefill_linear(x, wq, sw, zw, bias, y=torch.empty((M, N))),
+        "bias on host": lambda: b.prefill_linear(x, wq, sw, zw, bias.cpu()),
+        "bias length": lambda: b.prefill_linear(x, wq, sw, zw, bias[:N - 1]),
+        "scale shape": lambda: b.prefill_linear(x, wq, sw[:, :1].contiguous(), zw, bias),
+        "zero dtype": lambda: b.prefill_linear(x, wq, sw, zw.float(), bias),
+        "wq depth": lambda: b.prefill_linear(x[:, :64].contiguous(), wq, sw, zw, bias),
+        "strided x": lambda: b.prefill_linear(torch.empty((M, 2 * K), device=dev())[:, :K], wq, sw, zw, bias),
+        "ws on host": lambda: b.linear(*b.quant_pack(x), wq, sw, zw, bias, ws=torch.empty(1 << 20,
+                                                                                         dtype=torch.uint8)),
+        "rowsum shape": lambda: b.linear(b.quant_pack(x)[0], b.quant_pack(x)[1],
+                                         torch.zeros((M, 1), dtype=torch.int32, device=dev()), wq, sw, zw),
+        "act too small": lambda: b.linear_prepared(torch.empty(64, dtype=torch.uint8, device=dev()),
+                                                   b.prepare_weights(wq, sw, zw), M, N, K),
+        "pw too small": lambda: b.linear_prepared_ex(b.prepare_activations(x),
+                                                     torch.empty(64, dtype=torch.uint8, device=dev()), M, N, K),
+        "debug wq rows": lambda: b.debug_block_acc(b.quant_pack(x)[0], wq, N + 1),
+        "debug window": lambda: b.debug_block_acc(b.quant_pack(x)[0], wq, N, m0=2, m_cnt=3),
+    }
+    y = torch.zeros((M, N), device=dev())
+    for what, call in bad.items():
+        with pytest.raises((TypeError, ValueError)):
+            call()
+    b.prefill_linear(x, wq, sw, zw, bias, y=y)
+    y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
+    check_y(y, y_ref, bound, "after rejected calls")
+    assert b.sync_status() == 0
+
+
 # ------------------------------------------------------------------ command tapes
 def test_tape_replays_a_mixed_sequence():
     """A tape recording the fused call at three forms (128-token, 256-token, few-token), the

@@ -107,13 +107,51 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _want(t: torch.Tensor, dtype, name: str):
+def _arg(t, dtype, shape, name: str, device=None, min_bytes=None):
+    """Check one tensor argument before its address reaches the library, which cannot: a CUDA
+    tensor on the call's device, contiguous, of the dtype and shape the C layout fixes (or, for
+    an opaque buffer, at least ``min_bytes`` long).  ``None`` passes (optional arguments)."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
     if not t.is_cuda:
-        raise TypeError(f"{name} must be a CUDA tensor (the library has no CPU path)")
-    if t.dtype != dtype:
+        raise TypeError(f"{name} must be a CUDA tensor (the library has no CPU path), got {t.device}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the call's other tensors on {device}")
+    if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if min_bytes is not None and _nbytes(t) < min_bytes:
+        raise ValueError(f"{name} holds {_nbytes(t)} bytes, the call needs {min_bytes}")
+
+
+def _want(t: torch.Tensor, dtype, name: str):
+    _arg(t, dtype, None, name)
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device} but the current CUDA device is "
+                         f"{torch.cuda.current_device()} (the library runs on the current device)")
+
+
+def _nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()
+
+
+def _weights(wq, w_scale, w_zero, N: int, K: int, device):
+    _arg(wq, torch.uint8, (N, K // 2), "wq", device)
+    _arg(w_scale, torch.float16, (N, K // 64), "w_scale", device)
+    _arg(w_zero, torch.float16, (N, K // 64), "w_zero", device)
+
+
+def _ws(ws, need: int, device):
+    """The caller's workspace (any dtype: its size in bytes is what the library is told)."""
+    if ws is None:
+        return workspace(need, device)
+    _arg(ws, None, None, "ws", device)
+    return ws
 
 
 def linear_workspace_bytes(M: int, N: int, K: int) -> int:
@@ -128,9 +166,15 @@ def debug_workspace_bytes(m_cnt: int, n_cnt: int, K: int) -> int:
     return int(load().w4a8_debug_workspace_bytes(m_cnt, n_cnt, K))
 
 
+_SIZE_REJECTED = (1 << 64) - 1   # what a size query returns for a shape the library rejects
+
+
 def workspace(nbytes: int, device) -> torch.Tensor:
-    """A caller-owned workspace buffer (uint8, at least 16-byte aligned)."""
-    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+    """A caller-owned workspace buffer (uint8, at least 16-byte aligned).  For a rejected
+    shape (size query = SIZE_MAX) a minimal buffer stands in: every call checks the shape
+    before the workspace, so it then returns W4A8_ERR_SHAPE."""
+    n = 16 if int(nbytes) == _SIZE_REJECTED else max(int(nbytes), 16)
+    return torch.empty(n, dtype=torch.uint8, device=device)
 
 
 def quant_pack(x: torch.Tensor, a_q=None, a_scale=None, rowsum=None, stream=None):
@@ -141,39 +185,66 @@ def quant_pack(x: torch.Tensor, a_q=None, a_scale=None, rowsum=None, stream=None
     a_q = torch.empty((M, K), dtype=torch.int8, device=dev) if a_q is None else a_q
     a_scale = torch.empty((M,), dtype=torch.float32, device=dev) if a_scale is None else a_scale
     rowsum = torch.empty((M, K // 64), dtype=torch.int32, device=dev) if rowsum is None else rowsum
+    _arg(a_q, torch.int8, (M, K), "a_q", dev)
+    _arg(a_scale, torch.float32, (M,), "a_scale", dev)
+    _arg(rowsum, torch.int32, (M, K // 64), "rowsum", dev)
     rc = load().w4a8_quant_pack(_ptr(x), M, K, _ptr(a_q), _ptr(a_scale), _ptr(rowsum), _stream(stream))
     _check(rc, "w4a8_quant_pack")
     return a_q, a_scale, rowsum
 
 
+def _quantized(a_q, a_scale, rowsum):
+    """Shape (M, K) of a pre-quantized activation triple, after checking all three."""
+    _want(a_q, torch.int8, "a_q")
+    M, K = a_q.shape
+    _arg(a_scale, torch.float32, (M,), "a_scale", a_q.device)
+    _arg(rowsum, torch.int32, (M, K // 64), "rowsum", a_q.device)
+    return M, K
+
+
 def linear(a_q, a_scale, rowsum, wq, w_scale, w_zero, bias=None, y=None, ws=None, stream=None):
     """w4a8_linear: pre-quantized activations -> y fp32 [M,N]."""
-    _want(a_q, torch.int8, "a_q")
-    _want(wq, torch.uint8, "wq")
-    _want(w_scale, torch.float16, "w_scale")
-    _want(w_zero, torch.float16, "w_zero")
-    M, K = a_q.shape
-    N = wq.shape[0]
-    y = torch.empty((M, N), dtype=torch.float32, device=a_q.device) if y is None else y
-    if ws is None:
-        ws = workspace(linear_workspace_bytes(M, N, K), a_q.device)
+    M, K = _quantized(a_q, a_scale, rowsum)
+    dev = a_q.device
+    N = _rows(wq)
+    _weights(wq, w_scale, w_zero, N, K, dev)
+    _arg(bias, torch.float32, (N,), "bias", dev)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev) if y is None else y
+    _arg(y, torch.float32, (M, N), "y", dev)
+    ws = _ws(ws, linear_workspace_bytes(M, N, K), dev)
     rc = load().w4a8_linear(_ptr(a_q), _ptr(a_scale), _ptr(rowsum), _ptr(wq), _ptr(w_scale), _ptr(w_zero),
-                            _ptr(bias), _ptr(y), M, N, K, _ptr(ws), ws.numel(), _stream(stream))
+                            _ptr(bias), _ptr(y), M, N, K, _ptr(ws), _nbytes(ws), _stream(stream))
     _check(rc, "w4a8_linear")
     return y
 
 
+def _rows(wq) -> int:
+    _want(wq, torch.uint8, "wq")
+    if wq.dim() != 2:
+        raise ValueError(f"wq must be 2-D [N, K/2], got shape {tuple(wq.shape)}")
+    return wq.shape[0]
+
+
+def _prefill_args(x, wq, w_scale, w_zero, bias):
+    """Shape (M, N, K) of a fused call, after checking x, the weights and the bias."""
+    _want(x, torch.float32, "x")
+    if x.dim() != 2:
+        raise ValueError(f"x must be 2-D [M, K], got shape {tuple(x.shape)}")
+    M, K = x.shape
+    N = _rows(wq)
+    _weights(wq, w_scale, w_zero, N, K, x.device)
+    _arg(bias, torch.float32, (N,), "bias", x.device)
+    return M, N, K
+
+
 def prefill_linear(x, wq, w_scale, w_zero, bias=None, y=None, ws=None, stream=None):
     """w4a8_prefill_linear: fp32 x [M,K] -> y fp32 [M,N] (pre-pass + linear)."""
-    _want(x, torch.float32, "x")
-    _want(wq, torch.uint8, "wq")
-    M, K = x.shape
-    N = wq.shape[0]
+    M, N, K = _prefill_args(x, wq, w_scale, w_zero, bias)
     y = torch.empty((M, N), dtype=torch.float32, device=x.device) if y is None else y
-    if ws is None:
-        ws = workspace(prefill_workspace_bytes(M, N, K), x.device)
+    _arg(y, torch.float32, (M, N), "y", x.device)
+    ws = _ws(ws, prefill_workspace_bytes(M, N, K), x.device)
     rc = load().w4a8_prefill_linear(_ptr(x), _ptr(wq), _ptr(w_scale), _ptr(w_zero), _ptr(bias), _ptr(y),
-                                    M, N, K, _ptr(ws), ws.numel(), _stream(stream))
+                                    M, N, K, _ptr(ws), _nbytes(ws), _stream(stream))
     _check(rc, "w4a8_prefill_linear")
     return y
 
@@ -181,11 +252,9 @@ def prefill_linear(x, wq, w_scale, w_zero, bias=None, y=None, ws=None, stream=No
 def prefill_linear_noalloc(x, wq, w_scale, w_zero, bias=None, y=None, stream=None):
     """w4a8_prefill_linear_noalloc: the fused call on the library's static scratch buffer,
     for callers that cannot allocate device memory.  Serialize calls that could overlap."""
-    _want(x, torch.float32, "x")
-    _want(wq, torch.uint8, "wq")
-    M, K = x.shape
-    N = wq.shape[0]
+    M, N, K = _prefill_args(x, wq, w_scale, w_zero, bias)
     y = torch.empty((M, N), dtype=torch.float32, device=x.device) if y is None else y
+    _arg(y, torch.float32, (M, N), "y", x.device)
     rc = load().w4a8_prefill_linear_noalloc(_ptr(x), _ptr(wq), _ptr(w_scale), _ptr(w_zero), _ptr(bias), _ptr(y),
                                             M, N, K, _stream(stream))
     _check(rc, "w4a8_prefill_linear_noalloc")
@@ -205,7 +274,8 @@ def prepare_activations(x, act=None, stream=None):
     _want(x, torch.float32, "x")
     M, K = x.shape
     act = workspace(prepared_activations_bytes(M, K), x.device) if act is None else act
-    rc = load().w4a8_prepare_activations(_ptr(x), M, K, _ptr(act), act.numel(), _stream(stream))
+    _arg(act, None, None, "act", x.device)
+    rc = load().w4a8_prepare_activations(_ptr(x), M, K, _ptr(act), _nbytes(act), _stream(stream))
     _check(rc, "w4a8_prepare_activations")
     return act
 
@@ -213,12 +283,12 @@ def prepare_activations(x, act=None, stream=None):
 def prepare_weights(wq, w_scale, w_zero, pw=None, stream=None):
     """w4a8_prepare_weights: the tensor-core weight operand and the scale / zero layout
     (an opaque buffer, returned)."""
-    _want(wq, torch.uint8, "wq")
-    _want(w_scale, torch.float16, "w_scale")
-    _want(w_zero, torch.float16, "w_zero")
-    N, K = wq.shape[0], 2 * wq.shape[1]
+    N = _rows(wq)
+    K = 2 * wq.shape[1]
+    _weights(wq, w_scale, w_zero, N, K, wq.device)
     pw = workspace(prepared_weights_bytes(N, K), wq.device) if pw is None else pw
-    rc = load().w4a8_prepare_weights(_ptr(wq), _ptr(w_scale), _ptr(w_zero), N, K, _ptr(pw), pw.numel(),
+    _arg(pw, None, None, "pw", wq.device)
+    rc = load().w4a8_prepare_weights(_ptr(wq), _ptr(w_scale), _ptr(w_zero), N, K, _ptr(pw), _nbytes(pw),
                                      _stream(stream))
     _check(rc, "w4a8_prepare_weights")
     return pw
@@ -229,23 +299,18 @@ def _out(y, shape, device, out_dtype):
     if dt not in _OUT_DTYPES:
         raise TypeError(f"y: unsupported output dtype {dt}")
     y = torch.empty(shape, dtype=dt, device=device) if y is None else y
-    if y.dtype != dt or not y.is_contiguous() or tuple(y.shape) != tuple(shape):
-        raise ValueError(f"y: want a contiguous {dt} tensor of shape {tuple(shape)}")
+    _arg(y, dt, shape, "y", device)
     return y, _OUT_DTYPES[dt]
 
 
 def prefill_linear_ex(x, wq, w_scale, w_zero, bias=None, y=None, out_dtype=None, clamp=(-math.inf, math.inf),
                       ws=None, stream=None):
     """w4a8_prefill_linear_ex: the fused call with the epilogue clamp and an fp32 or bf16 y."""
-    _want(x, torch.float32, "x")
-    _want(wq, torch.uint8, "wq")
-    M, K = x.shape
-    N = wq.shape[0]
+    M, N, K = _prefill_args(x, wq, w_scale, w_zero, bias)
     y, code = _out(y, (M, N), x.device, out_dtype if y is None else y.dtype)
-    if ws is None:
-        ws = workspace(prefill_workspace_bytes(M, N, K), x.device)
+    ws = _ws(ws, prefill_workspace_bytes(M, N, K), x.device)
     rc = load().w4a8_prefill_linear_ex(_ptr(x), _ptr(wq), _ptr(w_scale), _ptr(w_zero), _ptr(bias), _ptr(y), code,
-                                       float(clamp[0]), float(clamp[1]), M, N, K, _ptr(ws), ws.numel(),
+                                       float(clamp[0]), float(clamp[1]), M, N, K, _ptr(ws), _nbytes(ws),
                                        _stream(stream))
     _check(rc, "w4a8_prefill_linear_ex")
     return y
@@ -254,24 +319,41 @@ def prefill_linear_ex(x, wq, w_scale, w_zero, bias=None, y=None, out_dtype=None,
 def linear_ex(a_q, a_scale, rowsum, wq, w_scale, w_zero, bias=None, y=None, out_dtype=None,
               clamp=(-math.inf, math.inf), ws=None, stream=None):
     """w4a8_linear_ex: pre-quantized activations, epilogue clamp, fp32 or bf16 y."""
-    _want(a_q, torch.int8, "a_q")
-    _want(wq, torch.uint8, "wq")
-    M, K = a_q.shape
-    N = wq.shape[0]
-    y, code = _out(y, (M, N), a_q.device, out_dtype if y is None else y.dtype)
-    if ws is None:
-        ws = workspace(linear_workspace_bytes(M, N, K), a_q.device)
+    M, K = _quantized(a_q, a_scale, rowsum)
+    dev = a_q.device
+    N = _rows(wq)
+    _weights(wq, w_scale, w_zero, N, K, dev)
+    _arg(bias, torch.float32, (N,), "bias", dev)
+    y, code = _out(y, (M, N), dev, out_dtype if y is None else y.dtype)
+    ws = _ws(ws, linear_workspace_bytes(M, N, K), dev)
     rc = load().w4a8_linear_ex(_ptr(a_q), _ptr(a_scale), _ptr(rowsum), _ptr(wq), _ptr(w_scale), _ptr(w_zero),
                                _ptr(bias), _ptr(y), code, float(clamp[0]), float(clamp[1]), M, N, K, _ptr(ws),
-                               ws.numel(), _stream(stream))
+                               _nbytes(ws), _stream(stream))
     _check(rc, "w4a8_linear_ex")
     return y
+
+
+def _prepared(act, pw, bias, M: int, N: int, K: int):
+    """Check the opaque operands of a prepared call against the sizes the library derives
+    from (M, N, K): the C call takes no buffer lengths, so this is the only check."""
+    _want(act, None, "act")
+    dev = act.device
+    if min(M, N, K) < 0:
+        raise ValueError(f"negative size in (M, N, K) = {(M, N, K)}")
+    if M and N and K > 0 and K % 64 == 0:
+        _arg(act, None, None, "act", dev, min_bytes=prepared_activations_bytes(M, K))
+        _arg(pw, None, None, "pw", dev, min_bytes=prepared_weights_bytes(N, K))
+    else:
+        _arg(pw, None, None, "pw", dev)
+    _arg(bias, torch.float32, (N,), "bias", dev)
+    return dev
 
 
 def linear_prepared_ex(act, pw, M: int, N: int, K: int, bias=None, y=None, out_dtype=None,
                        clamp=(-math.inf, math.inf), stream=None):
     """w4a8_linear_prepared_ex: prepared operands, epilogue clamp, fp32 or bf16 y."""
-    y, code = _out(y, (M, N), act.device, out_dtype if y is None else y.dtype)
+    dev = _prepared(act, pw, bias, M, N, K)
+    y, code = _out(y, (M, N), dev, out_dtype if y is None else y.dtype)
     rc = load().w4a8_linear_prepared_ex(_ptr(act), _ptr(pw), _ptr(bias), _ptr(y), code, float(clamp[0]),
                                         float(clamp[1]), M, N, K, _stream(stream))
     _check(rc, "w4a8_linear_prepared_ex")
@@ -280,7 +362,9 @@ def linear_prepared_ex(act, pw, M: int, N: int, K: int, bias=None, y=None, out_d
 
 def linear_prepared(act, pw, M: int, N: int, K: int, bias=None, y=None, stream=None):
     """w4a8_linear_prepared: contraction + epilogue from prepared operands -> y fp32 [M,N]."""
-    y = torch.empty((M, N), dtype=torch.float32, device=act.device) if y is None else y
+    dev = _prepared(act, pw, bias, M, N, K)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev) if y is None else y
+    _arg(y, torch.float32, (M, N), "y", dev)
     rc = load().w4a8_linear_prepared(_ptr(act), _ptr(pw), _ptr(bias), _ptr(y), M, N, K, _stream(stream))
     _check(rc, "w4a8_linear_prepared")
     return y
@@ -290,13 +374,15 @@ def debug_block_acc(a_q, wq, N, m0=0, m_cnt=None, n0=0, n_cnt=None, ws=None, str
     """w4a8_debug_block_acc: exact per-block int32 accumulators [m_cnt, n_cnt, K/64]."""
     _want(a_q, torch.int8, "a_q")
     M, K = a_q.shape
+    _arg(wq, torch.uint8, (N, K // 2), "wq", a_q.device)
     m_cnt = M - m0 if m_cnt is None else m_cnt
     n_cnt = N - n0 if n_cnt is None else n_cnt
+    if not (0 <= m0 and 0 <= m_cnt and m0 + m_cnt <= M and 0 <= n0 and 0 <= n_cnt and n0 + n_cnt <= N):
+        raise ValueError(f"window rows [{m0}, {m0}+{m_cnt}) x cols [{n0}, {n0}+{n_cnt}) outside [{M}] x [{N}]")
     acc = torch.empty((m_cnt, n_cnt, K // 64), dtype=torch.int32, device=a_q.device)
-    if ws is None:
-        ws = workspace(debug_workspace_bytes(m_cnt, n_cnt, K), a_q.device)
+    ws = _ws(ws, debug_workspace_bytes(m_cnt, n_cnt, K), a_q.device)
     rc = load().w4a8_debug_block_acc(_ptr(a_q), _ptr(wq), M, N, K, m0, m_cnt, n0, n_cnt, _ptr(acc),
-                                     _ptr(ws), ws.numel(), _stream(stream))
+                                     _ptr(ws), _nbytes(ws), _stream(stream))
     _check(rc, "w4a8_debug_block_acc")
     return acc
 
