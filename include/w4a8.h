@@ -22,9 +22,10 @@
  *   y       fp32  [M][N]
  *
  * Conventions for every call below:
- *   - Every array pointer is a DEVICE pointer owned by the caller; the library never
- *     allocates, frees or retains memory (command tapes, below, are the one exception).
- *     Scratch comes from the caller's `workspace`.
+ *   - Every array pointer is a DEVICE pointer owned by the caller (w4a8_prefill_linear_host,
+ *     below, takes x and y in host memory); the library never allocates, frees or retains
+ *     memory (command tapes, and the streams and events the host-buffer call keeps, below,
+ *     are the exceptions).  Scratch comes from the caller's `workspace`.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
  *     asynchronous: W4A8_OK means the work was validated and enqueued.
  *   - Shapes: K must be a positive multiple of 64; M >= 0 and N >= 0 (M == 0 or
@@ -171,6 +172,29 @@ int w4a8_linear_prepared_ex(const void *act, const void *pw, const float *bias, 
 int w4a8_prefill_linear_noalloc(const float *x, const uint8_t *wq, const uint16_t *w_scale,
                                 const uint16_t *w_zero, const float *bias, float *y,
                                 int64_t M, int64_t N, int64_t K, void *stream);
+
+/* w4a8_prefill_linear with x and y in HOST memory (no counterpart in the paper; it carries
+ * the copies an application makes around the fused call, section 3 eq. (1)-(2), and hides
+ * them behind the computation).  x_host: fp32 [M][K], y_host: fp32 [M][N], both page-locked
+ * (cudaHostAlloc / cudaHostRegister; any other pointer gives W4A8_ERR_ARG); the weights,
+ * bias and workspace are device memory as elsewhere.  workspace: at least
+ * w4a8_prefill_host_workspace_bytes(M, N, K) bytes, 16-byte aligned (it holds the device
+ * copies of x and y and the pre-pass scratch).
+ *   - The rows are cut into up to four chunks (none below 128 rows, none below 4096 rows
+ *     once M reaches 4096; few-token and short calls are one chunk).  Chunk c+1's copy to
+ *     the device, chunk c's linear and chunk c-1's copy back overlap, on streams the library
+ *     creates on a device's first chunked call and keeps until the process exits.
+ *   - Stream-ordered like every call: the work starts after what was enqueued on `stream`
+ *     before it, and what is enqueued after it sees y_host complete.  The host buffers must
+ *     stay valid and x_host unchanged until then.  Calls sharing a workspace must be
+ *     ordered (one stream).  It may be recorded into a tape (make one call of the shape
+ *     first).
+ *   - Results are bit-identical to w4a8_prefill_linear on the same inputs. */
+size_t w4a8_prefill_host_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int w4a8_prefill_linear_host(const float *x_host, const uint8_t *wq, const uint16_t *w_scale,
+                             const uint16_t *w_zero, const float *bias, float *y_host,
+                             int64_t M, int64_t N, int64_t K, void *workspace,
+                             size_t workspace_bytes, void *stream);
 
 /* Workspace sizes in bytes (0 for an empty problem; (size_t)-1 for invalid shapes). */
 size_t w4a8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);

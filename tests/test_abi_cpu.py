@@ -44,7 +44,7 @@ def test_status_strings(lib):
         s = b.status_string(code)
         assert s and s != "unknown status"
     assert b.status_string(12345) == "unknown status"
-    assert lib.w4a8_abi_version() == 202
+    assert lib.w4a8_abi_version() == 203
 
 
 def test_shape_checks_need_no_gpu(lib):
@@ -183,3 +183,75 @@ def test_binding_rejects_host_tensors_before_the_library():
             call()
     with pytest.raises(TypeError, match="torch.Tensor"):
         b._arg(object(), None, None, "y")
+
+
+def _align(v):
+    return (v + 255) & ~255
+
+
+def test_host_call_workspace_and_chunking(lib):
+    """The host-buffer call's workspace: the device copies of x and y, then either the fused
+    call's scratch (one chunk) or the prepared weights and one prepared-activation buffer per
+    compute stream (at most four), sized for the last, largest chunk.  A call is cut into at
+    most eight chunks of whole token tiles, each moving at least 8 MiB of x and y."""
+    def plan(M, N, K):
+        tw = 256 if M >= 4096 else 128
+        chunks = 1 if M <= 8 else max(1, min(8, M // tw, M * (K + N) * 4 // (8 << 20)))
+        rows = (M // chunks) // tw * tw if chunks > 1 else M
+        return chunks, M - (chunks - 1) * rows
+
+    def base(M, N, K):
+        return _align(_align(M * K * 4) + M * N * 4)
+
+    cases = [  # (M, N, K, chunks, rows of the last chunk)
+        (512, 3072, 1024, 1, 512),        # the pp512 linear: 8 MiB in all, one chunk
+        (700, 200, 256, 1, 700),
+        (3, 256, 1024, 1, 3),
+        (1500, 2560, 1024, 2, 860),
+        (2048, 4096, 1024, 5, 512),
+        (1000, 8192, 1024, 4, 616),
+        (2048, 4096, 2048, 6, 768),
+    ]
+    for M, N, K, chunks, last in cases:
+        assert plan(M, N, K) == (chunks, last), (M, N, K)
+        got = lib.w4a8_prefill_host_workspace_bytes(M, N, K)
+        if chunks == 1:
+            want = base(M, N, K) + lib.w4a8_prefill_workspace_bytes(M, N, K)
+        else:
+            want = base(M, N, K) + lib.w4a8_prepared_weights_bytes(N, K) + \
+                min(chunks, 4) * lib.w4a8_prepared_activations_bytes(last, K)
+        assert got == want, (M, N, K)
+    # 256-token records: chunks of whole 256-row tiles, below 4096 rows each
+    for M, N, K in ((8192, 14336, 4096), (8300, 512, 256), (9000, 1536, 512)):
+        chunks, last = plan(M, N, K)
+        assert chunks > 1 and last < 4096
+        got = lib.w4a8_prefill_host_workspace_bytes(M, N, K)
+        assert got >= base(M, N, K) + lib.w4a8_prepared_weights_bytes(N, K) + min(chunks, 4) * (last * K * 2)
+    assert lib.w4a8_prefill_host_workspace_bytes(0, 64, 128) == 0
+    assert lib.w4a8_prefill_host_workspace_bytes(4, 64, 100) == ctypes.c_size_t(-1).value
+
+
+def test_host_call_arguments_rejected_before_launch(lib):
+    from w4a8_block_quantized_gb300 import binding as b
+    P = ctypes.c_void_p
+    d = P(1 << 20)
+    M, N, K = 512, 64, 128
+    need = lib.w4a8_prefill_host_workspace_bytes(M, N, K)
+    assert lib.w4a8_prefill_linear_host(d, d, d, d, None, d, M, N, 96, d, need, None) == b.W4A8_ERR_SHAPE
+    assert lib.w4a8_prefill_linear_host(None, d, d, d, None, d, M, N, K, d, need, None) == b.W4A8_ERR_ARG
+    assert lib.w4a8_prefill_linear_host(d, d, d, d, None, None, M, N, K, d, need, None) == b.W4A8_ERR_ARG
+    assert lib.w4a8_prefill_linear_host(d, d, d, d, None, d, M, N, K, None, need, None) == b.W4A8_ERR_ARG
+    assert lib.w4a8_prefill_linear_host(d, d, d, d, None, d, M, N, K, P((1 << 20) + 8), need, None) == \
+        b.W4A8_ERR_ALIGN
+    assert lib.w4a8_prefill_linear_host(d, d, d, d, None, d, M, N, K, d, need - 1, None) == b.W4A8_ERR_WORKSPACE
+    assert lib.w4a8_prefill_linear_host(None, None, None, None, None, None, 0, N, K, None, 0, None) == b.W4A8_OK
+
+
+def test_binding_host_call_wants_page_locked_buffers():
+    import torch
+    from w4a8_block_quantized_gb300 import binding as b
+    x = torch.zeros((4, 64))
+    wq = torch.zeros((8, 32), dtype=torch.uint8)
+    sw = torch.zeros((8, 1), dtype=torch.float16)
+    with pytest.raises(TypeError, match="page-locked"):
+        b.prefill_linear_host(x, wq, sw, sw)

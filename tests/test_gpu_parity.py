@@ -486,6 +486,104 @@ def test_binding_checks_every_tensor_before_launch():
     assert b.sync_status() == 0
 
 
+
+# ------------------------------------------------------------------ host-buffer call
+def _pinned(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+
+
+@pytest.mark.parametrize("M,K,N", [(1500, 1024, 2560), (2048, 2048, 4096), (8300, 512, 256), (9000, 512, 1536),
+                                   (512, 1024, 640), (3, 1024, 256)])
+def test_host_call_equals_fused(M, K, N):
+    """x and y in page-locked host memory, chunked copies overlapping the computation: the
+    outputs equal the device-buffer fused call's bit for bit -- two chunks with a ragged
+    last one; six chunks over four compute streams (streams and activation buffers reused);
+    chunks of whole 256-row tiles below 4096 rows each through the 256-token kernel; the
+    full eight chunks; one chunk; the few-token form -- and lie within tolerance of the
+    oracle."""
+    b = B()
+    d = synth.random_small(M, K, N, seed=70 + M + N, bias=True)
+    g = inputs_to_dev(d)
+    xh = _pinned(d["x"])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y_dev = b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"], stream=s)
+        yh = b.prefill_linear_host(xh, g["wq"], g["s_w"], g["z_w"], g["bias"], stream=s)
+    s.synchronize()
+    assert torch.equal(yh, y_dev.cpu())
+    rows = np.unique(np.linspace(0, M - 1, min(M, 64)).astype(np.int64))
+    y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"], rows=rows)
+    check_y(yh[rows], y_ref, bound, f"host call {M}x{K}->{N}")
+    assert b.sync_status() == 0
+
+
+def test_host_call_reuses_a_workspace_in_stream_order():
+    """Three calls on one stream through one workspace, each with its own host x and y: the
+    later calls' copies in wait for the earlier calls to finish, so every y is its own x's."""
+    b = B()
+    M, K, N = 1024, 2048, 2048
+    ds = [synth.random_small(M, K, N, seed=90 + i, bias=i == 1) for i in range(3)]
+    ws = b.workspace(b.prefill_host_workspace_bytes(M, N, K), dev())
+    s = torch.cuda.Stream()
+    outs = []
+    for d in ds:
+        gw = inputs_to_dev(d)
+        xh = _pinned(d["x"])   # held until the stream is synchronized: torch cannot see the library's copies
+        outs.append((d, gw, xh, b.prefill_linear_host(xh, gw["wq"], gw["s_w"], gw["z_w"], gw["bias"], ws=ws,
+                                                       stream=s)))
+    s.synchronize()
+    for d, gw, _, yh in outs:
+        ref = b.prefill_linear(to_dev(d["x"]), gw["wq"], gw["s_w"], gw["z_w"], gw["bias"])
+        assert torch.equal(yh, ref.cpu())
+    assert b.sync_status() == 0
+
+
+def test_tape_records_the_host_call():
+    """The host-buffer call recorded into a tape (its side streams joined back into the
+    capture) replays bit for bit, and follows new contents of the same host x."""
+    b = B()
+    M, K, N = 2048, 1024, 2048
+    d = synth.random_small(M, K, N, seed=95, bias=True)
+    g = inputs_to_dev(d)
+    xh = _pinned(d["x"])
+    yh = torch.empty((M, N)).pin_memory()
+    ws = b.workspace(b.prefill_host_workspace_bytes(M, N, K), dev())
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b.prefill_linear_host(xh, g["wq"], g["s_w"], g["z_w"], g["bias"], y=yh, ws=ws, stream=s)
+        s.synchronize()
+        eager = yh.clone()
+        with b.Tape(s) as tape:
+            b.prefill_linear_host(xh, g["wq"], g["s_w"], g["z_w"], g["bias"], y=yh, ws=ws, stream=s)
+    yh.fill_(float("nan"))
+    tape.replay(s)
+    s.synchronize()
+    assert torch.equal(yh, eager)
+    xh.mul_(-0.5)
+    ref = b.prefill_linear(xh.to(dev()), g["wq"], g["s_w"], g["z_w"], g["bias"]).cpu()
+    tape.replay(s)
+    s.synchronize()
+    assert torch.equal(yh, ref)
+    tape.free()
+    assert b.sync_status() == 0
+
+
+def test_host_call_rejects_pageable_memory():
+    """A host pointer the driver does not know as page-locked is refused (nothing launched)."""
+    b = B()
+    M, K, N = 256, 128, 64
+    d = synth.random_small(M, K, N, seed=3, bias=False)
+    g = inputs_to_dev(d)
+    xp = torch.from_numpy(d["x"].copy())                  # pageable
+    yp = torch.empty((M, N))
+    ws = b.workspace(b.prefill_host_workspace_bytes(M, N, K), dev())
+    lib = b.load()
+    rc = lib.w4a8_prefill_linear_host(b._ptr(xp), b._ptr(g["wq"]), b._ptr(g["s_w"]), b._ptr(g["z_w"]), None,
+                                      b._ptr(yp), M, N, K, b._ptr(ws), ws.numel(), b._stream(None))
+    assert rc == b.W4A8_ERR_ARG
+    assert b.sync_status() == 0
+
+
 # ------------------------------------------------------------------ command tapes
 def test_tape_replays_a_mixed_sequence():
     """A tape recording the fused call at three forms (128-token, 256-token, few-token), the

@@ -47,6 +47,8 @@ SIGNATURES = {
                                       _I64, _I64, _I64, _P, _SZ, _P]),
     "w4a8_linear_prepared_ex": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int, ctypes.c_float, ctypes.c_float,
                                                _I64, _I64, _I64, _P]),
+    "w4a8_prefill_linear_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    "w4a8_prefill_host_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "w4a8_prepared_activations_bytes": (_SZ, [_I64, _I64]),
     "w4a8_prepared_weights_bytes": (_SZ, [_I64, _I64]),
     "w4a8_linear_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
@@ -258,6 +260,45 @@ def prefill_linear_noalloc(x, wq, w_scale, w_zero, bias=None, y=None, stream=Non
     rc = load().w4a8_prefill_linear_noalloc(_ptr(x), _ptr(wq), _ptr(w_scale), _ptr(w_zero), _ptr(bias), _ptr(y),
                                             M, N, K, _stream(stream))
     _check(rc, "w4a8_prefill_linear_noalloc")
+    return y
+
+
+def prefill_host_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().w4a8_prefill_host_workspace_bytes(M, N, K))
+
+
+def _host(t, dtype, shape, name: str):
+    """A host-buffer argument: a page-locked, contiguous CPU tensor of the C layout."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+    if t.device.type != "cpu" or not t.is_pinned():
+        raise TypeError(f"{name} must be a page-locked host tensor (tensor.pin_memory())")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def prefill_linear_host(x, wq, w_scale, w_zero, bias=None, y=None, ws=None, stream=None):
+    """w4a8_prefill_linear_host: page-locked host x fp32 [M,K] -> page-locked host y fp32
+    [M,N]; the copies overlap the computation.  Asynchronous like every call: synchronize
+    the stream before reading y."""
+    _host(x, torch.float32, None, "x")
+    if x.dim() != 2:
+        raise ValueError(f"x must be 2-D [M, K], got shape {tuple(x.shape)}")
+    M, K = x.shape
+    N = _rows(wq)
+    dev = wq.device
+    _weights(wq, w_scale, w_zero, N, K, dev)
+    _arg(bias, torch.float32, (N,), "bias", dev)
+    y = torch.empty((M, N), dtype=torch.float32).pin_memory() if y is None else y
+    _host(y, torch.float32, (M, N), "y")
+    ws = _ws(ws, prefill_host_workspace_bytes(M, N, K), dev)
+    rc = load().w4a8_prefill_linear_host(_ptr(x), _ptr(wq), _ptr(w_scale), _ptr(w_zero), _ptr(bias), _ptr(y),
+                                         M, N, K, _ptr(ws), _nbytes(ws), _stream(stream))
+    _check(rc, "w4a8_prefill_linear_host")
     return y
 
 

@@ -3,6 +3,7 @@
 #include "../../include/w4a8.h"
 #include "w4a8_internal.h"
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -81,16 +82,18 @@ CallLayout call_layout(int64_t M, int64_t N, int64_t K, bool with_sa) {
     return c;
 }
 
-// GEMM + epilogue from prepared activations (token records) and prepared weights.
+// GEMM + epilogue from prepared activations (token records `tw` tokens wide) and prepared
+// weights.  Each output depends only on its own row and the kernel the width selects, so
+// rows cut into whole tiles of one width give the uncut call's outputs.
 int run_linear(const uint8_t* trec, const float* s_a, const uint8_t* pw, const float* bias, const OutSpec& out,
-               int64_t M, int64_t N, int64_t K, const DeviceInfo& d, cudaStream_t st) {
+               int64_t M, int64_t N, int64_t K, int tw, const DeviceInfo& d, cudaStream_t st) {
     const WLayout W = w_layout(N, K);
     GemmArgs g;
     g.M = M;
     g.N = N;
     g.K = K;
     g.trec = trec;
-    g.tw = token_tile(M);
+    g.tw = tw;
     g.wrec = pw;
     g.sc = reinterpret_cast<const float*>(pw + W.sc);
     g.s_a = s_a;
@@ -179,7 +182,7 @@ using namespace w4a8;
 
 extern "C" {
 
-int w4a8_abi_version(void) { return 202; }
+int w4a8_abi_version(void) { return 203; }
 
 const char* w4a8_status_string(int status) {
     switch (status) {
@@ -297,7 +300,7 @@ int linear_impl(const int8_t* a_q, const float* a_scale, const int32_t* rowsum, 
     p.tw = L.act.tw;
     set_weight_job(&p, wq, w_scale, w_zero, N, K, ws + L.w_off);
     if (launch_pack(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
-    return run_linear(ws + L.act.rec, a_scale, ws + L.w_off, bias, out, M, N, K, *d, st);
+    return run_linear(ws + L.act.rec, a_scale, ws + L.w_off, bias, out, M, N, K, L.act.tw, *d, st);
 }
 
 int prefill_impl(const float* x, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero,
@@ -344,7 +347,7 @@ int prefill_impl(const float* x, const uint8_t* wq, const uint16_t* w_scale, con
     p.tw = L.act.tw;
     set_weight_job(&p, wq, w_scale, w_zero, N, K, ws + L.w_off);
     if (launch_quant(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
-    return run_linear(ws + L.act.rec, s_a, ws + L.w_off, bias, out, M, N, K, *d, st);
+    return run_linear(ws + L.act.rec, s_a, ws + L.w_off, bias, out, M, N, K, L.act.tw, *d, st);
 }
 
 int linear_prepared_impl(const void* act, const void* pw, const float* bias, const OutSpec& out, int64_t M,
@@ -360,7 +363,7 @@ int linear_prepared_impl(const void* act, const void* pw, const float* bias, con
     const ActLayout A = act_layout(M, K, true, token_tile(M));
     const uint8_t* a = static_cast<const uint8_t*>(act);
     return run_linear(a + A.rec, reinterpret_cast<const float*>(a + A.s_a), static_cast<const uint8_t*>(pw), bias,
-                      out, M, N, K, *d, static_cast<cudaStream_t>(stream));
+                      out, M, N, K, A.tw, *d, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -542,6 +545,197 @@ int w4a8_prefill_linear_noalloc(const float* x, const uint8_t* wq, const uint16_
     if ((rc = noalloc_scratch(&scratch)) != W4A8_OK) return rc;
     return w4a8_prefill_linear(x, wq, w_scale, w_zero, bias, y, M, N, K, scratch, W4A8_NOALLOC_SCRATCH_BYTES,
                                stream);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- host-buffer call
+// w4a8_prefill_linear_host: x and y in page-locked host memory.  The rows are cut into chunks
+// so that the copy of chunk c+1 to the device, the linear on chunk c and the copy of chunk
+// c-1 back run at the same time: one stream carries the host-to-device copies in row order,
+// one the device-to-host copies, and the chunks' pre-passes and contractions rotate over
+// kHostStreams streams of their own (a chunk's GEMM covers a part of the SMs; concurrent
+// chunks fill the rest).  The weights are prepared once, on the caller's stream, while the
+// first chunk is copied in.  Chunks are whole token tiles of the width the uncut call would
+// use, and the GEMM is told that width, so chunking changes no output (the prepared form
+// gives the fused call's results bit for bit).  A chunk moves at least kHostChunkBytes of x
+// and y: below that the fixed cost of a copy and a launch outweighs the overlap.
+namespace w4a8 {
+namespace {
+
+constexpr int kHostChunks = 8;
+constexpr int kHostStreams = 4;
+constexpr int64_t kHostChunkBytes = int64_t(8) << 20;
+
+struct HostPlan {
+    int chunks = 1;
+    int tw = 128;      // token-record width of the uncut call
+    int64_t rows = 0;  // rows of every chunk but the last, which takes the remainder
+    size_t y_off = 0, ws_off = 0, act_stride = 0, total = 0;  // x at offset 0
+};
+
+HostPlan host_plan(int64_t M, int64_t N, int64_t K) {
+    HostPlan h;
+    h.tw = token_tile(M);
+    if (!few_tokens(M, K)) {
+        const int64_t by_rows = M / h.tw;
+        const int64_t by_bytes = M * (K + N) * 4 / kHostChunkBytes;
+        h.chunks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({kHostChunks, by_rows, by_bytes})));
+    }
+    h.rows = h.chunks > 1 ? (M / h.chunks) / h.tw * h.tw : M;
+    h.y_off = align_ws(static_cast<size_t>(M) * static_cast<size_t>(K) * 4u);
+    h.ws_off = align_ws(h.y_off + static_cast<size_t>(M) * static_cast<size_t>(N) * 4u);
+    if (h.chunks == 1) {
+        h.total = h.ws_off + prefill_ws(M, N, K);
+        return h;
+    }
+    // prepared weights, then one prepared-activation buffer per compute stream, sized for the
+    // last (largest) chunk; a stream's chunks run in order, so they can share one
+    const int64_t last = M - (h.chunks - 1) * h.rows;
+    h.act_stride = act_layout(last, K, true, h.tw).total;
+    h.total = h.ws_off + w_layout(N, K).total + static_cast<size_t>(std::min(h.chunks, kHostStreams)) * h.act_stride;
+    return h;
+}
+
+// Streams and events of the host-buffer call, created on a device's first chunked call and
+// kept for the life of the process.  The mutex keeps concurrent callers from interleaving
+// their event records.
+struct HostRes {
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr, comp[kHostStreams] = {};
+    cudaEvent_t start = nullptr, weights = nullptr, done = nullptr, in[kHostChunks] = {}, out[kHostChunks] = {};
+    std::mutex mu;
+};
+
+HostRes g_host[kMaxDevices];
+std::mutex g_host_init_mu;
+
+int host_resources(HostRes** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return W4A8_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return W4A8_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(g_host_init_mu);
+    HostRes& r = g_host[dev];
+    if (!r.ready) {
+        const unsigned sf = cudaStreamNonBlocking;
+        const unsigned ef = cudaEventDisableTiming;
+        // each handle is created once: a failed attempt keeps what it made for the next one
+        auto stream = [&](cudaStream_t* h) { return *h || cudaStreamCreateWithFlags(h, sf) == cudaSuccess; };
+        auto event = [&](cudaEvent_t* h) { return *h || cudaEventCreateWithFlags(h, ef) == cudaSuccess; };
+        bool ok = stream(&r.h2d) && stream(&r.d2h) && event(&r.start) && event(&r.weights) && event(&r.done);
+        for (int i = 0; ok && i < kHostStreams; ++i) ok = stream(&r.comp[i]);
+        for (int c = 0; ok && c < kHostChunks; ++c) ok = event(&r.in[c]) && event(&r.out[c]);
+        if (!ok) return W4A8_ERR_CUDA;
+        r.ready = true;
+    }
+    *out = &r;
+    return W4A8_OK;
+}
+
+bool page_locked(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // an unknown pointer is an answer here, not a sticky error
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
+
+}  // namespace
+}  // namespace w4a8
+
+extern "C" {
+
+size_t w4a8_prefill_host_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (check_shape(M, N, K) != W4A8_OK) return static_cast<size_t>(-1);
+    if (M == 0 || N == 0) return 0;
+    return host_plan(M, N, K).total;
+}
+
+int w4a8_prefill_linear_host(const float* x_host, const uint8_t* wq, const uint16_t* w_scale,
+                             const uint16_t* w_zero, const float* bias, float* y_host, int64_t M, int64_t N,
+                             int64_t K, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_shape(M, N, K);
+    if (rc != W4A8_OK) return rc;
+    if (M == 0 || N == 0) return W4A8_OK;
+    if (!x_host || !y_host || !wq || !w_scale || !w_zero || !workspace) return W4A8_ERR_ARG;
+    if (!aligned(wq, 16) || !aligned(w_scale, 2) || !aligned(w_zero, 2) || (bias && !aligned(bias, 4)) ||
+        !aligned(workspace, 16))
+        return W4A8_ERR_ALIGN;
+    const HostPlan h = host_plan(M, N, K);
+    if (workspace_bytes < h.total) return W4A8_ERR_WORKSPACE;
+    DeviceInfo* d = nullptr;
+    if ((rc = current_device(&d)) != W4A8_OK) return rc;
+    if (!page_locked(x_host) || !page_locked(y_host)) return W4A8_ERR_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* x_dev = reinterpret_cast<float*>(ws);
+    float* y_dev = reinterpret_cast<float*>(ws + h.y_off);
+    const size_t x_bytes = static_cast<size_t>(M) * static_cast<size_t>(K) * 4u;
+    const size_t y_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * 4u;
+
+    if (h.chunks == 1) {
+        // too little to overlap: copy in, the fused call, copy out, all on the caller's stream
+        if (cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return W4A8_ERR_CUDA;
+        rc = prefill_impl(x_dev, wq, w_scale, w_zero, bias, f32_out(y_dev), M, N, K, ws + h.ws_off,
+                          workspace_bytes - h.ws_off, stream);
+        if (rc != W4A8_OK) return rc;
+        return cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, st) == cudaSuccess ? W4A8_OK
+                                                                                                : W4A8_ERR_CUDA;
+    }
+
+    HostRes* r = nullptr;
+    if ((rc = host_resources(&r)) != W4A8_OK) return rc;
+    std::lock_guard<std::mutex> lk(r->mu);
+    uint8_t* pw = ws + h.ws_off;
+    uint8_t* act0 = pw + w_layout(N, K).total;
+    bool ok = cudaEventRecord(r->start, st) == cudaSuccess && cudaStreamWaitEvent(r->h2d, r->start, 0) == cudaSuccess &&
+              cudaStreamWaitEvent(r->d2h, r->start, 0) == cudaSuccess;
+    // the weight records, once, on the caller's stream
+    if (ok) {
+        PrepArgs p;
+        p.M = 0;
+        set_weight_job(&p, wq, w_scale, w_zero, N, K, pw);
+        ok = launch_pack(p, st) == cudaSuccess && cudaEventRecord(r->weights, st) == cudaSuccess;
+    }
+    for (int c = 0; ok && c < h.chunks; ++c) {
+        const int64_t r0 = c * h.rows;
+        const int64_t rows = c + 1 < h.chunks ? h.rows : M - r0;
+        const size_t xo = static_cast<size_t>(r0) * static_cast<size_t>(K);
+        const size_t yo = static_cast<size_t>(r0) * static_cast<size_t>(N);
+        const int si = c % kHostStreams;
+        cudaStream_t cs = r->comp[si];
+        ok = cudaMemcpyAsync(x_dev + xo, x_host + xo, static_cast<size_t>(rows) * static_cast<size_t>(K) * 4u,
+                             cudaMemcpyHostToDevice, r->h2d) == cudaSuccess &&
+             cudaEventRecord(r->in[c], r->h2d) == cudaSuccess && cudaStreamWaitEvent(cs, r->in[c], 0) == cudaSuccess &&
+             cudaStreamWaitEvent(cs, r->weights, 0) == cudaSuccess;
+        if (ok) {
+            uint8_t* act = act0 + static_cast<size_t>(si) * h.act_stride;
+            const ActLayout A = act_layout(rows, K, true, h.tw);
+            PrepArgs p;
+            p.x = x_dev + xo;
+            p.M = rows;
+            p.K = K;
+            p.s_a_out = reinterpret_cast<float*>(act + A.s_a);
+            p.trec = act + A.rec;
+            p.tw = A.tw;
+            ok = launch_quant(p, cs) == cudaSuccess &&
+                 run_linear(act + A.rec, p.s_a_out, pw, bias, f32_out(y_dev + yo), rows, N, K, h.tw, *d, cs) ==
+                     W4A8_OK &&
+                 cudaEventRecord(r->out[c], cs) == cudaSuccess;
+        }
+        ok = ok && cudaStreamWaitEvent(r->d2h, r->out[c], 0) == cudaSuccess &&
+             cudaMemcpyAsync(y_host + yo, y_dev + yo, static_cast<size_t>(rows) * static_cast<size_t>(N) * 4u,
+                             cudaMemcpyDeviceToHost, r->d2h) == cudaSuccess;
+    }
+    // The caller's stream resumes once the last copy back has landed.  It waits on every side
+    // stream's final event, not only the last one's, so that a capture into a tape joins each
+    // forked stream back to the capturing stream directly.
+    ok = ok && cudaEventRecord(r->done, r->d2h) == cudaSuccess && cudaStreamWaitEvent(st, r->done, 0) == cudaSuccess &&
+         cudaStreamWaitEvent(st, r->in[h.chunks - 1], 0) == cudaSuccess;
+    for (int c = std::max(0, h.chunks - kHostStreams); ok && c < h.chunks; ++c)
+        ok = cudaStreamWaitEvent(st, r->out[c], 0) == cudaSuccess;
+    return ok ? W4A8_OK : W4A8_ERR_CUDA;
 }
 
 }  // extern "C"
