@@ -180,10 +180,15 @@ int w4a8_prefill_linear_noalloc(const float *x, const uint8_t *wq, const uint16_
  * bias and workspace are device memory as elsewhere.  workspace: at least
  * w4a8_prefill_host_workspace_bytes(M, N, K) bytes, 16-byte aligned (it holds the device
  * copies of x and y and the pre-pass scratch).
- *   - The rows are cut into up to four chunks (none below 128 rows, none below 4096 rows
- *     once M reaches 4096; few-token and short calls are one chunk).  Chunk c+1's copy to
- *     the device, chunk c's linear and chunk c-1's copy back overlap, on streams the library
- *     creates on a device's first chunked call and keeps until the process exits.
+ *   - Large calls are cut into up to eight row chunks, each a whole number of token tiles
+ *     and at least 8 MiB of x and y.  Chunk c+1's copy to the device, chunk c's linear and
+ *     chunk c-1's copy back overlap, on six streams the library creates on a device's first
+ *     chunked call and keeps until the process exits.
+ *   - Smaller calls are one chunk.  When the driver maps the host buffers into the device's
+ *     address space (cudaHostAlloc memory under unified addressing), the kernels then read
+ *     x and write y in place over the host link, so the transfers overlap the computation;
+ *     otherwise x and y are copied through the workspace.  The few-token form always copies
+ *     x.
  *   - Stream-ordered like every call: the work starts after what was enqueued on `stream`
  *     before it, and what is enqueued after it sees y_host complete.  The host buffers must
  *     stay valid and x_host unchanged until then.  Calls sharing a workspace must be

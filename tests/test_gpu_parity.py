@@ -539,31 +539,41 @@ def test_host_call_reuses_a_workspace_in_stream_order():
 
 
 def test_tape_records_the_host_call():
-    """The host-buffer call recorded into a tape (its side streams joined back into the
-    capture) replays bit for bit, and follows new contents of the same host x."""
+    """Host-buffer calls recorded into a tape -- one cut into chunks (its side streams joined
+    back into the capture), one small enough to work on the mapped host buffers in place --
+    replay bit for bit, and follow new contents of the same host x."""
     b = B()
-    M, K, N = 2048, 1024, 2048
-    d = synth.random_small(M, K, N, seed=95, bias=True)
-    g = inputs_to_dev(d)
-    xh = _pinned(d["x"])
-    yh = torch.empty((M, N)).pin_memory()
-    ws = b.workspace(b.prefill_host_workspace_bytes(M, N, K), dev())
+    shapes = [(2048, 1024, 2048), (512, 1024, 320)]
+    ds = [synth.random_small(M, K, N, seed=95 + i, bias=True) for i, (M, K, N) in enumerate(shapes)]
+    gs = [inputs_to_dev(d) for d in ds]
+    xs = [_pinned(d["x"]) for d in ds]
+    ys = [torch.empty((M, N)).pin_memory() for M, K, N in shapes]
+    wss = [b.workspace(b.prefill_host_workspace_bytes(M, N, K), dev()) for M, K, N in shapes]
     s = torch.cuda.Stream()
-    with torch.cuda.stream(s):
-        b.prefill_linear_host(xh, g["wq"], g["s_w"], g["z_w"], g["bias"], y=yh, ws=ws, stream=s)
-        s.synchronize()
-        eager = yh.clone()
-        with b.Tape(s) as tape:
+
+    def calls():
+        for g, xh, yh, ws in zip(gs, xs, ys, wss):
             b.prefill_linear_host(xh, g["wq"], g["s_w"], g["z_w"], g["bias"], y=yh, ws=ws, stream=s)
-    yh.fill_(float("nan"))
+
+    with torch.cuda.stream(s):
+        calls()
+        s.synchronize()
+        eager = [y.clone() for y in ys]
+        with b.Tape(s) as tape:
+            calls()
+    for y in ys:
+        y.fill_(float("nan"))
     tape.replay(s)
     s.synchronize()
-    assert torch.equal(yh, eager)
-    xh.mul_(-0.5)
-    ref = b.prefill_linear(xh.to(dev()), g["wq"], g["s_w"], g["z_w"], g["bias"]).cpu()
+    for y, e in zip(ys, eager):
+        assert torch.equal(y, e)
+    for xh in xs:
+        xh.mul_(-0.5)
+    refs = [b.prefill_linear(xh.to(dev()), g["wq"], g["s_w"], g["z_w"], g["bias"]).cpu() for xh, g in zip(xs, gs)]
     tape.replay(s)
     s.synchronize()
-    assert torch.equal(yh, ref)
+    for y, r in zip(ys, refs):
+        assert torch.equal(y, r)
     tape.free()
     assert b.sync_status() == 0
 

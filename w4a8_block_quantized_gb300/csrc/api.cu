@@ -559,7 +559,8 @@ int w4a8_prefill_linear_noalloc(const float* x, const uint8_t* wq, const uint16_
 // first chunk is copied in.  Chunks are whole token tiles of the width the uncut call would
 // use, and the GEMM is told that width, so chunking changes no output (the prepared form
 // gives the fused call's results bit for bit).  A chunk moves at least kHostChunkBytes of x
-// and y: below that the fixed cost of a copy and a launch outweighs the overlap.
+// and y: below that the fixed cost of a copy and a launch outweighs the overlap, and a call
+// too small for two chunks works on mapped host buffers in place instead.
 namespace w4a8 {
 namespace {
 
@@ -632,13 +633,23 @@ int host_resources(HostRes** out) {
     return W4A8_OK;
 }
 
-bool page_locked(const void* p) {
+// A page-locked host buffer and, when the driver maps it into the device's address space
+// (always for cudaHostAlloc memory under unified addressing), the address kernels use.
+struct HostBuf {
+    bool locked = false;
+    void* dev = nullptr;
+};
+
+HostBuf host_buffer(const void* p) {
+    HostBuf h;
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
         cudaGetLastError();  // an unknown pointer is an answer here, not a sticky error
-        return false;
+        return h;
     }
-    return a.type == cudaMemoryTypeHost;
+    h.locked = a.type == cudaMemoryTypeHost;
+    if (h.locked && a.devicePointer && aligned(a.devicePointer, 16)) h.dev = a.devicePointer;
+    return h;
 }
 
 }  // namespace
@@ -666,7 +677,8 @@ int w4a8_prefill_linear_host(const float* x_host, const uint8_t* wq, const uint1
     if (workspace_bytes < h.total) return W4A8_ERR_WORKSPACE;
     DeviceInfo* d = nullptr;
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
-    if (!page_locked(x_host) || !page_locked(y_host)) return W4A8_ERR_ARG;
+    const HostBuf xb = host_buffer(x_host), yb = host_buffer(y_host);
+    if (!xb.locked || !yb.locked) return W4A8_ERR_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     float* x_dev = reinterpret_cast<float*>(ws);
@@ -675,11 +687,19 @@ int w4a8_prefill_linear_host(const float* x_host, const uint8_t* wq, const uint1
     const size_t y_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * 4u;
 
     if (h.chunks == 1) {
-        // too little to overlap: copy in, the fused call, copy out, all on the caller's stream
-        if (cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return W4A8_ERR_CUDA;
-        rc = prefill_impl(x_dev, wq, w_scale, w_zero, bias, f32_out(y_dev), M, N, K, ws + h.ws_off,
+        // Too little to cut into chunks.  Where the host buffers are mapped, the kernels work
+        // on them in place over the host link, so the transfers overlap the computation
+        // without a copy's fixed cost: the pre-pass reads x with plain loads, and every
+        // epilogue writes y with plain stores.  The few-token kernel fetches x with bulk
+        // copies, so its x goes through the device copy.  Unmapped buffers are copied.
+        const bool x_direct = xb.dev && !few_tokens(M, K);
+        const float* x_in = x_direct ? static_cast<const float*>(xb.dev) : x_dev;
+        float* y_out = yb.dev ? static_cast<float*>(yb.dev) : y_dev;
+        if (!x_direct && cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return W4A8_ERR_CUDA;
+        rc = prefill_impl(x_in, wq, w_scale, w_zero, bias, f32_out(y_out), M, N, K, ws + h.ws_off,
                           workspace_bytes - h.ws_off, stream);
-        if (rc != W4A8_OK) return rc;
+        if (rc != W4A8_OK || yb.dev) return rc;
         return cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, st) == cudaSuccess ? W4A8_OK
                                                                                                 : W4A8_ERR_CUDA;
     }
