@@ -474,7 +474,9 @@ def run_bench(args):
         "e2e": {"value": e2e_value, "unit": unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3 / e2e_steps, 4),
-                "call": "w4a8_prefill_linear_host (page-locked x and y; chunked copies overlap the linear)",
+                "call": "w4a8_prefill_linear_host: page-locked host x and y; a call of 16 MiB or more "
+                        "overlaps its row chunks' copies with the linear, a smaller one reads x and writes y "
+                        "in place over the host link (the few-token form copies x)",
                 "bound": e2e_bound,
                 "copies_then_call": {"value": round(e2e_value * e2e_s / e2e_serial_s, 3 if not decode else 1),
                                      "ms_per_step": round(e2e_serial_s * 1e3 / e2e_steps, 4)}},
