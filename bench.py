@@ -349,6 +349,8 @@ def run_bench(args):
         # x read, two e4m3 planes written, s_a, and one 16-byte zero-point operand entry per 64-block
         prep_bytes = sum(s.M * s.K * 4 + s.M * s.K * 2 + s.M * 4 + s.M * (s.K // 64) * 16 for s in specs) / len(lin)
     prep_gbs = prep_bytes / (prep_avg * 1e-3) / 1e9
+    gemm_hbm_bytes = sum(s.M * s.K + s.M * (s.K // 64) * 4 + s.N * s.K // 2 + 2 * s.N * (s.K // 64) * 2 +
+                         (4 * s.N if s.bias else 0) + 4 * s.M * s.N for s in specs) / len(lin)
 
     # ---------------- end to end through the C ABI with host buffers: the host-buffer call
     # (x in, y out in page-locked host memory; its chunked copies overlap the computation),
@@ -432,7 +434,13 @@ def run_bench(args):
                     "frac": round(gemm_tops / tensor_peak, 4),
                     "traffic": None if args.shape else recorded_traffic(args.workload),
                     "peak_source": f"{peak_src} bf16 burst x2 (fp8 nominal ratio) /2 (two e4m3 MACs per int8 MAC)",
-                    "gemm_us_per_launch": round(gemm_avg * 1e3, 3)}
+                    "gemm_us_per_launch": round(gemm_avg * 1e3, 3),
+                    # small M is also read against HBM: the bytes a launch must move (codes, row
+                    # sums, packed weights, scales and zeros, bias, y) over the same time
+                    "hbm_view": {"bytes_per_launch": int(gemm_hbm_bytes),
+                                 "achieved": round(gemm_hbm_bytes / (gemm_avg * 1e-3) / 1e9, 1),
+                                 "peak": hbm_gbs, "unit": "GB/s",
+                                 "frac": round(gemm_hbm_bytes / (gemm_avg * 1e-3) / 1e9 / hbm_gbs, 4)}}
     e2e_tops = whole_job_rate(ops_per_step * e2e_steps, world, e2e_s) / 1e12
     if decode:
         # a decode step is one token (per sequence of the batch) through every linear:
@@ -454,6 +462,8 @@ def run_bench(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5),
+        "ms_median": round(statistics.median(step_ms), 5),
+        "ms_min": round(min(step_ms), 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -605,9 +615,39 @@ def cpu_baseline(lin, specs, seconds):
         total_ops += 2 * n * s.N * s.K * (reps + 1)
         total_s += dt
         parts.append(f"{s.name}: {n}/{s.M} rows x {reps + 1}")
-    return {"value": round(total_ops / total_s / 1e12, 6), "unit": "TOPS", "cores": oracle.num_threads(),
-            "kind": "oracle", "sample": "evenly spaced rows of the workload, all outputs: " + "; ".join(parts),
-            "seconds": round(total_s, 2)}
+    out = {"value": round(total_ops / total_s / 1e12, 6), "unit": "TOPS", "cores": oracle.num_threads(),
+           "kind": "oracle", "sample": "evenly spaced rows of the workload, all outputs: " + "; ".join(parts),
+           "seconds": round(total_s, 2), "cpu": cpu_model(), "nproc": os.cpu_count()}
+    # the same oracle compiled without OpenMP, on one core, for a quarter of the time
+    oracle.build(tag="oracle_1core", openmp=False)
+    s, h = specs[0], lin[0]["host"]
+    rows1 = np.arange(min(4, s.M), dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.prefill_linear(h["x"], h["wq"], h["s_w"], h["z_w"], h["bias"], rows=rows1, tag="oracle_1core")
+    dt1 = max(time.perf_counter() - t0, 1e-4) / len(rows1)
+    n1 = int(max(4, min(s.M, seconds / 4 / dt1)))
+    rows1 = np.linspace(0, s.M - 1, n1).astype(np.int64)
+    reps1 = max(1, min(1000, int(seconds / 4 / (dt1 * n1))))
+    t0 = time.perf_counter()
+    for _ in range(reps1):
+        oracle.prefill_linear(h["x"], h["wq"], h["s_w"], h["z_w"], h["bias"], rows=rows1, tag="oracle_1core")
+    dt1 = time.perf_counter() - t0
+    out["one_core"] = {"value": round(2 * n1 * s.N * s.K * reps1 / dt1 / 1e12, 6), "unit": "TOPS",
+                       "sample": f"{s.name}: {n1}/{s.M} rows x {reps1}", "seconds": round(dt1, 2)}
+    return out
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), else the machine type."""
+    import platform
+    try:
+        text = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in text.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
 
 
 def run_reference(args):

@@ -39,8 +39,7 @@ def build(defines: tuple[str, ...] = (), tag: str = "oracle", openmp: bool = Tru
         return out
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
            "-fno-fast-math", "-Wall", "-Wextra"]
-    if openmp:
-        cmd.append("-fopenmp")
+    cmd.append("-fopenmp" if openmp else "-Wno-unknown-pragmas")
     cmd += [f"-D{d}" for d in defines]
     tmp = out + f".tmp{os.getpid()}"
     cmd += [_SRC, "-o", tmp, "-lm"]
