@@ -255,3 +255,17 @@ def test_binding_host_call_wants_page_locked_buffers():
     sw = torch.zeros((8, 1), dtype=torch.float16)
     with pytest.raises(TypeError, match="page-locked"):
         b.prefill_linear_host(x, wq, sw, sw)
+
+
+def test_plain_c_client(lib, tmp_path):
+    """The header compiles as strict C99 and a C program links against the library and gets
+    the documented answers from the calls that need no GPU."""
+    import subprocess
+    from w4a8_block_quantized_gb300 import binding
+    libdir = os.path.dirname(binding.LIB_PATH)
+    exe = tmp_path / "c_client"
+    subprocess.run(["gcc", "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), os.path.join(ROOT, "tests", "c_client.c"),
+                    "-L", libdir, "-lw4a8", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", out.stdout + out.stderr
