@@ -180,7 +180,7 @@ int w4a8_prefill_linear_noalloc(const float *x, const uint8_t *wq, const uint16_
  * bias and workspace are device memory as elsewhere.  workspace: at least
  * w4a8_prefill_host_workspace_bytes(M, N, K) bytes, 16-byte aligned (it holds the device
  * copies of x and y and the pre-pass scratch).
- *   - Large calls are cut into up to eight row chunks, each a whole number of token tiles
+ *   - Large calls are cut into up to sixteen row chunks, each a whole number of token tiles
  *     and at least 8 MiB of x and y.  Chunk c+1's copy to the device, chunk c's linear and
  *     chunk c-1's copy back overlap, on six streams the library creates on a device's first
  *     chunked call and keeps until the process exits.

@@ -193,10 +193,10 @@ def test_host_call_workspace_and_chunking(lib):
     """The host-buffer call's workspace: the device copies of x and y, then either the fused
     call's scratch (one chunk) or the prepared weights and one prepared-activation buffer per
     compute stream (at most four), sized for the last, largest chunk.  A call is cut into at
-    most eight chunks of whole token tiles, each moving at least 8 MiB of x and y."""
+    most sixteen chunks of whole token tiles, each moving at least 8 MiB of x and y."""
     def plan(M, N, K):
         tw = 256 if M >= 4096 else 128
-        chunks = 1 if M <= 8 else max(1, min(8, M // tw, M * (K + N) * 4 // (8 << 20)))
+        chunks = 1 if M <= 8 else max(1, min(16, M // tw, M * (K + N) * 4 // (8 << 20)))
         rows = (M // chunks) // tw * tw if chunks > 1 else M
         return chunks, M - (chunks - 1) * rows
 
@@ -222,7 +222,8 @@ def test_host_call_workspace_and_chunking(lib):
                 min(chunks, 4) * lib.w4a8_prepared_activations_bytes(last, K)
         assert got == want, (M, N, K)
     # 256-token records: chunks of whole 256-row tiles, below 4096 rows each
-    for M, N, K in ((8192, 14336, 4096), (8300, 512, 256), (9000, 1536, 512)):
+    assert plan(8192, 14336, 4096)[0] == 16 and plan(16384, 1024, 1024) == (16, 1024)
+    for M, N, K in ((8192, 14336, 4096), (8300, 512, 256), (9000, 1536, 512), (16384, 1024, 1024)):
         chunks, last = plan(M, N, K)
         assert chunks > 1 and last < 4096
         got = lib.w4a8_prefill_host_workspace_bytes(M, N, K)

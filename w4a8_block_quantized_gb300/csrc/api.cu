@@ -564,7 +564,7 @@ int w4a8_prefill_linear_noalloc(const float* x, const uint8_t* wq, const uint16_
 namespace w4a8 {
 namespace {
 
-constexpr int kHostChunks = 8;
+constexpr int kHostChunks = 16;
 constexpr int kHostStreams = 4;
 constexpr int64_t kHostChunkBytes = int64_t(8) << 20;
 
