@@ -1,5 +1,6 @@
 // api.cu -- the C ABI declared in include/w4a8.h: argument validation, workspace
-// carving, routing by shape and kernel launches.  Nothing here allocates memory.
+// carving, routing by shape and kernel launches.  Nothing here allocates memory; the
+// host-buffer call keeps a few streams and events per device, created on first use.
 #include "../../include/w4a8.h"
 #include "w4a8_internal.h"
 
