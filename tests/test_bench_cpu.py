@@ -40,3 +40,21 @@ def test_workloads_match_the_documented_shapes():
     # the decode workloads' weights at 4.5 bits per weight
     s = synth.workload("d4")[1][0]
     assert synth.weight_bytes(s) == s.N * s.K // 2 + 4 * s.N * (s.K // 64)
+
+
+def test_cpu_baseline_object():
+    """The GPU line's `cpu_baseline`: the oracle on all host cores over a stated sample, the CPU
+    model and core count, and the single-thread build's figure beside it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from w4a8_block_quantized_gb300 import synth
+    _, specs = synth.workload("c0")
+    lin = [{"host": synth.make_linear(s), "spec": s} for s in specs]
+    c = bench.cpu_baseline(lin, specs, 1.0)
+    assert c["kind"] == "oracle" and c["unit"] == "TOPS" and c["value"] > 0
+    assert c["cores"] >= 1 and c["nproc"] == os.cpu_count() and c["cpu"]
+    assert "rows" in c["sample"] and c["seconds"] > 0
+    one = c["one_core"]
+    assert one["unit"] == "TOPS" and 0 < one["value"] and "rows" in one["sample"]
+    # one thread cannot outrun the whole pool by much (timing noise aside)
+    assert one["value"] <= 2 * c["value"]
