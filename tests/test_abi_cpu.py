@@ -256,6 +256,10 @@ def test_binding_host_call_wants_page_locked_buffers():
     sw = torch.zeros((8, 1), dtype=torch.float16)
     with pytest.raises(TypeError, match="page-locked"):
         b.prefill_linear_host(x, wq, sw, sw)
+    # an empty problem has nothing to pin: its host tensors pass the check
+    b._host(torch.empty((0, 64)), torch.float32, (0, 64), "x")
+    with pytest.raises(TypeError, match="page-locked"):
+        b._host(torch.empty((1, 64)), torch.float32, (1, 64), "x")
 
 
 def test_plain_c_client(lib, tmp_path):

@@ -271,7 +271,8 @@ def _host(t, dtype, shape, name: str):
     """A host-buffer argument: a page-locked, contiguous CPU tensor of the C layout."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
-    if t.device.type != "cpu" or not t.is_pinned():
+    # an empty tensor has no storage to pin; the library reads no pointer of an empty problem
+    if t.device.type != "cpu" or (t.numel() and not t.is_pinned()):
         raise TypeError(f"{name} must be a page-locked host tensor (tensor.pin_memory())")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
@@ -293,7 +294,9 @@ def prefill_linear_host(x, wq, w_scale, w_zero, bias=None, y=None, ws=None, stre
     dev = wq.device
     _weights(wq, w_scale, w_zero, N, K, dev)
     _arg(bias, torch.float32, (N,), "bias", dev)
-    y = torch.empty((M, N), dtype=torch.float32).pin_memory() if y is None else y
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32)
+        y = y.pin_memory() if y.numel() else y
     _host(y, torch.float32, (M, N), "y")
     ws = _ws(ws, prefill_host_workspace_bytes(M, N, K), dev)
     rc = load().w4a8_prefill_linear_host(_ptr(x), _ptr(wq), _ptr(w_scale), _ptr(w_zero), _ptr(bias), _ptr(y),
