@@ -193,7 +193,9 @@ int w4a8_prefill_linear_noalloc(const float *x, const uint8_t *wq, const uint16_
  *     before it, and what is enqueued after it sees y_host complete.  The host buffers must
  *     stay valid and x_host unchanged until then.  Calls sharing a workspace must be
  *     ordered (one stream).  It may be recorded into a tape (make one call of the shape
- *     first).
+ *     first).  A chunked call joins the library's side streams to the capture until
+ *     w4a8_tape_end, so meanwhile no other thread may make a host-buffer call on that
+ *     device.
  *   - Results are bit-identical to w4a8_prefill_linear on the same inputs. */
 size_t w4a8_prefill_host_workspace_bytes(int64_t M, int64_t N, int64_t K);
 int w4a8_prefill_linear_host(const float *x_host, const uint8_t *wq, const uint16_t *w_scale,
