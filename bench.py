@@ -32,6 +32,26 @@ import torch  # noqa: E402
 METRIC = "W4A8 block64 prefill linear: effective TOPS & tok/s at M=512; % of INT8 peak"
 DECODE_METRIC = "W4A8 block64 decode linear: tokens/s at M=1 (weights streamed at 4.5 bits each); % of HBM"
 L2_FLUSH_BYTES = 256 << 20
+# The other INT8 denominator: the integer tensor path sm_103a still has, the legacy warp-level
+# mma.sync.m16n8k32.s8.s8.s32, measured on a GB300 of this kind by a standalone probe (608 CTAs
+# x 8 warps, 8 independent accumulators per warp, SM clock 2070 MHz).  tcgen05 has no integer
+# kind on sm_103a, so this is the only "INT8 tensor peak" the part offers.
+MMA_SYNC_S8_TOPS = 158.2
+MMA_SYNC_S8_SOURCE = "measured: mma.sync.m16n8k32.s8 probe on GB300 (608 CTAs x 8 warps, 8 accumulators per warp)"
+
+
+def prepass_bytes(M: int, K: int) -> int:
+    """Algorithmic bytes of one activation pre-pass: x read (4 B per element); the int8 codes
+    (1 B), the int32 block row sums (4 B per 64 elements) and the row's scale written --
+    M*K*(4 + 1 + 4/64) + 8*M."""
+    return M * K * 4 + M * K + M * (K // 64) * 4 + 8 * M
+
+
+def record_prepass_bytes(M: int, K: int) -> int:
+    """Bytes the fused call's pre-pass actually moves in its tensor-core record format: x read,
+    two e4m3 nibble planes (2 B per element), one 16-byte zero-point operand entry per 64
+    elements and the scale written."""
+    return M * K * 4 + M * K * 2 + M * (K // 64) * 16 + 4 * M
 
 
 def parse_args(argv=None):
@@ -48,6 +68,8 @@ def parse_args(argv=None):
     p.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
     p.add_argument("--profile", action="store_true",
                    help="only the warm-up and timed fused steps (for ncu captures); prints a short line")
+    p.add_argument("--no-targets", action="store_true",
+                   help="skip the 7B-class kernel measurements of the targets object")
     return p.parse_args(argv)
 
 
@@ -190,6 +212,15 @@ def measured_peaks():
 
 
 # ------------------------------------------------------------------ workload
+def workload_config(key, title, specs, world):
+    """The `config` object of a bench line (the same for both arms)."""
+    return {"workload": f"{key}: {title}",
+            "linears": [{"name": s.name, "M": s.M, "K": s.K, "N": s.N, "bias": s.bias} for s in specs],
+            "tokens_per_step": specs[0].M, "ops_per_step": sum(s.ops for s in specs),
+            "l2": "flushed before every timed step (256 MiB written, then read back; outside the timed events)",
+            "parallelism": f"replicas x{world}"}
+
+
 def load_workload(key, device, shape=None):
     from w4a8_block_quantized_gb300 import binding, synth
     if shape:
@@ -261,7 +292,6 @@ def run_bench(args):
         ev[i][1].record(stream)
     torch.cuda.synchronize(device)
     t_end = time.time()
-    clk.__exit__(None, None, None)
     dist_barrier(world)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_s = reduce_max(sum(step_ms) / 1e3, world, device)
@@ -271,6 +301,7 @@ def run_bench(args):
     value_tops = whole_job_rate(ops_per_step * args.steps, world, total_s) / 1e12
     tok_s = whole_job_rate(M * args.steps, world, total_s)
     if args.profile:
+        clk.__exit__(None, None, None)
         if rank == 0:
             print(json.dumps({"profile": title, "ms_per_step": ms_per_step, "tops": value_tops,
                               "status": binding.sync_status(stream),
@@ -338,7 +369,7 @@ def run_bench(args):
     gemm_tops = gemm_ops / (gemm_avg * 1e-3) / 1e12
     if decode:
         # x read; a_q, s_a and the int32 row sums written (API layout)
-        prep_bytes = sum(s.M * s.K * 4 + s.M * s.K + s.M * 4 + s.M * (s.K // 64) * 4 for s in specs) / len(lin)
+        prep_bytes = sum(prepass_bytes(s.M, s.K) for s in specs) / len(lin)
         # packed weights + s_w + z_w, the activations (x when the kernel quantizes, else the
         # codes, row sums and scales), bias and y
         gemv_bytes = sum(synth.weight_bytes(s) + (4 * s.M * s.K if one_launch else
@@ -346,8 +377,10 @@ def run_bench(args):
                          (4 * s.N if s.bias else 0) + 4 * s.M * s.N for s in specs) / len(lin)
         gemv_gbs = gemv_bytes / (gemm_avg * 1e-3) / 1e9
     else:
-        # x read, two e4m3 planes written, s_a, and one 16-byte zero-point operand entry per 64-block
-        prep_bytes = sum(s.M * s.K * 4 + s.M * s.K * 2 + s.M * 4 + s.M * (s.K // 64) * 16 for s in specs) / len(lin)
+        # the algorithmic bytes of the step (int8 codes, int32 row sums); the record format's own
+        # bytes (two e4m3 planes, 16-byte zero-point entries) ride along as a second reading
+        prep_bytes = sum(prepass_bytes(s.M, s.K) for s in specs) / len(lin)
+        prep_fmt_bytes = sum(record_prepass_bytes(s.M, s.K) for s in specs) / len(lin)
     prep_gbs = prep_bytes / (prep_avg * 1e-3) / 1e9
     gemm_hbm_bytes = sum(s.M * s.K + s.M * (s.K // 64) * 4 + s.N * s.K // 2 + 2 * s.N * (s.K // 64) * 2 +
                          (4 * s.N if s.bias else 0) + 4 * s.M * s.N for s in specs) / len(lin)
@@ -417,6 +450,11 @@ def run_bench(args):
     if args.workload in ("c3", "d3") and not args.shape:
         layer = layer_step(lin, specs, stream, flush, max(20, min(args.steps, 200)), decode)
 
+    targets = None
+    if not decode and not args.shape and not args.no_targets:
+        targets = measure_targets(device, stream, flush, clk, tensor_peak, hbm_gbs, peak_src)
+    clk.__exit__(None, None, None)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(lin, specs, args.cpu_seconds)
@@ -434,6 +472,8 @@ def run_bench(args):
                     "frac": round(gemm_tops / tensor_peak, 4),
                     "traffic": None if args.shape else recorded_traffic(args.workload),
                     "peak_source": f"{peak_src} bf16 burst x2 (fp8 nominal ratio) /2 (two e4m3 MACs per int8 MAC)",
+                    "int8_mma_sync": {"peak": MMA_SYNC_S8_TOPS, "frac": round(gemm_tops / MMA_SYNC_S8_TOPS, 4),
+                                      "unit": "TOPS", "source": MMA_SYNC_S8_SOURCE},
                     "gemm_us_per_launch": round(gemm_avg * 1e3, 3),
                     # small M is also read against HBM: the bytes a launch must move (codes, row
                     # sums, packed weights, scales and zeros, bias, y) over the same time
@@ -470,17 +510,22 @@ def run_bench(args):
         "dtype": ("int8 x u4 dp4a -> exact int32 blocks, f32 epilogue" if decode else
                   "e4m3xe4m3->f32 (exact int8 x u4 blocks), f32 epilogue"),
         "data": "synthetic (seeded Philox; no model weights)",
-        "config": {"workload": f"{args.workload}: {title}",
-                   "linears": [{"name": s.name, "M": s.M, "K": s.K, "N": s.N, "bias": s.bias} for s in specs],
-                   "tokens_per_step": M, "ops_per_step": ops_per_step,
-                   "l2": "flushed before every timed step (256 MiB written, then read back; outside the timed events)",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(args.workload, title, specs, world),
         "roofline": roofline,
         "prepass": ({"fused": "the few-token kernel quantizes the rows itself (one launch per linear)"}
                     if one_launch else
-                    {"bound": "hbm", "achieved": round(prep_gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
-                     "frac": round(prep_gbs / hbm_gbs, 4), "us_per_launch": round(prep_avg * 1e3, 3),
-                     "peak_source": peak_src}),
+                    dict({"bound": "hbm", "achieved": round(prep_gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
+                          "frac": round(prep_gbs / hbm_gbs, 4), "us_per_launch": round(prep_avg * 1e3, 3),
+                          "bytes_per_launch": int(prep_bytes),
+                          "bytes_rule": "M*K*(4 + 1 + 4/64) + 8*M: x read; int8 codes, int32 block row sums, "
+                                        "scale written",
+                          "peak_source": peak_src},
+                         **({} if decode else {"format_bytes": {
+                             "bytes_per_launch": int(prep_fmt_bytes),
+                             "achieved": round(prep_fmt_bytes / (prep_avg * 1e-3) / 1e9, 1),
+                             "frac": round(prep_fmt_bytes / (prep_avg * 1e-3) / 1e9 / hbm_gbs, 4),
+                             "rule": "bytes of the tensor-core record format: x read; two e4m3 nibble planes, "
+                                     "16-byte zero-point entries per 64 elements, scale written"}}))),
         "e2e": {"value": e2e_value, "unit": unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3 / e2e_steps, 4),
@@ -496,11 +541,94 @@ def run_bench(args):
     }
     if layer is not None:
         out["layer"] = layer
+    if targets is not None:
+        out["targets"] = targets
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ 7B-class kernel targets
+def measure_targets(device, stream, flush, clk, tensor_peak, hbm_gbs, peak_src, reps=20):
+    """The two kernel targets on the 7B-class workload (M 8192: K 4096 -> N 14336, then
+    K 14336 -> N 4096), timed alone with CUDA events on the launching stream, L2 flushed
+    before every launch (outside the events):
+      - the contraction (gemm_wide_kernel, through w4a8_linear_prepared) against the INT8
+        peaks: >= 50 % targeted;
+      - the activation pre-pass against HBM on the algorithmic bytes M*K*(4 + 1 + 4/64) + 8*M,
+        both as the fused call runs it (tensor-core records, w4a8_prepare_activations) and in
+        the API layout (int8 a_q, s_a, int32 row sums: w4a8_quant_pack): >= 70 % targeted."""
+    from w4a8_block_quantized_gb300 import binding, synth
+    title, specs = synth.workload("c4")
+    t0 = time.time()
+    rows = {"gemm": [], "prep": [], "quant_pack": []}
+    for spec in specs:
+        d = synth.make_linear(spec)
+        x = torch.from_numpy(d["x"]).to(device)
+        wq, sw, zw = (torch.from_numpy(d[k]).to(device) for k in ("wq", "s_w", "z_w"))
+        act = binding.prepare_activations(x, stream=stream)
+        pw = binding.prepare_weights(wq, sw, zw, stream=stream)
+        a_q, s_a, rs = binding.quant_pack(x, stream=stream)
+        y = torch.empty((spec.M, spec.N), dtype=torch.float32, device=device)
+        calls = {"gemm": lambda: binding.linear_prepared(act, pw, spec.M, spec.N, spec.K, y=y, stream=stream),
+                 "prep": lambda: binding.prepare_activations(x, act=act, stream=stream),
+                 "quant_pack": lambda: binding.quant_pack(x, a_q=a_q, a_scale=s_a, rowsum=rs, stream=stream)}
+        for name, fn in calls.items():
+            ms = []
+            for i in range(reps + 3):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                b.synchronize()
+                if i >= 3:
+                    ms.append(a.elapsed_time(b))
+            rows[name].append(statistics.fmean(ms) * 1e3)   # us per launch
+        del x, wq, sw, zw, act, pw, a_q, s_a, rs, y
+        torch.cuda.empty_cache()
+    t1 = time.time()
+    if binding.sync_status(stream) != 0:
+        raise RuntimeError("device status reported a timeout in the targets leg")
+    ops = sum(s.ops for s in specs)
+    g_us = sum(rows["gemm"])
+    g_tops = ops / (g_us * 1e-6) / 1e12
+    pbytes = sum(prepass_bytes(s.M, s.K) for s in specs)
+    fbytes = sum(record_prepass_bytes(s.M, s.K) for s in specs)
+
+    def hbm(bytes_, us):
+        gbs = bytes_ / (us * 1e-6) / 1e9
+        return round(gbs, 1), round(gbs / hbm_gbs, 4)
+
+    p_gbs, p_frac = hbm(pbytes, sum(rows["prep"]))
+    q_gbs, q_frac = hbm(pbytes, sum(rows["quant_pack"]))
+    f_gbs, f_frac = hbm(fbytes, sum(rows["prep"]))
+    return {
+        "workload": f"c4: {title}",
+        "timing": f"each kernel alone, {reps} launches per linear after 3 warm-up launches, L2 flushed before "
+                  "every launch (outside the events); figures over the two linears",
+        "gemm": {"kernel": "gemm_wide_kernel (tcgen05 kind::f8f6f4 + kind::f16 zero-point MMA, 256-token tiles)",
+                 "us_per_launch": [round(v, 2) for v in rows["gemm"]], "achieved": round(g_tops, 1),
+                 "unit": "TOPS", "target_frac": 0.5,
+                 "fp8_derived": {"peak": round(tensor_peak, 1), "frac": round(g_tops / tensor_peak, 4),
+                                 "met": g_tops / tensor_peak >= 0.5,
+                                 "source": f"{peak_src} bf16 burst x2 (fp8 nominal ratio) /2 (two e4m3 MACs "
+                                           "per int8 MAC)"},
+                 "int8_mma_sync": {"peak": MMA_SYNC_S8_TOPS, "frac": round(g_tops / MMA_SYNC_S8_TOPS, 4),
+                                   "met": g_tops / MMA_SYNC_S8_TOPS >= 0.5, "source": MMA_SYNC_S8_SOURCE}},
+        "prepass": {"kernel": "quant_kernel, tensor-core record output (the fused call's pre-pass)",
+                    "us_per_launch": [round(v, 2) for v in rows["prep"]], "achieved": p_gbs, "unit": "GB/s",
+                    "peak": hbm_gbs, "frac": p_frac, "target_frac": 0.7, "met": p_frac >= 0.7,
+                    "bytes": int(pbytes), "bytes_rule": "M*K*(4 + 1 + 4/64) + 8*M",
+                    "format_bytes": {"bytes": int(fbytes), "achieved": f_gbs, "frac": f_frac}},
+        "quant_pack": {"kernel": "quant_kernel, API layout (int8 a_q, fp32 s_a, int32 row sums)",
+                       "us_per_launch": [round(v, 2) for v in rows["quant_pack"]], "achieved": q_gbs,
+                       "unit": "GB/s", "peak": hbm_gbs, "frac": q_frac, "target_frac": 0.7, "met": q_frac >= 0.7,
+                       "bytes": int(pbytes), "bytes_rule": "M*K*(4 + 1 + 4/64) + 8*M"},
+        "clocks": clk.summary(t0, t1),
+    }
 
 
 # ------------------------------------------------------------------ decoder layer as a layer
@@ -685,8 +813,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int32/int64 blocks, f64 output", "data": "synthetic (seeded Philox)",
-        "config": {"workload": f"{args.workload}: {title}",
-                   "linears": [{"name": s.name, "M": s.M, "K": s.K, "N": s.N, "bias": s.bias} for s in specs]},
+        "config": workload_config(args.workload, title, specs, args.gpus),
         "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

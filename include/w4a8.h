@@ -209,10 +209,14 @@ size_t w4a8_prefill_workspace_bytes(int64_t M, int64_t N, int64_t K);
 size_t w4a8_debug_workspace_bytes(int64_t m_cnt, int64_t n_cnt, int64_t K);
 
 /* Debug: the exact per-block int32 accumulators acc[m][n][b] (section 3 eq. (2), first
- * sum) for the window m0 <= m < m0 + m_cnt, n0 <= n < n0 + n_cnt, computed by the same
- * tensor-core contraction as w4a8_linear.  acc: int32 [m_cnt][n_cnt][K/64], indexed by
- * the position inside the window.  The window must lie inside [0, M) x [0, N) and be
- * non-empty.  workspace: at least w4a8_debug_workspace_bytes(m_cnt, n_cnt, K) bytes. */
+ * sum) for the window m0 <= m < m0 + m_cnt, n0 <= n < n0 + n_cnt, computed by the
+ * tensor-core contraction that w4a8_linear runs for a problem of M tokens: the 256-token
+ * kernel (token records 256 wide, N = 256 MMAs) when M >= 4096, the 128-token kernel
+ * otherwise.  For M <= W4A8_DECODE_MAX_M w4a8_linear forms its block products on the CUDA
+ * cores instead; this call still runs the 128-token tensor-core contraction there.
+ * acc: int32 [m_cnt][n_cnt][K/64], indexed by the position inside the window.  The window
+ * must lie inside [0, M) x [0, N) and be non-empty.  workspace: at least
+ * w4a8_debug_workspace_bytes(m_cnt, n_cnt, K) bytes (one size for either kernel). */
 int w4a8_debug_block_acc(const int8_t *a_q, const uint8_t *wq, int64_t M, int64_t N, int64_t K,
                          int64_t m0, int64_t m_cnt, int64_t n0, int64_t n_cnt, int32_t *acc,
                          void *workspace, size_t workspace_bytes, void *stream);

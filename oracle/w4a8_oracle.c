@@ -19,7 +19,8 @@
  * Readings taken where the page is silent (each one is listed in the design notes):
  *   - activation scale s_a = absmax / 127 as an fp32 IEEE division, and the code is
  *     a_q = clamp(roundf(x / s_a), -127, 127) with an fp32 IEEE division and
- *     round-half-away-from-zero; an all-zero row gives s_a = 0 and a_q = 0;
+ *     round-half-away-from-zero; a row whose s_a is 0 (an all-zero row, or absmax / 127
+ *     underflowing to 0) gives a_q = 0;
  *   - one (s_w, z_w) fp16 pair per 64 consecutive K elements of one output row n;
  *     z_w is a real fp16 value, q is unsigned 0..15;
  *   - packed weights: byte wq[n][k/2] holds k even in its low nibble, k odd in
@@ -82,7 +83,9 @@ void oracle_quant_pack(const float *x, long M, long K,
         s_a[m] = scale;
         for (long k = 0; k < K; ++k) {
             int q = 0;
-            if (absmax > 0.0f) {
+            /* A row whose scale is 0 -- absmax 0, or absmax / 127 below half the smallest
+             * subnormal -- has no quotient to round; its codes are 0, as for a zero row. */
+            if (scale > 0.0f) {
 #if ORACLE_MUTANT == 5
                 float r = rintf(row[k] / scale);    /* mutant: ties to even */
 #else

@@ -54,6 +54,42 @@ def pin_quant_closed_forms(tag):
         assert np.array_equal(rs[r], exp_rs)
 
 
+def pin_quant_tiny_scales(tag):
+    """Rows whose scale sits in or below the subnormal range, in units u = 2^-149 (the
+    smallest fp32 subnormal), where every step is exact integer arithmetic on multiples of u:
+      - absmax 7u or 63u: absmax / 127 < u / 2 rounds to s_a = 0, and the row quantizes like
+        a zero row (codes 0, row sums 0);
+      - absmax 64u or 143u: absmax / 127 lies in (u/2, 3u/2), so s_a = u and each code is the
+        element's multiple of u, clamped to +-127 (143 -> 127);
+      - absmax 1e-38 and 1e-36 (s_a subnormal with 16 and 23 significant bits): a single
+        spike still maps to +-127 and s_a = RN(|v| / 127)."""
+    u = np.float32(2.0 ** -149)
+    K = 128
+    x = np.zeros((6, K), np.float32)
+    x[0, [3, 70]] = [7 * u, -5 * u]
+    x[1, [0, 1, 127]] = [-63 * u, 62 * u, u]
+    x[2, [5, 6, 64]] = [64 * u, -64 * u, 3 * u]
+    x[3, [0, 9, 10, 100]] = [143 * u, 71 * u, -100 * u, -u]
+    x[4, 17] = np.float32(1e-38)
+    x[5, 90] = np.float32(-1e-36)
+    a_q, s_a, rs = oracle.quant_pack(x, tag=tag)
+    assert s_a[0] == 0 and s_a[1] == 0
+    assert not a_q[:2].any() and not rs[:2].any()
+    assert s_a[2] == u and s_a[3] == u
+    e2 = np.zeros(K, np.int8)
+    e2[[5, 6, 64]] = [64, -64, 3]
+    e3 = np.zeros(K, np.int8)
+    e3[[0, 9, 10, 100]] = [127, 71, -100, -1]
+    assert np.array_equal(a_q[2], e2) and np.array_equal(a_q[3], e3)
+    assert np.array_equal(rs[2], [0, 3]) and np.array_equal(rs[3], [127 + 71 - 100, -1])
+    for r, j, v in ((4, 17, 1e-38), (5, 90, -1e-36)):
+        assert s_a[r] == np.float32(abs(np.float32(v))) / np.float32(127.0)
+        assert 0 < s_a[r] < np.float32(2.0 ** -126)
+        exp = np.zeros(K, np.int8)
+        exp[j] = 127 if v > 0 else -127
+        assert np.array_equal(a_q[r], exp)
+
+
 def pin_quant_invariants(tag):
     """On seeded workload-style rows: codes within +-127, the absmax element maps to
     +-127, the reconstruction error is at most half a step, and the per-64 sums are
@@ -238,6 +274,7 @@ ALL_PINS = [
     pin_half_decode,
     pin_quant_golden,
     pin_quant_closed_forms,
+    pin_quant_tiny_scales,
     pin_quant_invariants,
     pin_nibble_identity,
     pin_block_acc_matches_codes,

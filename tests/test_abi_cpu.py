@@ -192,25 +192,27 @@ def _align(v):
 def test_host_call_workspace_and_chunking(lib):
     """The host-buffer call's workspace: the device copies of x and y, then either the fused
     call's scratch (one chunk) or the prepared weights and one prepared-activation buffer per
-    compute stream (at most four), sized for the last, largest chunk.  A call is cut into at
-    most sixteen chunks of whole token tiles, each moving at least 8 MiB of x and y."""
+    compute stream (at most four), sized for the largest chunk.  A call is cut into at most
+    sixteen chunks of whole token tiles, each moving at least 8 MiB of x and y; the tiles are
+    spread evenly, so the first (tiles mod chunks) chunks take one tile more than the rest."""
     def plan(M, N, K):
         tw = 256 if M >= 4096 else 128
         chunks = 1 if M <= 8 else max(1, min(16, M // tw, M * (K + N) * 4 // (8 << 20)))
-        rows = (M // chunks) // tw * tw if chunks > 1 else M
-        return chunks, M - (chunks - 1) * rows
+        tiles = -(-M // tw)
+        largest = min((tiles // chunks + (tiles % chunks > 0)) * tw, M)
+        return chunks, largest
 
     def base(M, N, K):
         return _align(_align(M * K * 4) + M * N * 4)
 
-    cases = [  # (M, N, K, chunks, rows of the last chunk)
+    cases = [  # (M, N, K, chunks, rows of the largest chunk)
         (512, 3072, 1024, 1, 512),        # the pp512 linear: 8 MiB in all, one chunk
         (700, 200, 256, 1, 700),
         (3, 256, 1024, 1, 3),
-        (1500, 2560, 1024, 2, 860),
-        (2048, 4096, 1024, 5, 512),
-        (1000, 8192, 1024, 4, 616),
-        (2048, 4096, 2048, 6, 768),
+        (1500, 2560, 1024, 2, 768),       # 12 tiles: 6 + 6 (the second ragged)
+        (2048, 4096, 1024, 5, 512),       # 16 tiles: 4 + 3 + 3 + 3 + 3
+        (1000, 8192, 1024, 4, 256),       # 8 tiles: 2 each
+        (2048, 4096, 2048, 6, 384),       # 16 tiles: 3 3 3 3 2 2
     ]
     for M, N, K, chunks, last in cases:
         assert plan(M, N, K) == (chunks, last), (M, N, K)

@@ -51,6 +51,57 @@ def test_quant_pack_golden_and_degenerate_rows():
     assert np.array_equal(gr.cpu().numpy(), rs)
 
 
+def _tiny_scale_rows(K, rng):
+    """Rows whose scale is subnormal without a finite reciprocal (absmax 1e-38, deep
+    subnormal multiples of u = 2^-149 where |x / s| can pass 127), subnormal with one
+    (1e-36), or rounds to 0 (absmax 1e-44 and 63u), next to an ordinary row."""
+    u = np.float32(2.0 ** -149)
+    rows = [rng.standard_normal(K) * np.float32(1e-38 / 4), rng.standard_normal(K) * np.float32(1e-36 / 4),
+            rng.integers(-143, 144, K) * u, rng.integers(-63, 64, K) * u, np.full(K, np.float32(1e-44)),
+            rng.standard_normal(K)]
+    x = np.stack([np.asarray(r, np.float32) for r in rows])
+    x[0, 1] = np.float32(1e-38)
+    x[2, 2] = 143 * u
+    return x
+
+
+@pytest.mark.parametrize("K", [1024, 4096, 20480])
+def test_quant_tiny_scales_bitexact(K):
+    """Scales in and below the subnormal range through the pre-pass (register-resident rows,
+    the 512-thread rows and the two-pass long rows): codes, scales and row sums bit for bit;
+    the fused call (operand records) within tolerance and equal to the separate calls."""
+    rng = np.random.default_rng(K)
+    # 16 rows, so that the linear takes the tensor-core form
+    x = np.concatenate([_tiny_scale_rows(K, rng), rng.standard_normal((10, K)).astype(np.float32)])
+    a_q, s_a, rs = B().quant_pack(to_dev(x))
+    ra, rsa, rrs = oracle.quant_pack(x)
+    assert np.array_equal(s_a.cpu().numpy(), rsa)
+    assert np.array_equal(a_q.cpu().numpy(), ra)
+    assert np.array_equal(rs.cpu().numpy(), rrs)
+    assert rsa[3] == 0 and rsa[4] == 0 and not ra[3:5].any()
+    d = synth.random_small(x.shape[0], K, 100, seed=K, bias=True)
+    d["x"] = x
+    y_fused, y_sep = _run_both(d)
+    y_ref, bound, _, _, _ = oracle.prefill_linear(x, d["wq"], d["s_w"], d["z_w"], d["bias"])
+    check_y(y_fused, y_ref, bound, f"tiny scales K={K}")
+    assert torch.equal(y_fused, y_sep)
+
+
+@pytest.mark.parametrize("K", [1024, 2048])
+def test_decode_quantizer_tiny_scales(K):
+    """The few-token kernel's own quantizer (M * K <= 16384) on the same rows: its outputs
+    equal those of the pre-pass + kernel path, whose codes match the oracle bit for bit."""
+    rng = np.random.default_rng(K + 1)
+    x = _tiny_scale_rows(K, rng)
+    d = synth.random_small(x.shape[0], K, 300, seed=K + 1, bias=True)
+    d["x"] = x
+    y_fused, y_sep = _run_both(d)
+    assert B().prefill_workspace_bytes(x.shape[0], 300, K) == 0   # the kernel quantized itself
+    y_ref, bound, _, _, _ = oracle.prefill_linear(x, d["wq"], d["s_w"], d["z_w"], d["bias"])
+    check_y(y_fused, y_ref, bound, f"decode tiny scales K={K}")
+    assert torch.equal(y_fused, y_sep)
+
+
 # ------------------------------------------------------------------ block accumulators
 def _acc_case(a_q, q, m0=0, mc=None, n0=0, nc=None):
     N = q.shape[0]
@@ -100,6 +151,31 @@ def test_block_acc_windows():
     _acc_case(a, q, m0=5, mc=131, n0=3, nc=300)
     _acc_case(a, q, m0=399, mc=1, n0=699, nc=1)
     _acc_case(a, q, m0=128, mc=200, n0=256, nc=444)
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 129, 256), (4097, 200, 128), (4352, 300, 192), (4100, 1, 64)])
+def test_block_acc_wide_contraction(M, N, K):
+    """M >= 4096 runs the 256-token kernel (N = 256 MMAs): its per-block accumulators, bit for
+    bit, over whole problems with ragged token tails (4097 and 4100 leave 1 and 4 rows in the
+    last tile; 4352 = 17 full tiles) and ragged or single weight rows."""
+    rng = np.random.default_rng(M + 7 * N + K)
+    a = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    a[:3] = np.array([127, -127, -128], np.int8)[:, None]   # the extremes, in whole rows
+    q = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+    q[0] = 15
+    _acc_case(a, q)
+
+
+def test_block_acc_wide_windows():
+    """Windows of an 8192-token problem (the 256-token kernel): crossing token-tile and
+    weight-tile boundaries, the last rows and columns, a single accumulator."""
+    rng = np.random.default_rng(17)
+    M, N, K = 8192, 700, 1024
+    a = rng.integers(-128, 128, size=(M, K)).astype(np.int8)
+    q = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+    _acc_case(a, q, m0=3900, mc=600, n0=100, nc=300)
+    _acc_case(a, q, m0=8000, mc=192, n0=572, nc=128)
+    _acc_case(a, q, m0=8191, mc=1, n0=699, nc=1)
 
 
 # ------------------------------------------------------------------ full linear
@@ -174,9 +250,12 @@ def test_workload_c4_sampled():
         assert np.array_equal(a_q.cpu().numpy(), ra)
         assert np.array_equal(s_a.cpu().numpy(), rsa)
         assert np.array_equal(rs.cpu().numpy(), rrs)
-        got = B().debug_block_acc(a_q, g["wq"], spec.N, 4000, 160, spec.N - 300, 300).cpu().numpy()
-        ref = oracle.block_acc(ra, d["wq"], spec.N, 4000, 160, spec.N - 300, 300)
-        assert np.array_equal(got, ref)
+        # the 256-token contraction the linear ran, on windows across tiles and at both ends
+        for m0, mc, n0, nc in ((4000, 160, spec.N - 300, 300), (0, 256, 0, 128), (8060, 132, 200, 260)):
+            got = B().debug_block_acc(a_q, g["wq"], spec.N, m0, mc, n0, nc).cpu().numpy()
+            ref = oracle.block_acc(ra, d["wq"], spec.N, m0, mc, n0, nc)
+            assert np.array_equal(got, ref), f"c4/{spec.name} window {(m0, mc, n0, nc)}"
+
         del g, y, ws
         torch.cuda.empty_cache()
 
@@ -376,6 +455,30 @@ def test_decode_model_shapes_full(K, N):
     assert torch.equal(b.prefill_linear_noalloc(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"]), y)
 
 
+@pytest.mark.parametrize("M,K,N", [(1, 1088, 257), (3, 6144, 130), (8, 2048, 301), (2, 192, 5), (1, 4096, 14336)])
+def test_decode_offset_scale_views(M, K, N):
+    """s_w and z_w as views that start 2 and 6 bytes into their allocations (so no span of a
+    tile's rows begins or ends on a 16-byte boundary): the outputs equal the call on fresh
+    arrays bit for bit and lie within tolerance of the oracle."""
+    b = B()
+    d = synth.random_small(M, K, N, seed=13 * M + K + N, bias=True)
+    g = inputs_to_dev(d)
+    y = b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"])
+    nel = N * (K // 64)
+    sbuf = torch.zeros(nel + 8, dtype=torch.float16, device=dev())
+    zbuf = torch.zeros(nel + 8, dtype=torch.float16, device=dev())
+    sw = sbuf[1:1 + nel].view(N, K // 64)
+    zw = zbuf[3:3 + nel].view(N, K // 64)
+    sw.copy_(g["s_w"])
+    zw.copy_(g["z_w"])
+    assert sw.data_ptr() % 16 == 2 and zw.data_ptr() % 16 == 6
+    y_off = b.prefill_linear(g["x"], g["wq"], sw, zw, g["bias"])
+    assert torch.equal(y_off, y)
+    y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
+    check_y(y_off, y_ref, bound, f"offset views {M}x{K}->{N}")
+    assert b.sync_status() == 0
+
+
 def test_decode_boundary_tokens():
     """8 tokens take the weight-streaming form, 9 the tensor-core form: both within the
     tolerance of the same definition on the same rows."""
@@ -485,6 +588,39 @@ def test_binding_checks_every_tensor_before_launch():
     check_y(y, y_ref, bound, "after rejected calls")
     assert b.sync_status() == 0
 
+
+
+def test_temporary_workspace_follows_the_call_stream(monkeypatch):
+    """A call on a stream that is not the current one, with no workspace given: the binding's
+    temporary workspace is held for that stream's work, so a block allocated on the current
+    stream right after the call is not the same memory while the call is still queued."""
+    b = B()
+    M, K, N = 512, 1024, 640
+    d = synth.random_small(M, K, N, seed=8, bias=True)
+    g = inputs_to_dev(d)
+    ref = b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"])
+    torch.cuda.synchronize()
+    made = []
+    orig = b.workspace
+
+    def spy(nbytes, device):
+        t = orig(nbytes, device)
+        made.append(t.data_ptr())
+        return t
+
+    monkeypatch.setattr(b, "workspace", spy)
+    s = torch.cuda.Stream()
+    y = torch.empty_like(ref)
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(50_000_000)            # keeps the side stream busy for some milliseconds
+    b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"], y=y, stream=s)
+    assert len(made) == 1
+    other = torch.empty(b.prefill_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev())
+    assert other.data_ptr() != made[0], "the temporary workspace was handed out while still in use"
+    other.fill_(0xA5)
+    s.synchronize()
+    assert torch.equal(y, ref)
+    assert b.sync_status() == 0
 
 
 # ------------------------------------------------------------------ host-buffer call

@@ -148,10 +148,17 @@ def _weights(wq, w_scale, w_zero, N: int, K: int, device):
     _arg(w_zero, torch.float16, (N, K // 64), "w_zero", device)
 
 
-def _ws(ws, need: int, device):
-    """The caller's workspace (any dtype: its size in bytes is what the library is told)."""
+def _ws(ws, need: int, device, stream=None):
+    """The caller's workspace (any dtype: its size in bytes is what the library is told), or
+    a temporary one.  A temporary is dropped when the call returns, while the library's work
+    on it is still queued on `stream`; the caching allocator is told about that stream
+    (record_stream), so it does not hand the block to other work before that work is done
+    (it otherwise tracks only the current stream, on which the block was allocated)."""
     if ws is None:
-        return workspace(need, device)
+        t = workspace(need, device)
+        if stream is not None:
+            t.record_stream(stream)
+        return t
     _arg(ws, None, None, "ws", device)
     return ws
 
@@ -213,7 +220,7 @@ def linear(a_q, a_scale, rowsum, wq, w_scale, w_zero, bias=None, y=None, ws=None
     _arg(bias, torch.float32, (N,), "bias", dev)
     y = torch.empty((M, N), dtype=torch.float32, device=dev) if y is None else y
     _arg(y, torch.float32, (M, N), "y", dev)
-    ws = _ws(ws, linear_workspace_bytes(M, N, K), dev)
+    ws = _ws(ws, linear_workspace_bytes(M, N, K), dev, stream)
     rc = load().w4a8_linear(_ptr(a_q), _ptr(a_scale), _ptr(rowsum), _ptr(wq), _ptr(w_scale), _ptr(w_zero),
                             _ptr(bias), _ptr(y), M, N, K, _ptr(ws), _nbytes(ws), _stream(stream))
     _check(rc, "w4a8_linear")
@@ -244,7 +251,7 @@ def prefill_linear(x, wq, w_scale, w_zero, bias=None, y=None, ws=None, stream=No
     M, N, K = _prefill_args(x, wq, w_scale, w_zero, bias)
     y = torch.empty((M, N), dtype=torch.float32, device=x.device) if y is None else y
     _arg(y, torch.float32, (M, N), "y", x.device)
-    ws = _ws(ws, prefill_workspace_bytes(M, N, K), x.device)
+    ws = _ws(ws, prefill_workspace_bytes(M, N, K), x.device, stream)
     rc = load().w4a8_prefill_linear(_ptr(x), _ptr(wq), _ptr(w_scale), _ptr(w_zero), _ptr(bias), _ptr(y),
                                     M, N, K, _ptr(ws), _nbytes(ws), _stream(stream))
     _check(rc, "w4a8_prefill_linear")
@@ -298,7 +305,7 @@ def prefill_linear_host(x, wq, w_scale, w_zero, bias=None, y=None, ws=None, stre
         y = torch.empty((M, N), dtype=torch.float32)
         y = y.pin_memory() if y.numel() else y
     _host(y, torch.float32, (M, N), "y")
-    ws = _ws(ws, prefill_host_workspace_bytes(M, N, K), dev)
+    ws = _ws(ws, prefill_host_workspace_bytes(M, N, K), dev, stream)
     rc = load().w4a8_prefill_linear_host(_ptr(x), _ptr(wq), _ptr(w_scale), _ptr(w_zero), _ptr(bias), _ptr(y),
                                          M, N, K, _ptr(ws), _nbytes(ws), _stream(stream))
     _check(rc, "w4a8_prefill_linear_host")
@@ -352,7 +359,7 @@ def prefill_linear_ex(x, wq, w_scale, w_zero, bias=None, y=None, out_dtype=None,
     """w4a8_prefill_linear_ex: the fused call with the epilogue clamp and an fp32 or bf16 y."""
     M, N, K = _prefill_args(x, wq, w_scale, w_zero, bias)
     y, code = _out(y, (M, N), x.device, out_dtype if y is None else y.dtype)
-    ws = _ws(ws, prefill_workspace_bytes(M, N, K), x.device)
+    ws = _ws(ws, prefill_workspace_bytes(M, N, K), x.device, stream)
     rc = load().w4a8_prefill_linear_ex(_ptr(x), _ptr(wq), _ptr(w_scale), _ptr(w_zero), _ptr(bias), _ptr(y), code,
                                        float(clamp[0]), float(clamp[1]), M, N, K, _ptr(ws), _nbytes(ws),
                                        _stream(stream))
@@ -369,7 +376,7 @@ def linear_ex(a_q, a_scale, rowsum, wq, w_scale, w_zero, bias=None, y=None, out_
     _weights(wq, w_scale, w_zero, N, K, dev)
     _arg(bias, torch.float32, (N,), "bias", dev)
     y, code = _out(y, (M, N), dev, out_dtype if y is None else y.dtype)
-    ws = _ws(ws, linear_workspace_bytes(M, N, K), dev)
+    ws = _ws(ws, linear_workspace_bytes(M, N, K), dev, stream)
     rc = load().w4a8_linear_ex(_ptr(a_q), _ptr(a_scale), _ptr(rowsum), _ptr(wq), _ptr(w_scale), _ptr(w_zero),
                                _ptr(bias), _ptr(y), code, float(clamp[0]), float(clamp[1]), M, N, K, _ptr(ws),
                                _nbytes(ws), _stream(stream))
@@ -424,7 +431,7 @@ def debug_block_acc(a_q, wq, N, m0=0, m_cnt=None, n0=0, n_cnt=None, ws=None, str
     if not (0 <= m0 and 0 <= m_cnt and m0 + m_cnt <= M and 0 <= n0 and 0 <= n_cnt and n0 + n_cnt <= N):
         raise ValueError(f"window rows [{m0}, {m0}+{m_cnt}) x cols [{n0}, {n0}+{n_cnt}) outside [{M}] x [{N}]")
     acc = torch.empty((m_cnt, n_cnt, K // 64), dtype=torch.int32, device=a_q.device)
-    ws = _ws(ws, debug_workspace_bytes(m_cnt, n_cnt, K), a_q.device)
+    ws = _ws(ws, debug_workspace_bytes(m_cnt, n_cnt, K), a_q.device, stream)
     rc = load().w4a8_debug_block_acc(_ptr(a_q), _ptr(wq), M, N, K, m0, m_cnt, n0, n_cnt, _ptr(acc),
                                      _ptr(ws), _nbytes(ws), _stream(stream))
     _check(rc, "w4a8_debug_block_acc")

@@ -212,9 +212,11 @@ size_t w4a8_prefill_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return prefill_ws(M, N, K);
 }
 
+// Sized for the wider token records, which never take less room than the 128-token ones, so
+// one size serves the window whatever the full problem's M selects.
 size_t w4a8_debug_workspace_bytes(int64_t m_cnt, int64_t n_cnt, int64_t K) {
     if (check_shape(m_cnt, n_cnt, K) != W4A8_OK || m_cnt == 0 || n_cnt == 0) return static_cast<size_t>(-1);
-    return act_layout(m_cnt, K, false, kTileT).total + w_layout(n_cnt, K).total;
+    return act_layout(m_cnt, K, false, 256).total + w_layout(n_cnt, K).total;
 }
 
 size_t w4a8_prepared_activations_bytes(int64_t M, int64_t K) {
@@ -446,9 +448,10 @@ int w4a8_debug_block_acc(const int8_t* a_q, const uint8_t* wq, int64_t M, int64_
     if (!a_q || !wq || !acc) return W4A8_ERR_ARG;
     if (m0 < 0 || n0 < 0 || m_cnt <= 0 || n_cnt <= 0 || m0 + m_cnt > M || n0 + n_cnt > N) return W4A8_ERR_SHAPE;
     if (!aligned(a_q, 16) || !aligned(wq, 16) || !aligned(acc, 4)) return W4A8_ERR_ALIGN;
-    const ActLayout L = act_layout(m_cnt, K, false, kTileT);
+    // the token-record width (and so the contraction kernel) that a linear of M tokens runs
+    const ActLayout L = act_layout(m_cnt, K, false, token_tile(M));
     const WLayout W = w_layout(n_cnt, K);
-    if (!workspace || workspace_bytes < L.total + W.total) return W4A8_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < w4a8_debug_workspace_bytes(m_cnt, n_cnt, K)) return W4A8_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return W4A8_ERR_ALIGN;
     DeviceInfo* d = nullptr;
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
@@ -462,6 +465,7 @@ int w4a8_debug_block_acc(const int8_t* a_q, const uint8_t* wq, int64_t M, int64_
     p.K = K;
     p.row0 = m0;
     p.trec = ws + L.rec;
+    p.tw = L.tw;
     p.wq = wq;
     p.n_first = n0;
     p.N = n_cnt;
@@ -472,6 +476,7 @@ int w4a8_debug_block_acc(const int8_t* a_q, const uint8_t* wq, int64_t M, int64_
     g.N = n_cnt;
     g.K = K;
     g.trec = ws + L.rec;
+    g.tw = L.tw;
     g.wrec = wrec;
     g.acc = acc;
     g.status = d->status;
@@ -571,20 +576,34 @@ constexpr int64_t kHostChunkBytes = int64_t(8) << 20;
 
 struct HostPlan {
     int chunks = 1;
-    int tw = 128;      // token-record width of the uncut call
-    int64_t rows = 0;  // rows of every chunk but the last, which takes the remainder
+    int tw = 128;          // token-record width of the uncut call
+    int64_t M = 0;
+    int64_t base = 0;      // token tiles of a chunk; the first `extra` chunks take one more
+    int64_t extra = 0;
     size_t y_off = 0, ws_off = 0, act_stride = 0, total = 0;  // x at offset 0
+
+    // first row and row count of chunk c (whole tiles; the last chunk ends at M)
+    void chunk(int c, int64_t* r0, int64_t* rows) const {
+        const int64_t t0 = c * base + std::min<int64_t>(c, extra);
+        const int64_t tiles = base + (c < extra ? 1 : 0);
+        *r0 = t0 * tw;
+        *rows = std::min<int64_t>(tiles * tw, M - *r0);
+    }
 };
 
 HostPlan host_plan(int64_t M, int64_t N, int64_t K) {
     HostPlan h;
     h.tw = token_tile(M);
+    h.M = M;
     if (!few_tokens(M, K)) {
         const int64_t by_rows = M / h.tw;
         const int64_t by_bytes = M * (K + N) * 4 / kHostChunkBytes;
         h.chunks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({kHostChunks, by_rows, by_bytes})));
     }
-    h.rows = h.chunks > 1 ? (M / h.chunks) / h.tw * h.tw : M;
+    // the token tiles spread evenly: chunks differ by at most one tile
+    const int64_t tiles = (M + h.tw - 1) / h.tw;
+    h.base = tiles / h.chunks;
+    h.extra = tiles % h.chunks;
     h.y_off = align_ws(static_cast<size_t>(M) * static_cast<size_t>(K) * 4u);
     h.ws_off = align_ws(h.y_off + static_cast<size_t>(M) * static_cast<size_t>(N) * 4u);
     if (h.chunks == 1) {
@@ -592,9 +611,10 @@ HostPlan host_plan(int64_t M, int64_t N, int64_t K) {
         return h;
     }
     // prepared weights, then one prepared-activation buffer per compute stream, sized for the
-    // last (largest) chunk; a stream's chunks run in order, so they can share one
-    const int64_t last = M - (h.chunks - 1) * h.rows;
-    h.act_stride = act_layout(last, K, true, h.tw).total;
+    // largest chunk (the first one); a stream's chunks run in order, so they can share one
+    int64_t r0, largest;
+    h.chunk(0, &r0, &largest);
+    h.act_stride = act_layout(largest, K, true, h.tw).total;
     h.total = h.ws_off + w_layout(N, K).total + static_cast<size_t>(std::min(h.chunks, kHostStreams)) * h.act_stride;
     return h;
 }
@@ -720,8 +740,8 @@ int w4a8_prefill_linear_host(const float* x_host, const uint8_t* wq, const uint1
         ok = launch_pack(p, st) == cudaSuccess && cudaEventRecord(r->weights, st) == cudaSuccess;
     }
     for (int c = 0; ok && c < h.chunks; ++c) {
-        const int64_t r0 = c * h.rows;
-        const int64_t rows = c + 1 < h.chunks ? h.rows : M - r0;
+        int64_t r0, rows;
+        h.chunk(c, &r0, &rows);
         const size_t xo = static_cast<size_t>(r0) * static_cast<size_t>(K);
         const size_t yo = static_cast<size_t>(r0) * static_cast<size_t>(N);
         const int si = c % kHostStreams;

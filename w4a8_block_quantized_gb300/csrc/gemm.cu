@@ -402,6 +402,9 @@ static_assert(kZeroBytes >= kTN * 16, "zero half of the token-side zero-point op
 static_assert(kStages % kIssuers == 0 && kIssuers <= 3, "each stage must have one issuer warp at every phase");
 }  // namespace wide
 
+// DEBUG: no zero-point MMA and no register split; the epilogue stores each block's exact
+// integer accumulator (acc * 2^-9 in TMEM, times 512) instead of folding it into y.
+template <bool DEBUG>
 __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs args) {
     namespace W = wide;
     extern __shared__ uint8_t smem_raw[];
@@ -434,9 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
         *abort_flag = 0u;
         fence_barrier_init();
     }
-    for (int i = threadIdx.x; i < kZeroBytes / 16; i += kThreads)
-        reinterpret_cast<uint4*>(smem + W::kOffZero)[i] = make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
+    if (!DEBUG) {
+        for (int i = threadIdx.x; i < kZeroBytes / 16; i += kThreads)
+            reinterpret_cast<uint4*>(smem + W::kOffZero)[i] = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
@@ -448,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
     griddep_wait();
 
     if (warp < 4) {
-        regs_dec<kRegsLow>();
+        if (!DEBUG) regs_dec<kRegsLow>();
         if (warp == 0) {
             // -------------------------------------------------------- producer
             if (lane == 0) {
@@ -501,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
                     mma_f8f6f4(d, dW + 2, dT + 2, idesc, 1u);
                     mma_f8f6f4(d, dW, dT + 4, idesc, 1u);
                     mma_f8f6f4(d, dW + 2, dT + 6, idesc, 1u);
-                    mma_f16(d, dAx0 + o - (o << 16), dBx0 + o - (o << 16), idesc, 1u);
+                    if (!DEBUG) mma_f16(d, dAx0 + o - (o << 16), dBx0 + o - (o << 16), idesc, 1u);
                     mma_commit(&tfull[buf]);
                 }
                 __syncwarp();
@@ -512,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        regs_inc<kRegsHigh>();
+        if (!DEBUG) regs_inc<kRegsHigh>();
         const int q = warp & 3, h = (warp - 4) >> 2;  // TMEM lane quarter, 64-column quarter
         const int row = q * 32 + lane;
         const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 64);
@@ -525,14 +530,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
             tile_at(first + static_cast<int64_t>(i) * gridDim.x, tiles_t, tiles_w, tt, tw);
             const int64_t mt0 = tt * W::kTN + h * 64;
             const int64_t n = tw * kTileW + row;
-            const float* sct = args.sc + static_cast<int64_t>(tw) * nb * kTileW + row;
-            float ns = __ldg(sct);
+            const float* sct = DEBUG ? nullptr : args.sc + static_cast<int64_t>(tw) * nb * kTileW + row;
+            float ns = DEBUG ? 0.0f : __ldg(sct);
             float y[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) y[c] = 0.0f;
+            // debug: this block's exact accumulators of 32 token columns starting at c0
+            auto store_acc = [&](const uint32_t (&v)[32], int c0, uint32_t b) {
+                if (n >= args.N) return;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int64_t m = mt0 + c0 + c;
+                    if (m < args.M)
+                        args.acc[(m * args.N + n) * nb + b] = static_cast<int32_t>(__uint_as_float(v[c]) * 512.0f);
+                }
+            };
             for (uint32_t b = 0; b < nb; ++b, ++g) {
                 const float sb = ns;
-                if (b + 1 < nb) ns = __ldg(sct + (b + 1) * kTileW);
+                if (!DEBUG && b + 1 < nb) ns = __ldg(sct + (b + 1) * kTileW);
                 const uint32_t buf = g & 1u;
                 if (!epi_all(mbar_wait(&tfull[buf], (g >> 1) & 1, ctl))) {
                     ok = false;
@@ -545,8 +560,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
                 tmem_ld_32x32b_x16(tb, v);
                 tmem_ld_32x32b_x16(tb + 16, v + 16);
                 tmem_wait_ld();
+                if (DEBUG) {
+                    store_acc(v, 0, b);
+                } else {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) y[c] = fmaf(sb, __uint_as_float(v[c]), y[c]);
+                    for (int c = 0; c < 32; ++c) y[c] = fmaf(sb, __uint_as_float(v[c]), y[c]);
+                }
                 tmem_ld_32x32b_x16(tb + 32, v);
                 tmem_ld_32x32b_x16(tb + 48, v + 16);
                 tmem_wait_ld();
@@ -554,11 +573,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
                 tc_fence_before();
                 epi_bar_sync();
                 if (warp == 4 && lane == 0 && g + W::kNBuf < total) mbar_arrive(&full[(g + W::kNBuf) % W::kStages]);
+                if (DEBUG) {
+                    store_acc(v, 32, b);
+                } else {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) y[32 + c] = fmaf(sb, __uint_as_float(v[c]), y[32 + c]);
+                    for (int c = 0; c < 32; ++c) y[32 + c] = fmaf(sb, __uint_as_float(v[c]), y[32 + c]);
+                }
             }
             if (!ok) break;
-            if (n < args.N) {
+            if (!DEBUG && n < args.N) {
                 const float bn = args.bias ? args.bias[n] : 0.0f;
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
@@ -620,12 +643,14 @@ cudaError_t launch(Kernel kernel, int smem_bytes, bool* attr_done, int64_t tiles
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& a, bool debug, int num_sms, cudaStream_t s) {
-    static bool attr_done[3][64] = {};
+    static bool attr_done[4][64] = {};
     if (num_sms < 1) return cudaErrorInvalidValue;
     const int64_t tiles_w = (a.N + kTileW - 1) / kTileW;
-    if (a.tw == wide::kTN && !debug)
-        return launch(gemm_wide_kernel, wide::kSmemBytes, attr_done[2], ((a.M + wide::kTN - 1) / wide::kTN) * tiles_w, a,
-                      num_sms, s);
+    if (a.tw == wide::kTN) {
+        const int64_t tiles = ((a.M + wide::kTN - 1) / wide::kTN) * tiles_w;
+        return debug ? launch(gemm_wide_kernel<true>, wide::kSmemBytes, attr_done[3], tiles, a, num_sms, s)
+                     : launch(gemm_wide_kernel<false>, wide::kSmemBytes, attr_done[2], tiles, a, num_sms, s);
+    }
     if (a.tw != kTileT) return cudaErrorInvalidValue;
     const int64_t tiles = ((a.M + kTileT - 1) / kTileT) * tiles_w;
     return debug ? launch(gemm_kernel<true>, kSmemBytes, attr_done[1], tiles, a, num_sms, s)

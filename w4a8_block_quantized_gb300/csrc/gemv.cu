@@ -13,10 +13,9 @@
 // Persistent CTAs, one per SM, each walking row tiles t = blockIdx.x, blockIdx.x + grid, ...
 //   warp 8       producer: per tile three bulk copies into a ring of shared-memory stages --
 //                the tile's packed rows (contiguous: rows are K/2 bytes apart) and the
-//                16-byte-aligned spans of memory holding its s_w and z_w rows (a span may
-//                start and end up to 15 bytes outside the rows; a 16-byte granule of device
-//                memory never straddles a page, so those bytes are always readable and are
-//                simply not used).
+//                16-byte-aligned interiors of its s_w and z_w rows (the few elements before
+//                and after an interior are read from global memory by the consumers, so
+//                nothing outside the caller's arrays is touched).
 //   warps 0-7    consumers.  A tile of TR >= 8 rows gives each warp TR/8 rows; a tile of
 //                TR < 8 rows gives each row 8/TR warps that split its K chunks.  A lane owns
 //                one 64-block of a row in every chunk of 32 blocks (2048 weights).
@@ -129,8 +128,6 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
-__device__ __forceinline__ float half_bits_to_float(uint16_t h) { return __half2float(__ushort_as_half(h)); }
-
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -155,15 +152,35 @@ __device__ __forceinline__ float lds_f32(uint32_t addr) {
     return v;
 }
 
-// The 16-byte-aligned span of device memory holding elements [e0, e1) of a fp16 array: its
-// start, its length and the offset of element e0 inside it.
-__device__ __forceinline__ void half_span(const uint16_t* base, int64_t e0, int64_t e1, const uint8_t*& src,
-                                          uint32_t& bytes, uint32_t& skew) {
+// Elements [e0, e1) of a fp16 array, staged with one bulk copy of their 16-byte-aligned
+// interior.  The slot keeps the array's alignment: element e0 sits `skew` bytes into it
+// (its address mod 16), and the interior -- bytes [lo, hi) counted from element e0 -- lands
+// at slot offset skew + lo.  The at most 7 elements before and 7 after the interior (byte
+// offsets outside [lo, hi)) are not copied; readers load them from global memory, so no copy
+// touches memory outside the caller's array.  An interior shorter than 16 bytes is empty
+// (lo == hi, bytes == 0).
+struct HalfSpan {
+    const uint8_t* src;  // the interior's first byte
+    uint32_t bytes, skew, lo, hi;
+};
+
+__device__ __forceinline__ HalfSpan half_span(const uint16_t* base, int64_t e0, int64_t e1) {
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(base + e0), a1 = reinterpret_cast<uintptr_t>(base + e1);
-    const uintptr_t s0 = a0 & ~uintptr_t(15), s1 = (a1 + 15) & ~uintptr_t(15);
-    src = reinterpret_cast<const uint8_t*>(s0);
-    bytes = static_cast<uint32_t>(s1 - s0);
-    skew = static_cast<uint32_t>(a0 - s0);
+    const uintptr_t i0 = (a0 + 15) & ~uintptr_t(15), i1 = a1 & ~uintptr_t(15);
+    HalfSpan h;
+    h.src = reinterpret_cast<const uint8_t*>(i0);
+    h.bytes = i1 > i0 ? static_cast<uint32_t>(i1 - i0) : 0u;
+    h.skew = static_cast<uint32_t>(a0 & 15);
+    h.lo = static_cast<uint32_t>(i0 - a0);
+    h.hi = h.lo + h.bytes;
+    return h;
+}
+
+// fp16 element at byte offset e of a staged span (slot base `slot`, element e0 at `gsrc`):
+// from shared memory inside the copied interior, else from global memory.
+__device__ __forceinline__ float span_elem(uint32_t slot, const HalfSpan& h, const uint16_t* gsrc, uint32_t e) {
+    const uint16_t v = e - h.lo < h.hi - h.lo ? lds16(slot + h.skew + e) : __ldg(gsrc + e / 2);
+    return __half2float(__ushort_as_half(v));
 }
 
 // A float code (an exact integer in [-127, 127]) as a word whose low byte is the code in two's
@@ -238,18 +255,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (warp == kCW) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            auto tile_src = [&](uint32_t i, const uint8_t*& w, uint32_t& wbytes, const uint8_t*& ss, uint32_t& sbytes,
-                                const uint8_t*& zs, uint32_t& zbytes) {
-                const int64_t n0 = (blockIdx.x + static_cast<int64_t>(i) * gridDim.x) * tr;
-                const int64_t rows = N - n0 < tr ? N - n0 : tr;
-                uint32_t skew;
-                w = a.wq + n0 * (K / 2);
-                wbytes = static_cast<uint32_t>(rows * (K / 2));
-                half_span(a.s_w, n0 * nb, (n0 + rows) * nb, ss, sbytes, skew);
-                half_span(a.z_w, n0 * nb, (n0 + rows) * nb, zs, zbytes, skew);
-            };
-            const uint8_t *w, *ss, *zs;
-            uint32_t wbytes, sbytes, zbytes;
             griddep_wait();
             if (a.x) {
                 // the rows to quantize go first: every CTA reads them, ahead of its weights
@@ -266,12 +271,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     ok = false;
                     break;
                 }
-                tile_src(i, w, wbytes, ss, sbytes, zs, zbytes);
+                const int64_t n0 = (blockIdx.x + static_cast<int64_t>(i) * gridDim.x) * tr;
+                const int64_t rows = N - n0 < tr ? N - n0 : tr;
+                const uint32_t wbytes = static_cast<uint32_t>(rows * (K / 2));
+                const HalfSpan hs = half_span(a.s_w, n0 * nb, (n0 + rows) * nb);
+                const HalfSpan hz = half_span(a.z_w, n0 * nb, (n0 + rows) * nb);
                 uint8_t* st = smem + P.stage_off + s * P.stage_bytes;
-                mbar_arrive_expect_tx(&full[s], wbytes + sbytes + zbytes);
-                bulk_load(st, w, wbytes, &full[s]);
-                bulk_load(st + P.w_bytes, ss, sbytes, &full[s]);
-                bulk_load(st + P.w_bytes + P.sz_bytes, zs, zbytes, &full[s]);
+                mbar_arrive_expect_tx(&full[s], wbytes + hs.bytes + hz.bytes);
+                bulk_load(st, a.wq + n0 * (K / 2), wbytes, &full[s]);
+                if (hs.bytes) bulk_load(st + P.w_bytes + hs.skew + hs.lo, hs.src, hs.bytes, &full[s]);
+                if (hz.bytes) bulk_load(st + P.w_bytes + P.sz_bytes + hz.skew + hz.lo, hz.src, hz.bytes, &full[s]);
             }
             if (!ok || *abort_flag) {
                 // let the copies already issued land before the CTA exits
@@ -331,7 +340,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                         xs[j] = make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
                                             __uint_as_float(v.w));
                     }
-                    if (amax > 0.0f) {
+                    if (s > 0.0f) {  // s = 0: every code 0
                         quant_lane<4>(xs, q, s, r);
                     } else {
 #pragma unroll
@@ -385,11 +394,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
             const int64_t n0 = (blockIdx.x + static_cast<int64_t>(i) * gridDim.x) * tr;
             const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (i / ns) & 1, ctl));
             const uint32_t st = smem_u32(smem + P.stage_off + s * P.stage_bytes);
-            const uint8_t* src;
-            uint32_t bytes, sskew, zskew;
-            half_span(a.s_w, n0 * nb, n0 * nb + 1, src, bytes, sskew);
-            half_span(a.z_w, n0 * nb, n0 * nb + 1, src, bytes, zskew);
-            const uint32_t swb = st + P.w_bytes + sskew, zwb = st + P.w_bytes + P.sz_bytes + zskew;
+            const int64_t rows = N - n0 < tr ? N - n0 : tr;
+            const HalfSpan hs = half_span(a.s_w, n0 * nb, (n0 + rows) * nb);
+            const HalfSpan hz = half_span(a.z_w, n0 * nb, (n0 + rows) * nb);
+            const uint32_t swb = st + P.w_bytes, zwb = st + P.w_bytes + P.sz_bytes;
+            const uint16_t *sws = a.s_w + n0 * nb, *zws = a.z_w + n0 * nb;
             // the rows of this warp in the tile: r_j = warp + 8 j (tr >= 8) or rslot (tr < 8)
             int rrow[RW];
             bool rok[RW];
@@ -416,8 +425,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
                         W0[j] = on ? lds128(wa) : make_uint4(0, 0, 0, 0);
                         W1[j] = on ? lds128(wa + 16) : make_uint4(0, 0, 0, 0);
                         const uint32_t e = (rrow[j] * nbu + b) * 2;
-                        sw[j] = on ? half_bits_to_float(lds16(swb + e)) : 0.0f;
-                        nz[j] = on ? -half_bits_to_float(lds16(zwb + e)) : 0.0f;
+                        sw[j] = on ? span_elem(swb, hs, sws, e) : 0.0f;
+                        nz[j] = on ? -span_elem(zwb, hz, zws, e) : 0.0f;
                     }
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {

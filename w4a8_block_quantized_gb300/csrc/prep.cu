@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) quant_kernel(const P
             float4 xh[H], q[H];
 #pragma unroll
             for (int j = 0; j < H; ++j) xh[j] = v[h0 + j];
-            if (amax > 0.0f) {
+            if (s > 0.0f) {  // s = 0 (absmax 0, or absmax / 127 below the smallest subnormal): codes 0
                 quant_lane<H>(xh, q, s, r);
             } else {
 #pragma unroll
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(256) quant_long_kernel(const PrepArgs a, int r
         __syncthreads();
         const float s = __fdiv_rn(amax, 127.0f);
         if (threadIdx.x == 0 && a.s_a_out) a.s_a_out[m] = s;
-        const bool nz = amax > 0.0f;
+        const bool nz = s > 0.0f;  // s = 0: every code 0
         // n4 is a multiple of 16, so every warp iteration covers whole blocks.
         for (int64_t f0 = 0; f0 < n4; f0 += 256) {
             const int64_t f = f0 + threadIdx.x;
