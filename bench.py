@@ -32,6 +32,7 @@ import torch  # noqa: E402
 METRIC = "W4A8 block64 prefill linear: effective TOPS & tok/s at M=512; % of INT8 peak"
 DECODE_METRIC = "W4A8 block64 decode linear: tokens/s at M=1 (weights streamed at 4.5 bits each); % of HBM"
 L2_FLUSH_BYTES = 256 << 20
+WIDE_M = 4096   # from this many tokens on the contraction runs 256-token tiles from weight records
 # The other INT8 denominator: the integer tensor path sm_103a still has, the legacy warp-level
 # mma.sync.m16n8k32.s8.s8.s32, measured on a GB300 of this kind by a standalone probe (608 CTAs
 # x 8 warps, 8 independent accumulators per warp, SM clock 2070 MHz).  tcgen05 has no integer
@@ -467,7 +468,11 @@ def run_bench(args):
                     "traffic": None if args.shape else recorded_traffic(args.workload), "peak_source": peak_src,
                     "bytes_per_launch": int(gemv_bytes), "gemv_us_per_launch": round(gemm_avg * 1e3, 3)}
     else:
-        roofline = {"bound": "tensor", "kernel": "gemm_kernel (tcgen05 kind::f8f6f4 + epilogue)",
+        roofline = {"bound": "tensor",
+                    "kernel": ("gemm_kernel (weight records; tcgen05 kind::f8f6f4 + kind::f16 zero-point MMA; "
+                               "128-token tiles)" if M < WIDE_M else
+                               "gemm_wide_kernel (weight records; tcgen05 kind::f8f6f4 + kind::f16 zero-point MMA; "
+                               "256-token tiles)"),
                     "achieved": round(gemm_tops, 2), "peak": round(tensor_peak, 1), "unit": "TOPS",
                     "frac": round(gemm_tops / tensor_peak, 4),
                     "traffic": None if args.shape else recorded_traffic(args.workload),

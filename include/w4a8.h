@@ -127,6 +127,24 @@ int w4a8_linear_prepared(const void *act, const void *pw, const float *bias, flo
 size_t w4a8_prepared_activations_bytes(int64_t M, int64_t K);
 size_t w4a8_prepared_weights_bytes(int64_t N, int64_t K);
 
+/* Contraction + epilogue (section 4 steps 2-3) from prepared activations (`act`, written by
+ * w4a8_prepare_activations for the same M and K) and the weights as given: wq, w_scale and
+ * w_zero in the layouts above.  One pre-pass can then serve several linears that read the
+ * same input, with no prepared copy of their weights and no workspace.  Below 4096 tokens
+ * the contraction stages the packed u4 codes itself (TMA) and expands them in shared memory
+ * (section 4 step 2: each task reuses one staged weight tile), so no expanded weights are
+ * written to or read from device memory, and `workspace` may be NULL (size 0).  The
+ * expansion shares the SM with the tensor cores and costs more per 64-block than reading
+ * expanded weights (w4a8_prepare_weights + w4a8_linear_prepared, or the fused call, whose
+ * pre-pass launch expands them): this call trades that time for the memory.  From 4096
+ * tokens on the weights are first expanded into the workspace, at least
+ * w4a8_linear_act_workspace_bytes(M, N, K) bytes.  The result equals w4a8_prefill_linear on
+ * the input `act` was prepared from, bit for bit, for M > W4A8_DECODE_MAX_M. */
+size_t w4a8_linear_act_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int w4a8_linear_act(const void *act, const uint8_t *wq, const uint16_t *w_scale, const uint16_t *w_zero,
+                    const float *bias, float *y, int64_t M, int64_t N, int64_t K,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
 /* Epilogue variants ("MNN LLM inference on the SpacemiT K3", section 4 step 3: the direct
  * epilogue adds the bias and may clamp).  The *_ex calls equal their plain counterparts
  * except for the store of y:

@@ -44,7 +44,7 @@ def test_status_strings(lib):
         s = b.status_string(code)
         assert s and s != "unknown status"
     assert b.status_string(12345) == "unknown status"
-    assert lib.w4a8_abi_version() == 203
+    assert lib.w4a8_abi_version() == 204
 
 
 def test_shape_checks_need_no_gpu(lib):
@@ -75,14 +75,19 @@ def test_shape_checks_need_no_gpu(lib):
 
 
 def test_workspace_sizes(lib):
-    M, N, K = 512, 3072, 1024
-    nb = K // 64
-    lin = lib.w4a8_linear_workspace_bytes(M, N, K)
-    pre = lib.w4a8_prefill_workspace_bytes(M, N, K)
-    # operand planes (2 bytes per activation) + transposed row sums (16 bytes per entry)
+    # operand planes (2 bytes per activation) + row-sum entries (16 bytes per token and block)
     # + expanded weights (1 byte each) + scales and weight-side zero-point rows (4 + 16 bytes)
-    assert lin >= 2 * M * K + nb * M * 16 + N * K + nb * N * 20
-    assert pre >= lin + 4 * M
+    for M in (512, 4096):
+        N, K = 3072, 1024
+        nb = K // 64
+        lin = lib.w4a8_linear_workspace_bytes(M, N, K)
+        pre = lib.w4a8_prefill_workspace_bytes(M, N, K)
+        assert lin >= 2 * M * K + nb * M * 16 + N * K + nb * N * 20
+        assert pre >= lin + 4 * M
+    # w4a8_linear_act: below 4096 tokens the contraction reads the packed weights itself (no
+    # workspace); from 4096 on the weight records go into the workspace
+    assert lib.w4a8_linear_act_workspace_bytes(512, 3072, 1024) == 0
+    assert lib.w4a8_linear_act_workspace_bytes(4096, 3072, 1024) == lib.w4a8_prepared_weights_bytes(3072, 1024)
     assert lib.w4a8_linear_workspace_bytes(0, N, K) == 0
     assert lib.w4a8_linear_workspace_bytes(M, N, 100) == ctypes.c_size_t(-1).value
     assert lib.w4a8_debug_workspace_bytes(7, 9, 128) >= 7 * 256 + 9 * 128

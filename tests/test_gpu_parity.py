@@ -359,6 +359,33 @@ def test_split_calls_equal_fused():
         check_y(y_split, y_ref, bound, f"split N={N}")
 
 
+@pytest.mark.parametrize("M,K,N", [(9, 64, 1), (300, 1024, 513), (512, 1088, 3072), (129, 6144, 130),
+                                   (4100, 512, 300)])
+def test_linear_act_equals_fused(M, K, N):
+    """w4a8_linear_act (prepared activations, the packed weights as given) equals the fused
+    call bit for bit -- below 4096 tokens the contraction expands the u4 codes in shared
+    memory (one 64-block, odd K/64, a ragged weight tile), at 4100 the weights go through the
+    workspace -- also right after the weights were rewritten by the previous kernel in the
+    stream, and one prepared activation buffer serves two weight sets."""
+    b = B()
+    d = synth.random_small(M, K, N, seed=M + 5 * K + N, bias=True)
+    g = inputs_to_dev(d)
+    y_fused = b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"])
+    act = b.prepare_activations(g["x"])
+    assert torch.equal(b.linear_act(act, g["wq"], g["s_w"], g["z_w"], M, N, K, bias=g["bias"]), y_fused)
+    wq2, sw2, zw2 = torch.zeros_like(g["wq"]), torch.zeros_like(g["s_w"]), torch.zeros_like(g["z_w"])
+    wq2.copy_(g["wq"])        # written by the kernel just before the call
+    sw2.copy_(g["s_w"])
+    zw2.copy_(g["z_w"])
+    assert torch.equal(b.linear_act(act, wq2, sw2, zw2, M, N, K, bias=g["bias"]), y_fused)
+    d2 = synth.random_small(M, K, 70, seed=M + K, bias=False)
+    g2 = inputs_to_dev(d2)
+    y2 = b.linear_act(act, g2["wq"], g2["s_w"], g2["z_w"], M, 70, K)
+    y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d2["wq"], d2["s_w"], d2["z_w"], None)
+    check_y(y2, y_ref, bound, f"linear_act {M}x{K}->70")
+    assert b.sync_status() == 0
+
+
 def test_quant_pack_near_ties_bitexact():
     """Activations placed on and around the rounding boundaries (k + 1/2) * s_a, for scales
     that are not powers of two: the codes must match the oracle's IEEE-division rounding

@@ -41,6 +41,8 @@ SIGNATURES = {
     "w4a8_prepare_activations": (ctypes.c_int, [_P, _I64, _I64, _P, _SZ, _P]),
     "w4a8_prepare_weights": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _SZ, _P]),
     "w4a8_linear_prepared": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "w4a8_linear_act": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    "w4a8_linear_act_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "w4a8_prefill_linear_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_float, ctypes.c_float,
                                               _I64, _I64, _I64, _P, _SZ, _P]),
     "w4a8_linear_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_float, ctypes.c_float,
@@ -418,6 +420,30 @@ def linear_prepared(act, pw, M: int, N: int, K: int, bias=None, y=None, stream=N
     _arg(y, torch.float32, (M, N), "y", dev)
     rc = load().w4a8_linear_prepared(_ptr(act), _ptr(pw), _ptr(bias), _ptr(y), M, N, K, _stream(stream))
     _check(rc, "w4a8_linear_prepared")
+    return y
+
+
+def linear_act_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().w4a8_linear_act_workspace_bytes(M, N, K))
+
+
+def linear_act(act, wq, w_scale, w_zero, M: int, N: int, K: int, bias=None, y=None, ws=None, stream=None):
+    """w4a8_linear_act: contraction + epilogue from prepared activations and the packed
+    weights as given -> y fp32 [M,N]."""
+    _want(act, None, "act")
+    dev = act.device
+    if min(M, N, K) < 0:
+        raise ValueError(f"negative size in (M, N, K) = {(M, N, K)}")
+    if M and N and K > 0 and K % 64 == 0:
+        _arg(act, None, None, "act", dev, min_bytes=prepared_activations_bytes(M, K))
+    _weights(wq, w_scale, w_zero, N, K, dev)
+    _arg(bias, torch.float32, (N,), "bias", dev)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev) if y is None else y
+    _arg(y, torch.float32, (M, N), "y", dev)
+    ws = _ws(ws, linear_act_workspace_bytes(M, N, K), dev, stream)
+    rc = load().w4a8_linear_act(_ptr(act), _ptr(wq), _ptr(w_scale), _ptr(w_zero), _ptr(bias), _ptr(y), M, N, K,
+                                _ptr(ws), _nbytes(ws), _stream(stream))
+    _check(rc, "w4a8_linear_act")
     return y
 
 

@@ -50,7 +50,7 @@ def up_to_date() -> bool:
 # launch allocation would leave setmaxnreg.inc waiting for registers that never come.  Keys
 # are matched against the mangled entry names; the debug instantiation of the 256-token
 # kernel (template argument true, "ILb1E") does not re-split and is not checked.
-REGISTER_SPLIT_KERNELS = {"gemm_kernel": 96, "gemm_wide_kernelILb0E": 96}
+REGISTER_SPLIT_KERNELS = {"gemm_kernel": 96, "gemm_wide_kernelILb0E": 96, "gemm_packed_kernel": 96}
 
 
 def check_register_split(ptxas_log: str) -> None:

@@ -67,6 +67,11 @@ int check_shape(int64_t M, int64_t N, int64_t K) {
     return W4A8_OK;
 }
 
+// Whether w4a8_linear_act contracts from the packed weights themselves (128-token tiles: the
+// GEMM stages the u4 codes and expands them in shared memory, no workspace) or from weight
+// records written into its workspace first (256-token tiles).
+bool packed_form(int64_t M) { return token_tile(M) == kTileT; }
+
 // Workspace of the one-call entry points: prepared activations, then prepared weights.
 struct CallLayout {
     ActLayout act;
@@ -102,6 +107,30 @@ int run_linear(const uint8_t* trec, const float* s_a, const uint8_t* pw, const f
     g.out = out;
     g.status = d.status;
     return launch_gemm(g, false, d.num_sms, st) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
+}
+
+// GEMM + epilogue from prepared activations (128-token records) and the caller's packed
+// weights, expanded inside the contraction.  `early`: the previous kernel in the stream is the
+// call's own pre-pass, which writes none of the weights, so the GEMM may stage them before it
+// has finished.  Each output equals run_linear's from weights prepared from the same arrays.
+int run_linear_packed(const uint8_t* trec, const float* s_a, const uint8_t* wq, const uint16_t* w_scale,
+                      const uint16_t* w_zero, const float* bias, const OutSpec& out, int64_t M, int64_t N, int64_t K,
+                      bool early, const DeviceInfo& d, cudaStream_t st) {
+    GemmArgs g;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.trec = trec;
+    g.tw = kTileT;
+    g.wq = wq;
+    g.s_w = w_scale;
+    g.z_w = w_zero;
+    g.early = early ? 1 : 0;
+    g.s_a = s_a;
+    g.bias = bias;
+    g.out = out;
+    g.status = d.status;
+    return launch_gemm_packed(g, false, d.num_sms, st) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
 }
 
 // Weight job arguments: all N rows of wq into the weight records at `wrec`.
@@ -183,7 +212,7 @@ using namespace w4a8;
 
 extern "C" {
 
-int w4a8_abi_version(void) { return 203; }
+int w4a8_abi_version(void) { return 204; }
 
 const char* w4a8_status_string(int status) {
     switch (status) {
@@ -299,6 +328,7 @@ int linear_impl(const int8_t* a_q, const float* a_scale, const int32_t* rowsum, 
     p.a_q_in = a_q;
     p.rs_in = rowsum;
     p.M = M;
+    p.K = K;
     p.trec = ws + L.act.rec;
     p.tw = L.act.tw;
     set_weight_job(&p, wq, w_scale, w_zero, N, K, ws + L.w_off);
@@ -345,6 +375,7 @@ int prefill_impl(const float* x, const uint8_t* wq, const uint16_t* w_scale, con
     PrepArgs p;
     p.x = x;
     p.M = M;
+    p.K = K;
     p.s_a_out = s_a;
     p.trec = ws + L.act.rec;
     p.tw = L.act.tw;
@@ -430,6 +461,43 @@ int w4a8_prepare_weights(const uint8_t* wq, const uint16_t* w_scale, const uint1
 int w4a8_linear_prepared(const void* act, const void* pw, const float* bias, float* y, int64_t M, int64_t N,
                          int64_t K, void* stream) {
     return linear_prepared_impl(act, pw, bias, f32_out(y), M, N, K, stream);
+}
+
+size_t w4a8_linear_act_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (check_shape(M, N, K) != W4A8_OK) return static_cast<size_t>(-1);
+    if (M == 0 || N == 0 || packed_form(M)) return 0;
+    return w_layout(N, K).total;
+}
+
+int w4a8_linear_act(const void* act, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero,
+                    const float* bias, float* y, int64_t M, int64_t N, int64_t K, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+    int rc = check_shape(M, N, K);
+    if (rc != W4A8_OK) return rc;
+    if (M == 0 || N == 0) return W4A8_OK;
+    if (!act || !wq || !w_scale || !w_zero || !y) return W4A8_ERR_ARG;
+    if (!aligned(act, 16) || !aligned(wq, 16) || !aligned(y, 16) || !aligned(w_scale, 2) || !aligned(w_zero, 2) ||
+        (bias && !aligned(bias, 4)))
+        return W4A8_ERR_ALIGN;
+    const size_t need = w4a8_linear_act_workspace_bytes(M, N, K);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return W4A8_ERR_WORKSPACE;
+    if (need > 0 && !aligned(workspace, 16)) return W4A8_ERR_ALIGN;
+    DeviceInfo* d = nullptr;
+    if ((rc = current_device(&d)) != W4A8_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const ActLayout A = act_layout(M, K, true, token_tile(M));
+    const uint8_t* a = static_cast<const uint8_t*>(act);
+    const float* s_a = reinterpret_cast<const float*>(a + A.s_a);
+    if (packed_form(M)) {
+        // the previous kernel in the stream may have written the weights: no early staging
+        return run_linear_packed(a + A.rec, s_a, wq, w_scale, w_zero, bias, f32_out(y), M, N, K, false, *d, st);
+    }
+    uint8_t* wrec = static_cast<uint8_t*>(workspace);
+    PrepArgs p;
+    p.M = 0;
+    set_weight_job(&p, wq, w_scale, w_zero, N, K, wrec);
+    if (launch_pack(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
+    return run_linear(a + A.rec, s_a, wrec, bias, f32_out(y), M, N, K, A.tw, *d, st);
 }
 
 int w4a8_linear_prepared_ex(const void* act, const void* pw, const float* bias, void* y, int out_dtype,

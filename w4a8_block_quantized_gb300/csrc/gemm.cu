@@ -48,7 +48,10 @@
 // wait), releases their buffers as soon as the accumulators are in registers, then folds
 // them into y; it frees a stage once its accumulators are complete.  Every wait is bounded (WaitCtl); a CTA
 // that gives up records a timeout and unwinds.
+#include <cuda_fp16.h>
+
 #include "epilogue.cuh"
+#include "operand_codes.cuh"
 #include "sm103_ptx.cuh"
 #include "w4a8_internal.h"
 
@@ -90,14 +93,19 @@ static_assert((2 * kStages) % kIssuers == 0, "each stage slot must have one issu
 // Grouped raster over the output tiles: groups of kGroup token tiles, the token tile
 // varying fastest inside a group, so the CTAs running at one time share token and weight
 // tiles in L2.
-constexpr int64_t kGroup = 8;
+// The arithmetic is 32-bit (a 64-bit division is a long software sequence, and a producer thread
+// runs this on its critical path): the host keeps the tile count below 2^31, and tiles_w is at
+// most 2^24.
+constexpr uint32_t kGroup = 8;
 __device__ __forceinline__ void tile_at(int64_t t, int64_t tiles_t, int64_t tiles_w, int64_t& tt, int64_t& tw) {
-    const int64_t per = kGroup * tiles_w;
-    const int64_t grp = t / per, r = t - grp * per;
-    const int64_t g0 = grp * kGroup;
-    const int64_t gsz = tiles_t - g0 < kGroup ? tiles_t - g0 : kGroup;
-    tt = g0 + r % gsz;
-    tw = r / gsz;
+    const uint32_t t32 = static_cast<uint32_t>(t), tt32 = static_cast<uint32_t>(tiles_t);
+    const uint32_t per = kGroup * static_cast<uint32_t>(tiles_w);
+    const uint32_t grp = t32 / per, r = t32 - grp * per;
+    const uint32_t g0 = grp * kGroup;
+    const uint32_t gsz = tt32 - g0 < kGroup ? tt32 - g0 : kGroup;
+    const uint32_t q = r / gsz;
+    tt = g0 + (r - q * gsz);
+    tw = q;
 }
 
 // Named barrier 1 over the 16 epilogue warps (barrier 0 is __syncthreads).  Every epilogue
@@ -601,6 +609,403 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
     }
 }
 
+// ---------------------------------------------------------------- 128-token tiles, packed weights
+// The contraction of gemm_kernel, reading the caller's packed weights (section 4 step 2: each
+// task reuses one staged B tile); it serves w4a8_linear_act.  The producer stages each stage's
+// 2 x 32 packed bytes of the tile's 128 weight rows with one tiled TMA load (64-byte swizzle,
+// rows past N filled with zeros), and the epilogue warps, between their drains, expand them in
+// shared memory to the e4m3 operand and write the {-z_w, -z_w} rows of the zero-point MMA --
+// the same bytes the weight job writes into a weight record, so the MMAs, and every output,
+// are those of gemm_kernel bit for bit.  The epilogue reads 512 s_w from s_w itself.  No
+// weight record is written to or read from device memory.
+// Measured on the pp512 linear (512 x 1024 -> 3072), a stage of two 64-blocks takes about
+// 1.7 us here against 0.63 us in gemm_kernel: while the expanding warps load and store shared
+// memory, the tensor cores' stages stretch (a variant without any expansion work runs at
+// 0.8 us).  So the one-call entry points keep the weight records; this kernel is the form that
+// needs neither a workspace nor expanded weights in memory.
+//
+// The packed weights have a ring of kPkSlots slots of their own, so their loads run ahead of the
+// operand stages -- and, with `early` set (they do not depend on the previous kernel), start
+// before the pre-pass has finished.  Operand stage s = j % kStages of stage j is expanded as soon
+// as stage j - kStages has completed its MMAs, right after the epilogue has drained that stage's
+// accumulators; the first kStages stages are expanded up front.  Each tile also prefetches the
+// next tile's s_w / z_w rows into L2.
+//
+// Warp roles (20 warps, register split as in gemm_kernel):
+//   warp 0       producer: per stage one TMA load (packed weights, into the ring) and one bulk
+//                copy (token records of the stage's two blocks)
+//   warps 1-3    MMA issue, as in gemm_kernel
+//   warps 4-19   epilogue and expansion: thread t expands the 16 packed bytes (t & 3) of weight
+//                row t >> 2 of a stage; the drain is gemm_kernel's
+// Barriers: per operand stage full (token records landed, the operand expanded, the two TMEM
+// buffers released) and empty (the stage's MMAs done: its operand buffers free); per ring slot
+// wfull (the packed weights landed).  A ring slot is reloaded only after the stage that last
+// used it has completed its MMAs (its expansion came before that stage's full barrier), so it
+// needs no barrier of its own for that.
+namespace packed {
+constexpr int kStages = 3;                        // operand stages (token records + expanded weights)
+constexpr int kPkSlots = 6;                       // staged packed weights: a deeper ring of their own
+constexpr int kPk = kTileW * 64;                  // 128 rows x 64 packed bytes (two blocks)
+constexpr int kOffWop = 2 * kTokRec;              // the stage's two expanded weight records
+constexpr int kStageBytes = kOffWop + 2 * kWRec;
+constexpr int kOffPk = kStages * kStageBytes;
+constexpr int kOffZero = kOffPk + kPkSlots * kPk;
+constexpr int kOffBar = kOffZero + kZeroBytes;
+constexpr int kNumBars = 2 * kStages + kPkSlots + 2 + kIssuers;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+static_assert(kOffWop == kStageTok && kStages == ::w4a8::kStages,
+              "the issuers' descriptors and the TMEM release schedule follow gemm_kernel's stage layout");
+static_assert(kStageBytes % 1024 == 0 && kOffPk % 1024 == 0 && kPk % 1024 == 0, "swizzled tiles must stay 1024-aligned");
+static_assert(kSmemBytes + 2 * kEpiWarps * 32 * 4 <= 227 * 1024, "shared memory budget");
+static_assert(kPkSlots >= kStages, "the weights of stage j + kStages go out while stage j's operands are in use");
+static_assert(kEpiWarps * 32 == 4 * kTileW, "one expanding thread per 16 packed bytes of a stage");
+}  // namespace packed
+
+// Prefetch [p, p + bytes) into L2, one instruction per 128-byte line.
+__device__ __forceinline__ void prefetch_l2_span(const void* p, int64_t bytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p) & ~uintptr_t(127);
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(bytes);
+    for (uintptr_t a = a0; a < a1; a += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
+// A walk over the (tile, stage of the tile) pairs of a CTA's stages.
+struct StageCursor {
+    uint32_t i, p;
+    int64_t tt, tw;
+};
+
+__device__ __forceinline__ void cursor_tile(StageCursor& c, uint32_t my_tiles, int64_t first, int64_t tiles_t,
+                                            int64_t tiles_w) {
+    if (c.i < my_tiles) tile_at(first + static_cast<int64_t>(c.i) * gridDim.x, tiles_t, tiles_w, c.tt, c.tw);
+}
+
+__device__ __forceinline__ void cursor_next(StageCursor& c, uint32_t spt, uint32_t my_tiles, int64_t first,
+                                            int64_t tiles_t, int64_t tiles_w) {
+    if (++c.p == spt) {
+        c.p = 0;
+        ++c.i;
+        cursor_tile(c, my_tiles, first, tiles_t, tiles_w);
+    }
+}
+
+// The producer's TMA load of stage `wnext`'s packed weights (the stage `cw` points at) into its
+// ring slot; advances both.
+__device__ __forceinline__ void issue_weights(const GemmArgs& args, uint8_t* smem, uint64_t* wfull, StageCursor& cw,
+                                              uint32_t& wnext, uint32_t spt, uint32_t my_tiles, int64_t first,
+                                              int64_t tiles_t, int64_t tiles_w) {
+    namespace P = packed;
+    uint64_t* bar = &wfull[wnext % P::kPkSlots];
+    mbar_arrive_expect_tx(bar, P::kPk);
+    tma_load_2d(smem + P::kOffPk + (wnext % P::kPkSlots) * P::kPk, &args.wmap, static_cast<int>(64 * cw.p),
+                static_cast<int>(cw.tw * kTileW), bar);
+    ++wnext;
+    cursor_next(cw, spt, my_tiles, first, tiles_t, tiles_w);
+}
+
+// 512 s_w[n, b] from the caller's fp16 scales (row pointer swr, null past N), 0 past the last
+// block: the power of two undoes the 2^-9 of the e4m3 weight operand (exact).
+__device__ __forceinline__ float weight_scale(const uint16_t* swr, uint32_t b, uint32_t nb) {
+    return (swr && b < nb) ? 512.0f * __half2float(__ushort_as_half(__ldg(swr + b))) : 0.0f;
+}
+
+// Expansion of stage jj's packed weights into operand stage jj % kStages, by the 512 epilogue
+// threads (thread et: the 16 packed bytes (et & 3) of weight row et >> 2).  Every epilogue
+// thread calls it for every stage in order, once that operand stage is free; false if a wait
+// gave up (all threads alike).  A plain function, not a lambda: nothing of it may live in local
+// memory, which with the shared-memory carve-out has next to no L1 behind it.
+template <bool DEBUG>
+__device__ __forceinline__ bool expand_stage(const GemmArgs& args, uint8_t* smem, uint64_t* wfull, uint64_t* full,
+                                             uint32_t jj, uint32_t spt, uint32_t nb, int64_t first, int64_t tiles_t,
+                                             int64_t tiles_w, int et, const WaitCtl& ctl) {
+    namespace P = packed;
+    const int xr = et >> 2, xc = et & 3, xsw = (xr >> 1) & 3;
+    const uint32_t ti = jj / spt, p = jj - ti * spt;
+    int64_t tt, tw;
+    tile_at(first + static_cast<int64_t>(ti) * gridDim.x, tiles_t, tiles_w, tt, tw);
+    const int64_t n = tw * kTileW + xr;
+    const uint32_t b = 2 * p + (xc >> 1);
+    const bool live = b < nb;
+    // the zero point first: its latency overlaps the wait
+    const uint32_t zz = (!DEBUG && live && (xc & 1) == 0 && n < args.N) ? neg_zero_pair(__ldg(args.z_w + n * nb + b)) : 0u;
+    if (!epi_all(mbar_wait(&wfull[jj % P::kPkSlots], (jj / P::kPkSlots) & 1, ctl))) return false;
+    if (live) {
+        const uint4 w =
+            *reinterpret_cast<const uint4*>(smem + P::kOffPk + (jj % P::kPkSlots) * P::kPk + xr * 64 + ((xc ^ xsw) << 4));
+        uint4 lo, hi;
+        expand8(w.x, lo.x, lo.y);
+        expand8(w.y, lo.z, lo.w);
+        expand8(w.z, hi.x, hi.y);
+        expand8(w.w, hi.z, hi.w);
+        uint8_t* rec = smem + (jj % P::kStages) * P::kStageBytes + P::kOffWop + (xc >> 1) * kWRec;
+        const int e0 = 2 * (xc & 1);
+        *reinterpret_cast<uint4*>(rec + xr * 64 + ((e0 ^ xsw) << 4)) = lo;
+        *reinterpret_cast<uint4*>(rec + xr * 64 + (((e0 + 1) ^ xsw) << 4)) = hi;
+        if (!DEBUG && (xc & 1) == 0) *reinterpret_cast<uint4*>(rec + kWZx + xr * 16) = make_uint4(zz, 0u, 0u, 0u);
+    }
+    // the operand is written (generic proxy) before the tensor cores (async proxy) read it
+    fence_proxy_async_smem();
+    epi_bar_sync();
+    if (et == 0) mbar_arrive(&full[jj % P::kStages]);
+    return true;
+}
+
+template <bool DEBUG>
+__global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_constant__ GemmArgs args) {
+    namespace P = packed;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + P::kOffBar);
+    uint64_t* empty = full + P::kStages;
+    uint64_t* wfull = empty + P::kStages;   // per ring slot
+    uint64_t* tfull = wfull + P::kPkSlots;  // one per pair of TMEM buffers
+    uint64_t* drain = tfull + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P::kOffMisc);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+    __shared__ float epi_sa[kEpiWarps][32];
+    __shared__ float epi_bias[kEpiWarps][32];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t tiles_t = (args.M + kTileT - 1) / kTileT;
+    const int64_t tiles_w = (args.N + kTileW - 1) / kTileW;
+    const int64_t ntiles = tiles_t * tiles_w;
+    const int64_t first = blockIdx.x;
+    const uint32_t my_tiles = ntiles > first ? static_cast<uint32_t>((ntiles - 1 - first) / gridDim.x + 1) : 0u;
+    const uint32_t nb = static_cast<uint32_t>(args.K / kBlock);
+    const uint32_t spt = (nb + 1) / 2;         // stages per tile
+    const uint32_t total = my_tiles * spt;
+    const WaitCtl ctl{abort_flag, args.status, args.wait_limit_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P::kStages; ++s) {
+            mbar_init(&full[s], 3);  // producer, two epilogue arrivals (operand expanded, TMEM released)
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < P::kPkSlots; ++s) mbar_init(&wfull[s], 1);  // producer
+        for (int i = 0; i < 2; ++i) mbar_init(&tfull[i], 2);
+        for (int i = 0; i < kIssuers; ++i) mbar_init(&drain[i], 1);
+        *abort_flag = 0u;
+        fence_barrier_init();
+    }
+    if (!DEBUG) {
+        for (int i = threadIdx.x; i < kZeroBytes / 16; i += kThreads)
+            reinterpret_cast<uint4*>(smem + P::kOffZero)[i] = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp < 4) {
+        regs_dec<kRegsLow>();
+        if (warp == 0) {
+            // -------------------------------------------------------- producer
+            if (lane == 0) {
+                tma_prefetch_map(&args.wmap);
+                // two walks over (tile, stage of the tile): W for the weights (ahead), T for the
+                // token records; each looks its tile up once
+                StageCursor cw{}, ct{};
+                cursor_tile(cw, my_tiles, first, tiles_t, tiles_w);
+                cursor_tile(ct, my_tiles, first, tiles_t, tiles_w);
+                uint32_t wnext = 0;  // stages whose weights were issued
+                const uint32_t ahead = P::kPkSlots - P::kStages;
+                const uint32_t pre = total < static_cast<uint32_t>(P::kPkSlots) ? total : static_cast<uint32_t>(P::kPkSlots);
+                if (args.early)
+                    while (wnext < pre) issue_weights(args, smem, wfull, cw, wnext, spt, my_tiles, first, tiles_t, tiles_w);
+                griddep_wait();
+                while (wnext < pre) issue_weights(args, smem, wfull, cw, wnext, spt, my_tiles, first, tiles_t, tiles_w);
+                bool ok = true;
+                uint32_t issued = 0;
+                for (uint32_t j = 0; j < total; ++j) {
+                    const uint32_t k = j / P::kStages;
+                    if (k > 0 && !mbar_wait(&empty[j % P::kStages], (k - 1) & 1, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t b0 = 2 * ct.p, cnt = nb - b0 < 2 ? 1u : 2u;
+                    uint64_t* bar = &full[j % P::kStages];
+                    mbar_arrive_expect_tx(bar, cnt * kTokRec);
+                    bulk_load(smem + (j % P::kStages) * P::kStageBytes,
+                              args.trec + (static_cast<int64_t>(ct.tt) * nb + b0) * kTokRec, cnt * kTokRec, bar);
+                    cursor_next(ct, spt, my_tiles, first, tiles_t, tiles_w);
+                    issued = j + 1;
+                    // stage j - kStages is complete, and so is every stage before it: W(j + ahead)
+                    // may reuse the slot of stage j + ahead - kPkSlots = j - kStages
+                    if (k > 0 && wnext == j + ahead && wnext < total)
+                        issue_weights(args, smem, wfull, cw, wnext, spt, my_tiles, first, tiles_t, tiles_w);
+                }
+                if (!ok || *abort_flag) {
+                    // let every copy already issued land before the CTA exits
+                    for (uint32_t q = (wnext > static_cast<uint32_t>(P::kPkSlots) ? wnext - P::kPkSlots : 0); q < wnext; ++q)
+                        drain_wait(&wfull[q % P::kPkSlots], (q / P::kPkSlots) & 1, 100000000ull);
+                    for (uint32_t q = (issued > static_cast<uint32_t>(P::kStages) ? issued - P::kStages : 0); q < issued; ++q)
+                        drain_wait(&full[q % P::kStages], (q / P::kStages) & 1, 100000000ull);
+                }
+            }
+        } else {
+            // -------------------------------------------------------- MMA issue (warps 1-3)
+            const int iw = warp - 1;
+            constexpr uint32_t idesc = idesc_e4m3_f32(kTileW, kTileT);
+            const uint32_t zr = smem_u32(smem + P::kOffZero);
+            const uint32_t t0a = smem_u32(smem), w0a = smem_u32(smem + P::kOffWop);
+            const uint64_t dT0 = smem_desc(t0a, 1024, kLayoutSw128);
+            const uint64_t dW0 = smem_desc(w0a, 512, kLayoutSw64);
+            const uint64_t dBx0 = smem_desc(t0a + kTokRx, 128, 0, zr - (t0a + kTokRx));
+            const uint64_t dAx0 = smem_desc(w0a + kWZx, 128, 0, zr - (w0a + kWZx));
+            for (uint32_t i = iw; i < 2 * total; i += kIssuers) {
+                const uint32_t j = i >> 1, k = i & 1u;
+                const int s = static_cast<int>(j % P::kStages);
+                const uint32_t pair = j & 1u;
+                const uint32_t b0 = 2 * (j % spt), cnt = nb - b0 < 2 ? 1u : 2u;
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (j / P::kStages) & 1, ctl))) break;
+                tc_fence_after();
+                if (elect_one()) {
+                    if (k < cnt) {
+                        const uint32_t d = tmem_base + (2 * pair + k) * kTileT;
+                        const uint64_t ot = static_cast<uint64_t>((s * P::kStageBytes + static_cast<int>(k) * kTokRec) >> 4);
+                        const uint64_t ow = static_cast<uint64_t>((s * P::kStageBytes + static_cast<int>(k) * kWRec) >> 4);
+                        const uint64_t dT = dT0 + ot, dW = dW0 + ow;
+                        mma_f8f6f4(d, dW, dT, idesc, 0u);
+                        mma_f8f6f4(d, dW + 2, dT + 2, idesc, 1u);
+                        mma_f8f6f4(d, dW, dT + 4, idesc, 1u);
+                        mma_f8f6f4(d, dW + 2, dT + 6, idesc, 1u);
+                        if (!DEBUG) mma_f16(d, dAx0 + ow - (ow << 16), dBx0 + ot - (ot << 16), idesc, 1u);
+                    }
+                    mma_commit(&tfull[pair]);
+                }
+                __syncwarp();
+            }
+            if (elect_one()) mma_commit(&drain[iw]);
+            __syncwarp();
+            drain_wait(&drain[iw], 0, 100000000ull);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue + expansion
+        regs_inc<kRegsHigh>();
+        const int et = threadIdx.x - 4 * 32;           // 0 .. 511
+        const int q = warp & 3, h = (warp - 4) >> 2;   // TMEM lane quarter (warp id mod 4), column quarter
+        const int row = q * 32 + lane;
+        const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 32);
+        const bool lead = et == 0;
+        bool ok = true;
+        // the first stages' operands (their buffers start free); with `early` before the previous
+        // kernel has finished: nothing here reads what it writes
+        if (!args.early) griddep_wait();
+        for (uint32_t jj = 0; ok && jj < total && jj < static_cast<uint32_t>(P::kStages); ++jj)
+            ok = expand_stage<DEBUG>(args, smem, wfull, full, jj, spt, nb, first, tiles_t, tiles_w, et, ctl);
+        if (args.early) griddep_wait();
+        // the TMEM buffers start free: release the first two stages
+        if (lead)
+            for (uint32_t q0 = 0; q0 < 2 && q0 < total; ++q0) mbar_arrive(&full[q0]);
+        uint32_t j = 0;  // stage counter of this CTA
+        for (uint32_t i = 0; ok && i < my_tiles; ++i) {
+            int64_t tt, tw;
+            tile_at(first + static_cast<int64_t>(i) * gridDim.x, tiles_t, tiles_w, tt, tw);
+            const int64_t mt0 = tt * kTileT + h * 32;  // first token column of this warp
+            const int64_t n = tw * kTileW + row;       // this thread's weight row
+            const uint16_t* swr = (!DEBUG && n < args.N) ? args.s_w + n * nb : nullptr;
+            if (!DEBUG && i + 1 < my_tiles && h == 0) {
+                // the next tile's scales and zero points into L2 while this tile runs
+                int64_t tt1, tw1;
+                tile_at(first + static_cast<int64_t>(i + 1) * gridDim.x, tiles_t, tiles_w, tt1, tw1);
+                const int64_t n1 = tw1 * kTileW + row;
+                if (n1 < args.N) {
+                    prefetch_l2_span(args.s_w + n1 * nb, nb * 2);
+                    prefetch_l2_span(args.z_w + n1 * nb, nb * 2);
+                }
+            }
+            if (!DEBUG) {
+                epi_sa[warp - 4][lane] = mt0 + lane < args.M ? __ldg(args.s_a + mt0 + lane) : 0.0f;
+                epi_bias[warp - 4][lane] = (args.bias && n < args.N) ? __ldg(args.bias + n) : 0.0f;
+            }
+            // 512 s_w: the power of two undoes the 2^-9 of the e4m3 weight operand (exact)
+            float ns0 = weight_scale(swr, 0, nb), ns1 = weight_scale(swr, 1, nb);
+            float y[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) y[c] = 0.0f;
+            for (uint32_t p = 0; p < spt; ++p, ++j) {
+                const int s = static_cast<int>(j % P::kStages);
+                const bool two = 2 * p + 1 < nb;
+                const float s0 = ns0, s1 = ns1;
+                if (!DEBUG && p + 1 < spt) {
+                    ns0 = weight_scale(swr, 2 * p + 2, nb);
+                    ns1 = weight_scale(swr, 2 * p + 3, nb);
+                }
+                const uint32_t pair = j & 1u, b0 = 2 * pair;
+                if (!epi_all(mbar_wait(&tfull[pair], (j >> 1) & 1, ctl))) {
+                    ok = false;
+                    break;
+                }
+                // the stage's MMAs are complete: its token records may be reloaded
+                if (lead) mbar_arrive(&empty[s]);
+                tc_fence_after();
+                // one block's accumulators at a time (32 registers): the expansion's state stays in
+                // registers beside them
+                uint32_t v[32];
+#pragma unroll 1
+                for (int e = 0; e < 2; ++e) {
+                    if (e == 1 && !two) break;
+                    const uint32_t tb = tl + (b0 + e) * kTileT;
+                    tmem_ld_32x32b_x16(tb, v);
+                    tmem_ld_32x32b_x16(tb + 16, v + 16);
+                    tmem_wait_ld();
+                    if (e == 1 || !two) {
+                        // the accumulators are in registers: the buffers serve the stage two later
+                        tc_fence_before();
+                        epi_bar_sync();
+                        if (lead && j + 2 < total) mbar_arrive(&full[(j + 2) % P::kStages]);
+                    }
+                    if (DEBUG) {
+                        if (n < args.N) {
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) {
+                                const int64_t m = mt0 + c;
+                                if (m < args.M)
+                                    args.acc[(m * args.N + n) * nb + 2 * p + e] =
+                                        static_cast<int32_t>(__uint_as_float(v[c]) * 512.0f);
+                            }
+                        }
+                    } else {
+                        const float sb = e == 0 ? s0 : s1;
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) y[c] = fmaf(sb, __uint_as_float(v[c]), y[c]);
+                    }
+                }
+                // operand stage s is free too (the stage's MMAs are done): the weights of stage
+                // j + kStages go in, with the accumulators already folded (their registers free)
+                if (j + P::kStages < total &&
+                    !expand_stage<DEBUG>(args, smem, wfull, full, j + P::kStages, spt, nb, first, tiles_t, tiles_w, et, ctl)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok) break;
+            if (!DEBUG) __syncwarp();  // every lane: the slots were written by other lanes of the warp
+            if (!DEBUG && n < args.N) {
+                const float bn = epi_bias[warp - 4][lane];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int64_t m = mt0 + c;
+                    if (m < args.M) store_y(args.out, m * args.N + n, fmaf(epi_sa[warp - 4][c], y[c], bn));
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
 // A CTA that waits on a barrier nothing completes, to exercise the bounded-wait path.
 __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
     __shared__ uint64_t bar;
@@ -618,7 +1023,7 @@ __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
 
 template <typename Kernel>
 cudaError_t launch(Kernel kernel, int smem_bytes, bool* attr_done, int64_t tiles, const GemmArgs& a, int num_sms,
-                   cudaStream_t s) {
+                   cudaStream_t s, int threads = kThreads) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_done[dev]) {
@@ -629,7 +1034,7 @@ cudaError_t launch(Kernel kernel, int smem_bytes, bool* attr_done, int64_t tiles
     const int64_t grid = tiles < num_sms ? tiles : num_sms;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -648,13 +1053,54 @@ cudaError_t launch_gemm(const GemmArgs& a, bool debug, int num_sms, cudaStream_t
     const int64_t tiles_w = (a.N + kTileW - 1) / kTileW;
     if (a.tw == wide::kTN) {
         const int64_t tiles = ((a.M + wide::kTN - 1) / wide::kTN) * tiles_w;
-        return debug ? launch(gemm_wide_kernel<true>, wide::kSmemBytes, attr_done[3], tiles, a, num_sms, s)
-                     : launch(gemm_wide_kernel<false>, wide::kSmemBytes, attr_done[2], tiles, a, num_sms, s);
+        return debug ? launch(gemm_wide_kernel<true>, wide::kSmemBytes, attr_done[2], tiles, a, num_sms, s)
+                     : launch(gemm_wide_kernel<false>, wide::kSmemBytes, attr_done[1], tiles, a, num_sms, s);
     }
     if (a.tw != kTileT) return cudaErrorInvalidValue;
     const int64_t tiles = ((a.M + kTileT - 1) / kTileT) * tiles_w;
-    return debug ? launch(gemm_kernel<true>, kSmemBytes, attr_done[1], tiles, a, num_sms, s)
+    return debug ? launch(gemm_kernel<true>, kSmemBytes, attr_done[3], tiles, a, num_sms, s)
                  : launch(gemm_kernel<false>, kSmemBytes, attr_done[0], tiles, a, num_sms, s);
+}
+
+namespace {
+// cuTensorMapEncodeTiled, resolved once through the runtime (no link-time dependence on the
+// driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+}  // namespace
+
+cudaError_t launch_gemm_packed(const GemmArgs& a0, bool debug, int num_sms, cudaStream_t s) {
+    static bool attr_done[2][64] = {};
+    if (num_sms < 1 || a0.tw != kTileT || !a0.wq || (!debug && (!a0.s_w || !a0.z_w))) return cudaErrorInvalidValue;
+    const EncodeTiledFn enc = encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    GemmArgs a = a0;
+    // wq [N][K/2] bytes; a box is the 64 packed bytes (two 64-blocks) of 128 rows, 64-byte
+    // swizzled as the converters read it; rows past N read as zeros
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K / 2), static_cast<cuuint64_t>(a.N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K / 2)};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTileW)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&a.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.wq), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    const int64_t tiles = ((a.M + kTileT - 1) / kTileT) * ((a.N + kTileW - 1) / kTileW);
+    return debug ? launch(gemm_packed_kernel<true>, packed::kSmemBytes, attr_done[1], tiles, a, num_sms, s)
+                 : launch(gemm_packed_kernel<false>, packed::kSmemBytes, attr_done[0], tiles, a, num_sms, s);
 }
 
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s) {

@@ -14,6 +14,7 @@
 // The same launch also prepares the weight side in its extra CTAs (the u4 codes expanded
 // to the GEMM's e4m3 operand, the fp16 scales and zeros laid out for the epilogue and the
 // zero-point MMA), so a call costs two launches in total.
+#include "operand_codes.cuh"
 #include "quant_math.cuh"
 #include "sm103_ptx.cuh"
 #include "w4a8_internal.h"
@@ -115,15 +116,6 @@ __device__ __forceinline__ float half_warp_sums(const float (&p)[H], int lane, i
     return v;
 }
 
-// u4 pairs -> bytes in k order: nibbles k0..k7 of w become bytes of (o0: k0..k3, o1: k4..k7).
-// A byte holding the code q is the e4m3 encoding of q * 2^-9, the GEMM's weight operand.
-__device__ __forceinline__ void expand8(uint32_t w, uint32_t& o0, uint32_t& o1) {
-    const uint32_t lo = w & 0x0F0F0F0Fu;         // k0 k2 k4 k6
-    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;  // k1 k3 k5 k7
-    o0 = __byte_perm(lo, hi, 0x5140);
-    o1 = __byte_perm(lo, hi, 0x7362);
-}
-
 // Weight job (the weight records of w4a8_internal.h), spread over the CTAs past the row
 // CTAs.  One thread per (row n, block b), rows padded to a multiple of 128: the 32 packed
 // bytes expanded to 64 e4m3 bytes in 64-byte-swizzled order; then {-z_w, -z_w} (fp16 pair,
@@ -163,8 +155,7 @@ __device__ void weights_job(const PrepArgs& a, int64_t cta, int64_t ctas) {
             if (n < a.N) {
                 const int64_t src = (a.n_first + n) * nb + b;
                 sv = 512.0f * h2f(a.s_w[src]);
-                const uint32_t zb = static_cast<uint32_t>(a.z_w[src]) ^ 0x8000u;  // -z_w, exact
-                zz = zb | (zb << 16);
+                zz = neg_zero_pair(a.z_w[src]);
             }
             *reinterpret_cast<uint4*>(rec + kWZx + r * 16) = make_uint4(zz, 0u, 0u, 0u);
             a.sc[i] = sv;  // [tile][b][r]: the same linear index as the thread's item

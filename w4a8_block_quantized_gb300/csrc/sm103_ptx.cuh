@@ -1,6 +1,6 @@
 // sm103_ptx.cuh -- thin inline-PTX wrappers for the sm_103a features the kernels use:
-// mbarrier (with bounded waits), TMA bulk / tensor copies, tcgen05 (TMEM alloc, MMA,
-// commit, loads, fences).  Nothing here computes; it only names instructions.
+// mbarrier (with bounded waits), bulk copies and tiled TMA loads, tcgen05 (TMEM alloc,
+// MMA, commit, loads, fences).  Nothing here computes; it only names instructions.
 #pragma once
 
 #include <cstdint>
@@ -116,6 +116,22 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
             smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// Tiled TMA load of a 2-D box at element coordinates (x inner, y outer) of `map` into shared
+// memory, completing `bar`'s transaction bytes (the whole box, including any part of it that
+// lies outside the tensor and is filled with zeros).  x times the element size must be a
+// multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05

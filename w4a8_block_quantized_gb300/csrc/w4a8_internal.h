@@ -131,16 +131,28 @@ struct GemmArgs {
     int tw = 128;                       // token tile (record width): 128 or 256
     const uint8_t* wrec = nullptr;      // weight records [ceil(N/128)][K/64]
     const float* sc = nullptr;          // weight scales [ceil(N/128)][K/64][128]
+    // packed-weight form (128-token tiles): the caller's wq [N][K/2], s_w and z_w [N][K/64],
+    // read by the contraction itself (wmap: a tiled TMA map over wq, filled by the launcher)
+    const uint8_t* wq = nullptr;
+    const uint16_t* s_w = nullptr;
+    const uint16_t* z_w = nullptr;
+    int early = 0;                      // the previous kernel in the stream writes none of wq / s_w / z_w
     const float* s_a = nullptr;
     const float* bias = nullptr;
     OutSpec out;                        // y [M][N]
     int32_t* acc = nullptr;             // debug: [M][N][K/64]
     uint32_t* status = nullptr;
     uint64_t wait_limit_ns = 1000000000ull;
+    CUtensorMap wmap{};
 };
 
-// Persistent launch over ceil(M/tw) x ceil(N/128) output tiles on at most `num_sms` CTAs.
+// Persistent launch over ceil(M/tw) x ceil(N/128) output tiles on at most `num_sms` CTAs, from
+// weight records (wrec, sc).
 cudaError_t launch_gemm(const GemmArgs& a, bool debug, int num_sms, cudaStream_t s);
+// The same contraction with 128-token tiles straight from the packed weights (wq, s_w, z_w): the
+// u4 codes are staged by TMA and expanded to the tensor-core operand in shared memory.  With
+// `early` set the weights are staged before the previous kernel in the stream has finished.
+cudaError_t launch_gemm_packed(const GemmArgs& a, bool debug, int num_sms, cudaStream_t s);
 
 // ---------------------------------------------------------------- few-token (decode) form
 // Up to kGemvMaxM tokens (and a K whose staged activations fit on chip): the packed weights
