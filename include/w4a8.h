@@ -103,6 +103,29 @@ int w4a8_prefill_linear(const float *x, const uint8_t *wq, const uint16_t *w_sca
                         int64_t M, int64_t N, int64_t K,
                         void *workspace, size_t workspace_bytes, void *stream);
 
+/* A sequence of fused calls (section 4: a decoder layer's linears) in one library call: the
+ * same as w4a8_prefill_linear on each entry in order, on `stream`, bit for bit, with one M
+ * for all.  The library then knows that from the second entry on the previous kernel in the
+ * stream is its own, which never writes the caller's weights; so a few-token kernel (M <=
+ * W4A8_DECODE_MAX_M) starts streaming its weights while the previous entry's kernel is still
+ * running (a programmatic dependent launch), which hides most of the fixed start-up cost of
+ * each launch.  Consequently no entry's y may overlap a later entry's wq, w_scale or w_zero
+ * (an entry's x may be an earlier entry's y: activations are read only after the previous
+ * kernel has finished).  Every entry is checked before anything is launched; the first
+ * failing check's status is returned. */
+typedef struct w4a8_linear_ref {
+    const float *x;            /* fp32 [M][K] */
+    const uint8_t *wq;         /* [N][K/2] */
+    const uint16_t *w_scale;   /* fp16 bits [N][K/64] */
+    const uint16_t *w_zero;    /* fp16 bits [N][K/64] */
+    const float *bias;         /* fp32 [N] or NULL */
+    float *y;                  /* fp32 [M][N] */
+    int64_t N, K;
+    void *workspace;           /* at least w4a8_prefill_workspace_bytes(M, N, K) bytes */
+    size_t workspace_bytes;
+} w4a8_linear_ref;
+int w4a8_prefill_linear_batch(const w4a8_linear_ref *linears, int64_t count, int64_t M, void *stream);
+
 /* Split form of w4a8_prefill_linear, for callers that reuse one side across calls
  * (one activation pre-pass shared by several linears that read the same input, or
  * weights prepared once at load time):

@@ -506,6 +506,56 @@ def test_decode_offset_scale_views(M, K, N):
     assert b.sync_status() == 0
 
 
+@pytest.mark.parametrize("M", [1, 3, 8, 300])
+def test_batch_equals_separate_calls(M):
+    """w4a8_prefill_linear_batch over a decoder layer's linears (hidden 2048: q/k/v and gate/up
+    as row-concatenated groups, o, down) and one more entry whose x is the previous entry's y:
+    every y equals the separate fused call's bit for bit (few-token kernels after the first
+    stream their weights while the previous kernel runs), and lies within tolerance of the
+    oracle."""
+    b = B()
+    shapes = [(2048, 4096), (2048, 2048), (2048, 12288), (6144, 2048)]
+    ds = [synth.random_small(M, K, N, seed=200 + i, bias=i == 0) for i, (K, N) in enumerate(shapes)]
+    gs = [inputs_to_dev(d) for d in ds]
+    ents = [dict(x=g["x"], wq=g["wq"], s_w=g["s_w"], z_w=g["z_w"], bias=g["bias"]) for g in gs]
+    # a fifth entry reading the fourth's output (K 2048 = the fourth's N)
+    d5 = synth.random_small(M, 2048, 512, seed=205, bias=True)
+    g5 = inputs_to_dev(d5)
+    ents.append(dict(x=None, wq=g5["wq"], s_w=g5["s_w"], z_w=g5["z_w"], bias=g5["bias"]))
+    y4 = torch.empty((M, 2048), device=dev())
+    ents[3]["y"] = y4
+    ents[4]["x"] = y4
+    ys = b.prefill_linear_batch(ents)
+    torch.cuda.synchronize()
+    for i, (e, y) in enumerate(zip(ents, ys)):
+        ref = b.prefill_linear(e["x"], e["wq"], e["s_w"], e["z_w"], e["bias"])
+        assert torch.equal(y, ref), f"entry {i}"
+    for i, (d, y) in enumerate(zip(ds, ys)):
+        y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
+        check_y(y, y_ref, bound, f"batch entry {i} M={M}")
+    assert b.sync_status() == 0
+
+
+def test_batch_rejects_before_launch():
+    """An invalid entry anywhere in the batch: its status, and no entry's y is written."""
+    b = B()
+    d = synth.random_small(1, 1024, 256, seed=7, bias=False)
+    g = inputs_to_dev(d)
+    lib = b.load()
+    ys = [torch.full((1, 256), 3.0, device=dev()) for _ in range(2)]
+    refs = (b.LinearRef * 2)()
+    for i in range(2):
+        refs[i] = b.LinearRef(g["x"].data_ptr(), g["wq"].data_ptr(), g["s_w"].data_ptr(), g["z_w"].data_ptr(), None,
+                              ys[i].data_ptr(), 256, 1024, None, 0)
+    refs[1].K = 1000                                      # not a multiple of 64
+    import ctypes
+    assert lib.w4a8_prefill_linear_batch(ctypes.cast(refs, ctypes.c_void_p), 2, 1, b._stream(None)) == \
+        b.W4A8_ERR_SHAPE
+    torch.cuda.synchronize()
+    assert all(bool((y == 3.0).all()) for y in ys)
+    assert b.sync_status() == 0
+
+
 def test_decode_boundary_tokens():
     """8 tokens take the weight-streaming form, 9 the tensor-core form: both within the
     tolerance of the same definition on the same rows."""

@@ -38,6 +38,7 @@ SIGNATURES = {
     "w4a8_linear": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "w4a8_prefill_linear": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "w4a8_prefill_linear_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "w4a8_prefill_linear_batch": (ctypes.c_int, [_P, _I64, _I64, _P]),
     "w4a8_prepare_activations": (ctypes.c_int, [_P, _I64, _I64, _P, _SZ, _P]),
     "w4a8_prepare_weights": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _SZ, _P]),
     "w4a8_linear_prepared": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
@@ -258,6 +259,53 @@ def prefill_linear(x, wq, w_scale, w_zero, bias=None, y=None, ws=None, stream=No
                                     M, N, K, _ptr(ws), _nbytes(ws), _stream(stream))
     _check(rc, "w4a8_prefill_linear")
     return y
+
+
+class LinearRef(ctypes.Structure):
+    """w4a8_linear_ref: one entry of w4a8_prefill_linear_batch."""
+    _fields_ = [("x", _P), ("wq", _P), ("w_scale", _P), ("w_zero", _P), ("bias", _P), ("y", _P),
+                ("N", _I64), ("K", _I64), ("workspace", _P), ("workspace_bytes", _SZ)]
+
+
+class Batch:
+    """The entries of a w4a8_prefill_linear_batch call, checked and marshalled once: a sequence
+    of dicts with x, wq, s_w, z_w, optional bias, y and ws (y and ws allocated when absent),
+    one M for all.  `run(stream)` makes the call; `ys` are the outputs.  The tensors are held
+    for the life of the object."""
+
+    def __init__(self, entries, stream=None):
+        entries = list(entries)
+        self.count = len(entries)
+        self.refs = (LinearRef * max(1, self.count))()
+        self.keep, self.ys = [], []
+        self.M = 0
+        for i, e in enumerate(entries):
+            x, wq, sw, zw, bias = e["x"], e["wq"], e["s_w"], e["z_w"], e.get("bias")
+            m, N, K = _prefill_args(x, wq, sw, zw, bias)
+            if i == 0:
+                self.M = m
+            elif m != self.M:
+                raise ValueError(f"entry {i}: x has {m} rows, the batch {self.M}")
+            y = e.get("y")
+            y = torch.empty((m, N), dtype=torch.float32, device=x.device) if y is None else y
+            _arg(y, torch.float32, (m, N), "y", x.device)
+            ws = _ws(e.get("ws"), prefill_workspace_bytes(m, N, K), x.device, stream)
+            self.refs[i] = LinearRef(x.data_ptr(), wq.data_ptr(), sw.data_ptr(), zw.data_ptr(),
+                                     None if bias is None else bias.data_ptr(), y.data_ptr(), N, K, ws.data_ptr(),
+                                     _nbytes(ws))
+            self.keep += [x, wq, sw, zw, bias, ws]
+            self.ys.append(y)
+
+    def run(self, stream=None):
+        rc = load().w4a8_prefill_linear_batch(ctypes.cast(self.refs, _P), self.count, self.M, _stream(stream))
+        _check(rc, "w4a8_prefill_linear_batch")
+        return self.ys
+
+
+def prefill_linear_batch(entries, stream=None):
+    """w4a8_prefill_linear_batch: the fused call on each entry in order (see Batch).  Returns
+    the list of y."""
+    return Batch(entries, stream).run(stream)
 
 
 def prefill_linear_noalloc(x, wq, w_scale, w_zero, bias=None, y=None, stream=None):

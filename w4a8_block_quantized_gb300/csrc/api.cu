@@ -162,8 +162,9 @@ size_t prefill_ws(int64_t M, int64_t N, int64_t K) {
 // The few-token kernel from x (it quantizes) or from the pre-pass outputs.
 int run_gemv(const float* x, const int8_t* a_q, const float* s_a, const int32_t* rs, const uint8_t* wq,
              const uint16_t* w_scale, const uint16_t* w_zero, const float* bias, const OutSpec& out, int64_t M,
-             int64_t N, int64_t K, const DeviceInfo& d, cudaStream_t st) {
+             int64_t N, int64_t K, const DeviceInfo& d, cudaStream_t st, bool early = false) {
     GemvArgs g;
+    g.early = early ? 1 : 0;
     g.x = x;
     g.a_q = a_q;
     g.s_a = s_a;
@@ -201,7 +202,10 @@ int linear_impl(const int8_t* a_q, const float* a_scale, const int32_t* rowsum, 
                 int64_t N, int64_t K, void* workspace, size_t workspace_bytes, void* stream);
 int prefill_impl(const float* x, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero,
                  const float* bias, const OutSpec& out, int64_t M, int64_t N, int64_t K, void* workspace,
-                 size_t workspace_bytes, void* stream);
+                 size_t workspace_bytes, void* stream, bool after_own = false);
+int prefill_check(const float* x, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero,
+                  const float* bias, const void* y, int64_t M, int64_t N, int64_t K, const void* workspace,
+                  size_t workspace_bytes);
 int linear_prepared_impl(const void* act, const void* pw, const float* bias, const OutSpec& out, int64_t M,
                          int64_t N, int64_t K, void* stream);
 
@@ -336,26 +340,37 @@ int linear_impl(const int8_t* a_q, const float* a_scale, const int32_t* rowsum, 
     return run_linear(ws + L.act.rec, a_scale, ws + L.w_off, bias, out, M, N, K, L.act.tw, *d, st);
 }
 
-int prefill_impl(const float* x, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero,
-                 const float* bias, const OutSpec& out, int64_t M, int64_t N, int64_t K, void* workspace,
-                 size_t workspace_bytes, void* stream) {
+// Argument checks of the fused call (everything but the device).
+int prefill_check(const float* x, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero,
+                  const float* bias, const void* y, int64_t M, int64_t N, int64_t K, const void* workspace,
+                  size_t workspace_bytes) {
     int rc = check_shape(M, N, K);
     if (rc != W4A8_OK) return rc;
     if (M == 0 || N == 0) return W4A8_OK;
-    if (!x || !wq || !w_scale || !w_zero || !out.y) return W4A8_ERR_ARG;
-    if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(out.y, 16) || !aligned(w_scale, 2) || !aligned(w_zero, 2) ||
+    if (!x || !wq || !w_scale || !w_zero || !y) return W4A8_ERR_ARG;
+    if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(y, 16) || !aligned(w_scale, 2) || !aligned(w_zero, 2) ||
         (bias && !aligned(bias, 4)))
         return W4A8_ERR_ALIGN;
     const size_t need = prefill_ws(M, N, K);
     if (need > 0 && (!workspace || workspace_bytes < need)) return W4A8_ERR_WORKSPACE;
     if (need > 0 && !aligned(workspace, 16)) return W4A8_ERR_ALIGN;
+    return W4A8_OK;
+}
+
+// `after_own`: the previous kernel in the stream is one of this library's, which never writes
+// the caller's weights, so a few-token kernel may start streaming them before it has finished.
+int prefill_impl(const float* x, const uint8_t* wq, const uint16_t* w_scale, const uint16_t* w_zero,
+                 const float* bias, const OutSpec& out, int64_t M, int64_t N, int64_t K, void* workspace,
+                 size_t workspace_bytes, void* stream, bool after_own) {
+    int rc = prefill_check(x, wq, w_scale, w_zero, bias, out.y, M, N, K, workspace, workspace_bytes);
+    if (rc != W4A8_OK || M == 0 || N == 0) return rc;
     DeviceInfo* d = nullptr;
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     if (few_tokens(M, K) && gemv_quantizes(M, K)) {
         // few-token form, one launch: the weight-streaming kernel quantizes x itself
-        return run_gemv(x, nullptr, nullptr, nullptr, wq, w_scale, w_zero, bias, out, M, N, K, *d, st);
+        return run_gemv(x, nullptr, nullptr, nullptr, wq, w_scale, w_zero, bias, out, M, N, K, *d, st, after_own);
     }
     if (few_tokens(M, K)) {
         // few-token form: the pre-pass in the API layout, then the weight-streaming kernel
@@ -368,7 +383,9 @@ int prefill_impl(const float* x, const uint8_t* wq, const uint16_t* w_scale, con
         p.s_a_out = reinterpret_cast<float*>(ws + D.s_a);
         p.rs_out = reinterpret_cast<int32_t*>(ws + D.rs);
         if (launch_quant(p, st) != cudaSuccess) return W4A8_ERR_CUDA;
-        return run_gemv(nullptr, p.a_q_out, p.s_a_out, p.rs_out, wq, w_scale, w_zero, bias, out, M, N, K, *d, st);
+        // the previous kernel is the pre-pass: the weights may stream while it runs
+        return run_gemv(nullptr, p.a_q_out, p.s_a_out, p.rs_out, wq, w_scale, w_zero, bias, out, M, N, K, *d, st,
+                        true);
     }
     const CallLayout L = call_layout(M, N, K, true);
     float* s_a = reinterpret_cast<float*>(ws + L.act.s_a);
@@ -418,6 +435,27 @@ int w4a8_prefill_linear_ex(const float* x, const uint8_t* wq, const uint16_t* w_
     const int rc = make_out(y, out_dtype, clamp_lo, clamp_hi, &o);
     if (rc != W4A8_OK) return rc;
     return prefill_impl(x, wq, w_scale, w_zero, bias, o, M, N, K, workspace, workspace_bytes, stream);
+}
+
+int w4a8_prefill_linear_batch(const w4a8_linear_ref* linears, int64_t count, int64_t M, void* stream) {
+    if (count < 0 || (count > 0 && !linears)) return W4A8_ERR_ARG;
+    // every entry is checked before anything is launched
+    for (int64_t i = 0; i < count; ++i) {
+        const w4a8_linear_ref& l = linears[i];
+        const int rc = prefill_check(l.x, l.wq, l.w_scale, l.w_zero, l.bias, l.y, M, l.N, l.K, l.workspace,
+                                     l.workspace_bytes);
+        if (rc != W4A8_OK) return rc;
+    }
+    bool launched = false;  // a kernel of this call is the previous one in the stream
+    for (int64_t i = 0; i < count; ++i) {
+        const w4a8_linear_ref& l = linears[i];
+        if (M == 0 || l.N == 0) continue;
+        const int rc = prefill_impl(l.x, l.wq, l.w_scale, l.w_zero, l.bias, f32_out(l.y), M, l.N, l.K, l.workspace,
+                                    l.workspace_bytes, stream, launched);
+        if (rc != W4A8_OK) return rc;
+        launched = true;
+    }
+    return W4A8_OK;
 }
 
 int w4a8_prepare_activations(const float* x, int64_t M, int64_t K, void* act, size_t act_bytes, void* stream) {

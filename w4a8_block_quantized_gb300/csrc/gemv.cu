@@ -14,7 +14,7 @@
 //   warp 8       producer: per tile three bulk copies into a ring of shared-memory stages --
 //                the tile's packed rows (contiguous: rows are K/2 bytes apart) and the
 //                16-byte-aligned interiors of its s_w and z_w rows (the few elements before
-//                and after an interior are read from global memory by the consumers, so
+//                and after an interior are copied from global memory by the consumers, so
 //                nothing outside the caller's arrays is touched).
 //   warps 0-7    consumers.  A tile of TR >= 8 rows gives each warp TR/8 rows; a tile of
 //                TR < 8 rows gives each row 8/TR warps that split its K chunks.  A lane owns
@@ -176,11 +176,30 @@ __device__ __forceinline__ HalfSpan half_span(const uint16_t* base, int64_t e0, 
     return h;
 }
 
-// fp16 element at byte offset e of a staged span (slot base `slot`, element e0 at `gsrc`):
-// from shared memory inside the copied interior, else from global memory.
-__device__ __forceinline__ float span_elem(uint32_t slot, const HalfSpan& h, const uint16_t* gsrc, uint32_t e) {
-    const uint16_t v = e - h.lo < h.hi - h.lo ? lds16(slot + h.skew + e) : __ldg(gsrc + e / 2);
-    return __half2float(__ushort_as_half(v));
+// Whether the span of elements [e0, e1) of `base` begins and ends on a 16-byte boundary (its
+// interior copy is then the whole span).
+__device__ __forceinline__ bool span_whole(const uint16_t* base, int64_t e0, int64_t e1) {
+    return ((reinterpret_cast<uintptr_t>(base + e0) | reinterpret_cast<uintptr_t>(base + e1)) & 15) == 0;
+}
+
+// The elements of a staged span that its interior copy left out (the at most 7 before and 7
+// after the interior, when the span does not begin or end on a 16-byte boundary), loaded from
+// global memory into the slot by consumer thread t < 32: threads 0-15 for the scales, 16-31 for
+// the zero points.  The caller synchronizes the consumers afterwards.
+__device__ __forceinline__ void fill_ragged(uint32_t s_slot, uint32_t z_slot, const uint16_t* s_w, const uint16_t* z_w,
+                                            int64_t e0, int64_t e1, int t) {
+    if (t >= 32) return;
+    const bool zs = t >= 16;
+    const uint16_t* base = zs ? z_w : s_w;
+    const HalfSpan h = half_span(base, e0, e1);
+    const uint32_t span = static_cast<uint32_t>((e1 - e0) * 2);
+    const uint32_t k = static_cast<uint32_t>(t & 15), head = h.lo / 2;
+    // head elements at byte offsets 0, 2, .., lo - 2; then the tail from hi on
+    const uint32_t eo = k < head ? 2 * k : h.hi + 2 * (k - head);
+    if (eo < span && (k < head || eo >= h.hi)) {
+        const uint16_t v = __ldg(base + e0 + eo / 2);
+        asm volatile("st.shared.u16 [%0], %1;" ::"r"((zs ? z_slot : s_slot) + h.skew + eo), "h"(v) : "memory");
+    }
 }
 
 // A float code (an exact integer in [-127, 127]) as a word whose low byte is the code in two's
@@ -255,22 +274,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (warp == kCW) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            griddep_wait();
-            if (a.x) {
-                // the rows to quantize go first: every CTA reads them, ahead of its weights
-                const uint32_t xbytes = static_cast<uint32_t>(MT * K * 4);
-                mbar_arrive_expect_tx(xbar, xbytes);
-                bulk_load(smem + P.x_off, a.x, xbytes, xbar);
-            }
-            uint32_t i = 0;
-            bool ok = true;
-            for (; i < my_tiles; ++i) {
-                const int s = static_cast<int>(i % ns);
-                const uint32_t k = i / ns;
-                if (k > 0 && !mbar_wait(&empty[s], (k - 1) & 1, ctl)) {
-                    ok = false;
-                    break;
-                }
+            // The weights are read-only inputs: when the previous kernel cannot have written them
+            // (`early`), the first stages' copies go out before it has finished, so this kernel's
+            // weight stream overlaps its tail.  Everything else waits for it.
+            auto issue_tile = [&](uint32_t i, int s) {
                 const int64_t n0 = (blockIdx.x + static_cast<int64_t>(i) * gridDim.x) * tr;
                 const int64_t rows = N - n0 < tr ? N - n0 : tr;
                 const uint32_t wbytes = static_cast<uint32_t>(rows * (K / 2));
@@ -281,6 +288,26 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 bulk_load(st, a.wq + n0 * (K / 2), wbytes, &full[s]);
                 if (hs.bytes) bulk_load(st + P.w_bytes + hs.skew + hs.lo, hs.src, hs.bytes, &full[s]);
                 if (hz.bytes) bulk_load(st + P.w_bytes + P.sz_bytes + hz.skew + hz.lo, hz.src, hz.bytes, &full[s]);
+            };
+            uint32_t i = 0;
+            if (a.early)
+                for (; i < my_tiles && i < static_cast<uint32_t>(ns); ++i) issue_tile(i, static_cast<int>(i));
+            griddep_wait();
+            if (a.x) {
+                // the rows to quantize: every CTA reads them (the first copy unless weights went early)
+                const uint32_t xbytes = static_cast<uint32_t>(MT * K * 4);
+                mbar_arrive_expect_tx(xbar, xbytes);
+                bulk_load(smem + P.x_off, a.x, xbytes, xbar);
+            }
+            bool ok = true;
+            for (; i < my_tiles; ++i) {
+                const int s = static_cast<int>(i % ns);
+                const uint32_t k = i / ns;
+                if (k > 0 && !mbar_wait(&empty[s], (k - 1) & 1, ctl)) {
+                    ok = false;
+                    break;
+                }
+                issue_tile(i, s);
             }
             if (!ok || *abort_flag) {
                 // let the copies already issued land before the CTA exits
@@ -395,10 +422,19 @@ __global__ void __launch_bounds__(kGThreads, 1)
             const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (i / ns) & 1, ctl));
             const uint32_t st = smem_u32(smem + P.stage_off + s * P.stage_bytes);
             const int64_t rows = N - n0 < tr ? N - n0 : tr;
-            const HalfSpan hs = half_span(a.s_w, n0 * nb, (n0 + rows) * nb);
-            const HalfSpan hz = half_span(a.z_w, n0 * nb, (n0 + rows) * nb);
-            const uint32_t swb = st + P.w_bytes, zwb = st + P.w_bytes + P.sz_bytes;
-            const uint16_t *sws = a.s_w + n0 * nb, *zws = a.z_w + n0 * nb;
+            // each span's element e0 sits at its slot offset `skew`; a span that does not begin
+            // and end on a 16-byte boundary (possible when K is not a multiple of 512, or for
+            // arrays that do not start on one) has its ragged ends filled in from global memory
+            const int64_t e0 = n0 * nb, e1 = (n0 + rows) * nb;
+            const uint32_t s_slot = st + P.w_bytes, z_slot = st + P.w_bytes + P.sz_bytes;
+            const uint32_t swb = s_slot + static_cast<uint32_t>(reinterpret_cast<uintptr_t>(a.s_w + e0) & 15);
+            const uint32_t zwb = z_slot + static_cast<uint32_t>(reinterpret_cast<uintptr_t>(a.z_w + e0) & 15);
+            if (!(span_whole(a.s_w, e0, e1) && span_whole(a.z_w, e0, e1))) {  // the same for every consumer
+                fill_ragged(s_slot, z_slot, a.s_w, a.z_w, e0, e1, static_cast<int>(threadIdx.x));
+                // the slot is reloaded by a bulk copy (async proxy) after the stage is released
+                fence_proxy_async_smem();
+                named_bar_sync(kBarStage, kCW * 32);
+            }
             // the rows of this warp in the tile: r_j = warp + 8 j (tr >= 8) or rslot (tr < 8)
             int rrow[RW];
             bool rok[RW];
@@ -425,8 +461,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
                         W0[j] = on ? lds128(wa) : make_uint4(0, 0, 0, 0);
                         W1[j] = on ? lds128(wa + 16) : make_uint4(0, 0, 0, 0);
                         const uint32_t e = (rrow[j] * nbu + b) * 2;
-                        sw[j] = on ? span_elem(swb, hs, sws, e) : 0.0f;
-                        nz[j] = on ? -span_elem(zwb, hz, zws, e) : 0.0f;
+                        sw[j] = on ? __half2float(__ushort_as_half(lds16(swb + e))) : 0.0f;
+                        nz[j] = on ? -__half2float(__ushort_as_half(lds16(zwb + e))) : 0.0f;
                     }
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {

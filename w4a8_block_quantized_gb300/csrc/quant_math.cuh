@@ -41,37 +41,27 @@ __device__ __forceinline__ float rint_flag(float t, bool& tie) {
     return q;
 }
 
-// One code by the definition (IEEE division, round half away from zero), for the rare
-// elements next to a rounding boundary.  Out of line and scalar: the division's code is then
-// not repeated in every quantizing loop body.
-static __device__ __noinline__ float requant(float x, float s) { return roundf(__fdiv_rn(x, s)); }
-
-// A code by the definition, clamp included, as a float: for the rows whose scale has no
-// finite reciprocal (below).  Out of line for the same reason as requant().
-static __device__ __noinline__ float quant_exact(float x, float s) { return static_cast<float>(quant1(x, s)); }
+// One code by the definition (IEEE division, round half away from zero, clamp to +-127), for the
+// rare elements next to a rounding boundary and for rows whose scale has no finite reciprocal.
+// Out of line and scalar: the division's code is then not repeated in every quantizing loop
+// body.  (For a scale with a finite reciprocal the clamp never binds: see quant_lane.)
+static __device__ __noinline__ float requant(float x, float s) {
+    return fminf(fmaxf(roundf(__fdiv_rn(x, s)), -127.0f), 127.0f);
+}
 
 // Quantize one lane's V float4 of a row to float codes; s > 0 is the row's scale and
 // r = RN(1/s).  No clamp is applied on the fast path: for finite inputs |x| <= absmax and
-// s = RN(absmax/127), so while s keeps at least 22 significant bits (s >= 2^-128, which
-// covers every s with a finite r) |x/s| <= 127 (1 + 2^-22) and no code can exceed 127 in
-// magnitude, exactly as the clamped definition gives.  The rare near-tie elements of the
-// warp are recomputed with the IEEE division (warp-uniform branch).  A scale below 2^-128
-// (absmax below about 127 * 2^-128) has no finite reciprocal, and deep in the subnormal
-// range so few significant bits that |x/s| can pass 127; such a row (uniform across the
-// warp) takes the definition element by element: IEEE division, round half away, clamp.
+// s = RN(absmax/127), so while s keeps at least 22 significant bits (s >= 2^-128, which covers
+// every s with a finite r) |x/s| <= 127 (1 + 2^-22) and no code can exceed 127 in magnitude,
+// exactly as the clamped definition gives.  The rare near-tie elements of the warp are
+// recomputed with the IEEE division (warp-uniform branch).  A scale below 2^-128 (absmax below
+// about 127 * 2^-128) has no finite reciprocal, and deep in the subnormal range so few
+// significant bits that |x/s| can pass 127; such a row (uniform across the warp) takes the
+// recompute for every element: IEEE division, round half away, clamp.
 template <int V>
 __device__ __forceinline__ void quant_lane(const float4 (&x)[V], float4 (&q)[V], float s, float r) {
-    if (!(r < __int_as_float(0x7f800000))) {
-#pragma unroll
-        for (int i = 0; i < V; ++i) {
-            q[i].x = quant_exact(x[i].x, s);
-            q[i].y = quant_exact(x[i].y, s);
-            q[i].z = quant_exact(x[i].z, s);
-            q[i].w = quant_exact(x[i].w, s);
-        }
-        return;
-    }
-    bool tie = false;
+    const bool tiny = !(r < __int_as_float(0x7f800000));
+    bool tie = tiny;
 #pragma unroll
     for (int i = 0; i < V; ++i) {
         q[i].x = rint_flag(x[i].x * r, tie);
@@ -82,10 +72,10 @@ __device__ __forceinline__ void quant_lane(const float4 (&x)[V], float4 (&q)[V],
     if (__any_sync(0xffffffffu, tie)) {
 #pragma unroll
         for (int i = 0; i < V; ++i) {
-            if (near_tie(x[i].x * r)) q[i].x = requant(x[i].x, s);
-            if (near_tie(x[i].y * r)) q[i].y = requant(x[i].y, s);
-            if (near_tie(x[i].z * r)) q[i].z = requant(x[i].z, s);
-            if (near_tie(x[i].w * r)) q[i].w = requant(x[i].w, s);
+            if (tiny || near_tie(x[i].x * r)) q[i].x = requant(x[i].x, s);
+            if (tiny || near_tie(x[i].y * r)) q[i].y = requant(x[i].y, s);
+            if (tiny || near_tie(x[i].z * r)) q[i].z = requant(x[i].z, s);
+            if (tiny || near_tie(x[i].w * r)) q[i].w = requant(x[i].w, s);
         }
     }
 }

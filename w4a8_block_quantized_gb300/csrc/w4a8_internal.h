@@ -171,6 +171,7 @@ struct GemvArgs {
     const float* bias = nullptr;
     OutSpec out;                        // y [M][N]
     int64_t M = 0, N = 0, K = 0;
+    int early = 0;                      // the previous kernel in the stream writes none of wq / s_w / z_w
 };
 
 // Scratch of the fused few-token call: the pre-pass outputs in the API layout.
