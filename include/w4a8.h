@@ -105,14 +105,20 @@ int w4a8_prefill_linear(const float *x, const uint8_t *wq, const uint16_t *w_sca
 
 /* A sequence of fused calls (section 4: a decoder layer's linears) in one library call: the
  * same as w4a8_prefill_linear on each entry in order, on `stream`, bit for bit, with one M
- * for all.  The library then knows that from the second entry on the previous kernel in the
- * stream is its own, which never writes the caller's weights; so a few-token kernel (M <=
- * W4A8_DECODE_MAX_M) starts streaming its weights while the previous entry's kernel is still
- * running (a programmatic dependent launch), which hides most of the fixed start-up cost of
- * each launch.  Consequently no entry's y may overlap a later entry's wq, w_scale or w_zero
- * (an entry's x may be an earlier entry's y: activations are read only after the previous
- * kernel has finished).  Every entry is checked before anything is launched; the first
- * failing check's status is returned. */
+ * for all.  Two ways the library uses what it then knows:
+ *   - Few tokens (M <= W4A8_DECODE_MAX_M), 3 to 8 entries whose rows the weight-streaming
+ *     kernel quantizes itself (M * K <= 16384) and whose activations fit one CTA together,
+ *     with no entry's y overlapping any x or another y: ONE launch walks the row tiles of all
+ *     entries as a single weight stream, so the kernel's start-up cost is paid once.  (Used
+ *     when each entry's own launch would give every output row one warp, so the sums run in
+ *     the same order and the outputs equal separate calls bit for bit.)
+ *   - Otherwise one launch per entry, in order; from the second entry on the previous kernel
+ *     is the library's own, which never writes the caller's weights, so a few-token kernel
+ *     starts streaming its weights before that kernel has finished (a programmatic dependent
+ *     launch).  An entry's x may be an earlier entry's y: activations are read only after the
+ *     previous kernel has finished.
+ * Either way no entry's y may overlap any entry's wq, w_scale or w_zero.  Every entry is
+ * checked before anything is launched; the first failing check's status is returned. */
 typedef struct w4a8_linear_ref {
     const float *x;            /* fp32 [M][K] */
     const uint8_t *wq;         /* [N][K/2] */

@@ -506,6 +506,28 @@ def test_decode_offset_scale_views(M, K, N):
     assert b.sync_status() == 0
 
 
+@pytest.mark.parametrize("M,K_N", [(1, ((2048, 4096), (2048, 2048), (2048, 12288), (6144, 2048))),
+                                   (1, ((4096, 14336), (14336, 4096))),
+                                   (2, ((1024, 3072), (2048, 1000), (1088, 257))),
+                                   (1, tuple((64 * (i + 1), 100 + 37 * i) for i in range(8))),
+                                   (1, tuple((1024, 512) for _ in range(9)))])
+def test_batch_of_independent_linears(M, K_N):
+    """Independent entries, which the few-token batch runs in one launch where they fit (a
+    decoder layer's four groups, the 7B-class pair, ragged K / odd N at two tokens, the most
+    entries one launch takes, and one entry more): every output equals the separate call's bit
+    for bit."""
+    b = B()
+    ds = [synth.random_small(M, K, N, seed=300 + 7 * i + K + N, bias=i % 2 == 0) for i, (K, N) in enumerate(K_N)]
+    gs = [inputs_to_dev(d) for d in ds]
+    ents = [dict(x=g["x"], wq=g["wq"], s_w=g["s_w"], z_w=g["z_w"], bias=g["bias"]) for g in gs]
+    ys = b.prefill_linear_batch(ents)
+    for i, (e, y, d) in enumerate(zip(ents, ys, ds)):
+        assert torch.equal(y, b.prefill_linear(e["x"], e["wq"], e["s_w"], e["z_w"], e["bias"])), f"entry {i}"
+        y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
+        check_y(y, y_ref, bound, f"entry {i}")
+    assert b.sync_status() == 0
+
+
 @pytest.mark.parametrize("M", [1, 3, 8, 300])
 def test_batch_equals_separate_calls(M):
     """w4a8_prefill_linear_batch over a decoder layer's linears (hidden 2048: q/k/v and gate/up

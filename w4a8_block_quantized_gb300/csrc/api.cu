@@ -446,6 +446,59 @@ int w4a8_prefill_linear_batch(const w4a8_linear_ref* linears, int64_t count, int
                                      l.workspace_bytes);
         if (rc != W4A8_OK) return rc;
     }
+    // Few tokens, every entry quantized by the weight-streaming kernel itself: one launch for
+    // all of them when their activations fit one CTA and each entry's own launch would give
+    // every output row one warp (then the sums run in the same order, and the outputs are those
+    // of separate calls bit for bit).  The start-up cost of a launch is then paid once.
+    // In one launch every CTA reads every entry's x before it writes any y, but CTAs run at
+    // different times: so no y may overlap an x or another y (an entry that reads an earlier
+    // entry's output takes the launch-per-entry path, where each kernel waits for the last).
+    auto overlap = [](const void* a, size_t an, const void* b, size_t bn) {
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+        return a0 < b0 + bn && b0 < a0 + an;
+    };
+    bool disjoint = true;
+    for (int64_t i = 0; i < count && disjoint; ++i) {
+        const w4a8_linear_ref& yi = linears[i];
+        const size_t ybytes = static_cast<size_t>(M) * static_cast<size_t>(yi.N) * 4u;
+        for (int64_t j = 0; j < count && disjoint; ++j) {
+            const w4a8_linear_ref& lj = linears[j];
+            const size_t xbytes = static_cast<size_t>(M) * static_cast<size_t>(lj.K) * 4u;
+            const size_t yjb = static_cast<size_t>(M) * static_cast<size_t>(lj.N) * 4u;
+            disjoint = !overlap(yi.y, ybytes, lj.x, xbytes) && (i == j || !overlap(yi.y, ybytes, lj.y, yjb));
+        }
+    }
+    if (disjoint && M >= 1 && M <= kGemvMaxM && count >= 1 && count <= kGemvMaxLinears) {
+        GemvArgs g[kGemvMaxLinears];
+        int n = 0;
+        bool one = true;
+        DeviceInfo* d = nullptr;
+        int rc = current_device(&d);
+        if (rc != W4A8_OK) return rc;
+        for (int64_t i = 0; i < count && one; ++i) {
+            const w4a8_linear_ref& l = linears[i];
+            if (l.N == 0) continue;
+            one = few_tokens(M, l.K) && gemv_quantizes(M, l.K);
+            GemvArgs& a = g[n++];
+            a.x = l.x;
+            a.wq = l.wq;
+            a.s_w = l.w_scale;
+            a.z_w = l.w_zero;
+            a.bias = l.bias;
+            a.out = f32_out(l.y);
+            a.M = M;
+            a.N = l.N;
+            a.K = l.K;
+            one = one && gemv_tile_rows(a, d->num_sms) >= 8;
+        }
+        // Measured: a decoder layer's four groups (and its seven linears) run faster in one
+        // launch, the 7B-class pair slower (staging both long rows leaves two weight stages), so
+        // one launch from three entries on.
+        if (one && n >= 3 && gemv_batch_fits(g, n))
+            return launch_gemv_batch(g, n, d->num_sms, d->status, static_cast<cudaStream_t>(stream)) == cudaSuccess
+                       ? W4A8_OK
+                       : W4A8_ERR_CUDA;
+    }
     bool launched = false;  // a kernel of this call is the previous one in the stream
     for (int64_t i = 0; i < count; ++i) {
         const w4a8_linear_ref& l = linears[i];

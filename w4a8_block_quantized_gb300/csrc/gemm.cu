@@ -93,16 +93,26 @@ static_assert((2 * kStages) % kIssuers == 0, "each stage slot must have one issu
 // Grouped raster over the output tiles: groups of kGroup token tiles, the token tile
 // varying fastest inside a group, so the CTAs running at one time share token and weight
 // tiles in L2.
-// The arithmetic is 32-bit (a 64-bit division is a long software sequence, and a producer thread
-// runs this on its critical path): the host keeps the tile count below 2^31, and tiles_w is at
-// most 2^24.
-constexpr uint32_t kGroup = 8;
+constexpr int64_t kGroup = 8;
 __device__ __forceinline__ void tile_at(int64_t t, int64_t tiles_t, int64_t tiles_w, int64_t& tt, int64_t& tw) {
+    const int64_t per = kGroup * tiles_w;
+    const int64_t grp = t / per, r = t - grp * per;
+    const int64_t g0 = grp * kGroup;
+    const int64_t gsz = tiles_t - g0 < kGroup ? tiles_t - g0 : kGroup;
+    tt = g0 + r % gsz;
+    tw = r / gsz;
+}
+
+// The same tile in 32-bit arithmetic, for the packed kernel, whose producer thread computed it
+// on its critical path (three 64-bit divisions, a long software sequence, per copy).  The host
+// keeps the tile count below 2^31 and tiles_w is at most 2^24.  The record kernels keep the
+// 64-bit form: measured, the 32-bit one made the 256-token kernel about 4% slower.
+__device__ __forceinline__ void tile_at32(int64_t t, int64_t tiles_t, int64_t tiles_w, int64_t& tt, int64_t& tw) {
     const uint32_t t32 = static_cast<uint32_t>(t), tt32 = static_cast<uint32_t>(tiles_t);
-    const uint32_t per = kGroup * static_cast<uint32_t>(tiles_w);
+    const uint32_t per = static_cast<uint32_t>(kGroup) * static_cast<uint32_t>(tiles_w);
     const uint32_t grp = t32 / per, r = t32 - grp * per;
-    const uint32_t g0 = grp * kGroup;
-    const uint32_t gsz = tt32 - g0 < kGroup ? tt32 - g0 : kGroup;
+    const uint32_t g0 = grp * static_cast<uint32_t>(kGroup);
+    const uint32_t gsz = tt32 - g0 < static_cast<uint32_t>(kGroup) ? tt32 - g0 : static_cast<uint32_t>(kGroup);
     const uint32_t q = r / gsz;
     tt = g0 + (r - q * gsz);
     tw = q;
@@ -677,7 +687,7 @@ struct StageCursor {
 
 __device__ __forceinline__ void cursor_tile(StageCursor& c, uint32_t my_tiles, int64_t first, int64_t tiles_t,
                                             int64_t tiles_w) {
-    if (c.i < my_tiles) tile_at(first + static_cast<int64_t>(c.i) * gridDim.x, tiles_t, tiles_w, c.tt, c.tw);
+    if (c.i < my_tiles) tile_at32(first + static_cast<int64_t>(c.i) * gridDim.x, tiles_t, tiles_w, c.tt, c.tw);
 }
 
 __device__ __forceinline__ void cursor_next(StageCursor& c, uint32_t spt, uint32_t my_tiles, int64_t first,
@@ -722,7 +732,7 @@ __device__ __forceinline__ bool expand_stage(const GemmArgs& args, uint8_t* smem
     const int xr = et >> 2, xc = et & 3, xsw = (xr >> 1) & 3;
     const uint32_t ti = jj / spt, p = jj - ti * spt;
     int64_t tt, tw;
-    tile_at(first + static_cast<int64_t>(ti) * gridDim.x, tiles_t, tiles_w, tt, tw);
+    tile_at32(first + static_cast<int64_t>(ti) * gridDim.x, tiles_t, tiles_w, tt, tw);
     const int64_t n = tw * kTileW + xr;
     const uint32_t b = 2 * p + (xc >> 1);
     const bool live = b < nb;
@@ -905,14 +915,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
         uint32_t j = 0;  // stage counter of this CTA
         for (uint32_t i = 0; ok && i < my_tiles; ++i) {
             int64_t tt, tw;
-            tile_at(first + static_cast<int64_t>(i) * gridDim.x, tiles_t, tiles_w, tt, tw);
+            tile_at32(first + static_cast<int64_t>(i) * gridDim.x, tiles_t, tiles_w, tt, tw);
             const int64_t mt0 = tt * kTileT + h * 32;  // first token column of this warp
             const int64_t n = tw * kTileW + row;       // this thread's weight row
             const uint16_t* swr = (!DEBUG && n < args.N) ? args.s_w + n * nb : nullptr;
             if (!DEBUG && i + 1 < my_tiles && h == 0) {
                 // the next tile's scales and zero points into L2 while this tile runs
                 int64_t tt1, tw1;
-                tile_at(first + static_cast<int64_t>(i + 1) * gridDim.x, tiles_t, tiles_w, tt1, tw1);
+                tile_at32(first + static_cast<int64_t>(i + 1) * gridDim.x, tiles_t, tiles_w, tt1, tw1);
                 const int64_t n1 = tw1 * kTileW + row;
                 if (n1 < args.N) {
                     prefetch_l2_span(args.s_w + n1 * nb, nb * 2);

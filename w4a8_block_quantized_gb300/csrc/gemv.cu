@@ -40,6 +40,8 @@
 #include "sm103_ptx.cuh"
 #include "w4a8_internal.h"
 
+#include <algorithm>
+
 namespace w4a8 {
 namespace {
 
@@ -52,14 +54,45 @@ constexpr int kSmemCap = 226 * 1024;  // dynamic; the static arrays fit in the l
 constexpr int kBarStage = 9;          // named barrier: the consumers while staging
 // named barriers 1..4: the warps sharing one row of a tile of fewer than 8 rows
 
-// Shared-memory plan of one launch (computed on the host; identical for every CTA).
+// One linear of a launch as the kernel sees it: the caller's arrays, and where its staged
+// activations (token-major planes), block row sums (floats) and fp32 rows (quantizing launch)
+// sit in shared memory.  Its row tiles are tiles tile0 .. tile0 + ceil(N / tr) - 1 of the
+// launch.
+struct GemvLin {
+    const float* x;
+    const int8_t* a_q;
+    const float* s_a;
+    const int32_t* rs;
+    const uint8_t* wq;
+    const uint16_t* s_w;
+    const uint16_t* z_w;
+    const float* bias;
+    OutSpec out;
+    int64_t N, K;
+    int64_t tile0;
+    uint32_t act_off, rs_off, x_off;
+    uint32_t act_stride;  // staged activation bytes per token (chunks * 2048)
+    int chunks;           // ceil(K / 2048)
+    int tr;               // rows per tile of this linear
+};
+
+// The linears of a launch (one M), read by the kernel from parameter space.
+struct GemvBatch {
+    GemvLin lin[kGemvMaxLinears];
+    int count = 0;
+    int quantize = 0;  // every linear's rows are quantized in the kernel (x), else read (a_q, s_a, rs)
+    int early = 0;     // the previous kernel in the stream writes none of the weights
+};
+
+// Shared-memory plan of one launch (computed on the host; identical for every CTA).  One tile
+// height for all linears (chosen over all their tiles; the measured alternative, each linear's
+// own height, balanced a decoder layer's tiles worse over the CTAs); a stage slot holds the
+// largest linear's tile.
 struct GemvPlan {
     int tr = 8;               // rows per tile
     int wpr = 1;              // warps per row (tr < 8)
     int ns = 2;               // stages
-    int chunks = 1;           // ceil(K / 2048)
-    uint32_t act_stride = 0;  // staged activation bytes per token (chunks * 2048)
-    uint32_t rs_off = 0, x_off = 0, bar_off = 0, stage_off = 0;  // x_off: the fp32 rows (quantizing kernel)
+    uint32_t bar_off = 0, stage_off = 0;
     uint32_t stage_bytes = 0, w_bytes = 0, sz_bytes = 0;  // a stage; its weight part; one s_w / z_w slot
     uint32_t smem = 0;
     int64_t tiles = 0;
@@ -68,28 +101,56 @@ struct GemvPlan {
 
 constexpr uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
-bool make_plan(int64_t M, int64_t N, int64_t K, bool quantize, int num_sms, GemvPlan* out) {
+// Lays out the linears' staging areas (into b) and picks the tile height; false if they do not
+// fit one CTA's shared memory next to two weight stages.
+// `min_tr`: the smallest tile height allowed.  Heights of 8 rows and more give every output row
+// one warp, whose sum runs in the same order whatever the height; a launch of several linears
+// uses only those, so its outputs equal each linear's own launch bit for bit when that launch
+// also has one warp per row.
+bool make_plan(const GemvArgs* a, int count, bool quantize, int num_sms, GemvBatch* b, GemvPlan* out,
+               int min_tr = 1) {
+    if (count < 1 || count > kGemvMaxLinears) return false;
+    const int64_t M = a[0].M;
+    int64_t off = 0;
+    for (int i = 0; i < count; ++i) {  // activations, then row sums, then fp32 rows
+        const int64_t nb = a[i].K / kBlock;
+        const int chunks = static_cast<int>((nb + kChunkBlocks - 1) / kChunkBlocks);
+        b->lin[i].chunks = chunks;
+        b->lin[i].act_stride = static_cast<uint32_t>(chunks) * kChunkAct;
+        b->lin[i].act_off = static_cast<uint32_t>(off);
+        off = align_up(static_cast<uint32_t>(off + M * chunks * kChunkAct), 128);
+        if (off > kSmemCap) return false;
+    }
+    for (int i = 0; i < count; ++i) {
+        b->lin[i].rs_off = static_cast<uint32_t>(off);
+        off = align_up(static_cast<uint32_t>(off + M * (a[i].K / kBlock) * 4), 128);
+        if (off > kSmemCap) return false;
+    }
+    for (int i = 0; i < count; ++i) {
+        b->lin[i].x_off = static_cast<uint32_t>(off);
+        if (quantize) off = align_up(static_cast<uint32_t>(off + M * a[i].K * 4), 128);
+        if (off > kSmemCap) return false;
+    }
+    const uint32_t bar_off = static_cast<uint32_t>(off);
+    const uint32_t stage_off = align_up(bar_off + (2 * kMaxStages + 1) * 8 + 16, 1024);
     GemvPlan best;
     int64_t best_cost = -1;
-    const int64_t nb = K / kBlock;
-    const int chunks = static_cast<int>((nb + kChunkBlocks - 1) / kChunkBlocks);
-    const int64_t act_stride = static_cast<int64_t>(chunks) * kChunkAct;
-    const int64_t act = M * act_stride, rs = M * nb * 4, xb = quantize ? M * K * 4 : 0;
-    if (act + rs + xb > kSmemCap) return false;
-    const uint32_t rs_off = align_up(static_cast<uint32_t>(act), 128);
-    const uint32_t x_off = align_up(rs_off + static_cast<uint32_t>(rs), 128);
-    const uint32_t bar_off = align_up(x_off + static_cast<uint32_t>(xb), 128);
-    const uint32_t stage_off = align_up(bar_off + (2 * kMaxStages + 1) * 8 + 16, 1024);
     for (int tr : {32, 16, 8, 4, 2, 1}) {
         if (tr > 8 && M > 2) continue;  // more rows per warp only for one or two tokens
-        const uint32_t wb = align_up(static_cast<uint32_t>(tr * K / 2), 16);
-        const uint32_t sz = align_up(static_cast<uint32_t>(tr * nb * 2 + 32), 16);
+        if (tr < min_tr) continue;
+        uint32_t wb = 0, sz = 0;
+        int64_t tiles = 0;
+        for (int i = 0; i < count; ++i) {
+            const int64_t K = a[i].K, nb = K / kBlock;
+            wb = std::max(wb, align_up(static_cast<uint32_t>(tr * K / 2), 16));
+            sz = std::max(sz, align_up(static_cast<uint32_t>(tr * nb * 2 + 32), 16));
+            tiles += (a[i].N + tr - 1) / tr;
+        }
         const uint32_t stage = align_up(wb + 2 * sz, 128);
         const int64_t room = kSmemCap - 1024 - static_cast<int64_t>(stage_off);
         int64_t ns = room / stage;
         if (ns > kMaxStages) ns = kMaxStages;
         if (ns < 2) continue;
-        const int64_t tiles = (N + tr - 1) / tr;
         const int64_t grid = tiles < num_sms ? tiles : num_sms;
         const int64_t waves = (tiles + grid - 1) / grid;
         // bytes streamed by the busiest CTA, plus a fixed cost per tile (barriers, sums)
@@ -99,10 +160,6 @@ bool make_plan(int64_t M, int64_t N, int64_t K, bool quantize, int num_sms, Gemv
             best.tr = tr;
             best.wpr = tr >= 8 ? 1 : 8 / tr;
             best.ns = static_cast<int>(ns);
-            best.chunks = chunks;
-            best.act_stride = static_cast<uint32_t>(act_stride);
-            best.rs_off = rs_off;
-            best.x_off = x_off;
             best.bar_off = bar_off;
             best.stage_off = stage_off;
             best.stage_bytes = stage;
@@ -114,8 +171,21 @@ bool make_plan(int64_t M, int64_t N, int64_t K, bool quantize, int num_sms, Gemv
         }
     }
     if (best_cost < 0) return false;
+    int64_t t0 = 0;
+    for (int i = 0; i < count; ++i) {
+        b->lin[i].tile0 = t0;
+        b->lin[i].tr = best.tr;
+        t0 += (a[i].N + best.tr - 1) / best.tr;
+    }
     *out = best;
     return true;
+}
+
+// The linear that global tile g belongs to.
+__device__ __forceinline__ int lin_of(const GemvBatch& B, int64_t g) {
+    int li = 0;
+    while (li + 1 < B.count && g >= B.lin[li + 1].tile0) ++li;
+    return li;
 }
 
 __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
@@ -240,9 +310,26 @@ __device__ __forceinline__ int block_dot(const uint4& W0, const uint4& W1, const
     return (la + lb) + ((ha + hb) >> 4);  // the high sums are 16 x (odd-code products), exact
 }
 
+// The producer's copies of one row tile (global tile g, of linear L) into stage s: the packed
+// rows, and the 16-byte-aligned interiors of the scale and zero spans.
+__device__ __forceinline__ void issue_tile(const GemvLin& L, const GemvPlan& P, uint8_t* smem, uint64_t* full,
+                                           int64_t g, int s) {
+    const int64_t K = L.K, nb = K / kBlock;
+    const int64_t n0 = (g - L.tile0) * L.tr;
+    const int64_t rows = L.N - n0 < L.tr ? L.N - n0 : L.tr;
+    const uint32_t wbytes = static_cast<uint32_t>(rows * (K / 2));
+    const HalfSpan hs = half_span(L.s_w, n0 * nb, (n0 + rows) * nb);
+    const HalfSpan hz = half_span(L.z_w, n0 * nb, (n0 + rows) * nb);
+    uint8_t* st = smem + P.stage_off + s * P.stage_bytes;
+    mbar_arrive_expect_tx(&full[s], wbytes + hs.bytes + hz.bytes);
+    bulk_load(st, L.wq + n0 * (K / 2), wbytes, &full[s]);
+    if (hs.bytes) bulk_load(st + P.w_bytes + hs.skew + hs.lo, hs.src, hs.bytes, &full[s]);
+    if (hz.bytes) bulk_load(st + P.w_bytes + P.sz_bytes + hz.skew + hz.lo, hz.src, hz.bytes, &full[s]);
+}
+
 template <int MT, int RW>
 __global__ void __launch_bounds__(kGThreads, 1)
-    gemv_kernel(const GemvArgs a, const GemvPlan P, uint32_t* status, uint64_t wait_limit_ns) {
+    gemv_kernel(const __grid_constant__ GemvBatch B, const GemvPlan P, uint32_t* status, uint64_t wait_limit_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + P.bar_off);
@@ -251,11 +338,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
     volatile uint32_t* abort_flag = reinterpret_cast<uint32_t*>(xbar + 1);
     __shared__ float red[2][kCW][MT];
     __shared__ float amax_red[2][kCW];
-    __shared__ float sa_sm[MT];
+    __shared__ float sa_sm[kGemvMaxLinears][MT];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t K = a.K, N = a.N, nb = K / kBlock;
-    const int ns = P.ns, tr = P.tr;
+    const int ns = P.ns;
     const uint32_t my_tiles =
         P.tiles > blockIdx.x ? static_cast<uint32_t>((P.tiles - 1 - blockIdx.x) / gridDim.x + 1) : 0u;
     const WaitCtl ctl{abort_flag, status, wait_limit_ns};
@@ -277,27 +363,20 @@ __global__ void __launch_bounds__(kGThreads, 1)
             // The weights are read-only inputs: when the previous kernel cannot have written them
             // (`early`), the first stages' copies go out before it has finished, so this kernel's
             // weight stream overlaps its tail.  Everything else waits for it.
-            auto issue_tile = [&](uint32_t i, int s) {
-                const int64_t n0 = (blockIdx.x + static_cast<int64_t>(i) * gridDim.x) * tr;
-                const int64_t rows = N - n0 < tr ? N - n0 : tr;
-                const uint32_t wbytes = static_cast<uint32_t>(rows * (K / 2));
-                const HalfSpan hs = half_span(a.s_w, n0 * nb, (n0 + rows) * nb);
-                const HalfSpan hz = half_span(a.z_w, n0 * nb, (n0 + rows) * nb);
-                uint8_t* st = smem + P.stage_off + s * P.stage_bytes;
-                mbar_arrive_expect_tx(&full[s], wbytes + hs.bytes + hz.bytes);
-                bulk_load(st, a.wq + n0 * (K / 2), wbytes, &full[s]);
-                if (hs.bytes) bulk_load(st + P.w_bytes + hs.skew + hs.lo, hs.src, hs.bytes, &full[s]);
-                if (hz.bytes) bulk_load(st + P.w_bytes + P.sz_bytes + hz.skew + hz.lo, hz.src, hz.bytes, &full[s]);
-            };
             uint32_t i = 0;
-            if (a.early)
-                for (; i < my_tiles && i < static_cast<uint32_t>(ns); ++i) issue_tile(i, static_cast<int>(i));
+            if (B.early)
+                for (; i < my_tiles && i < static_cast<uint32_t>(ns); ++i) {
+                    const int64_t g = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
+                    issue_tile(B.lin[lin_of(B, g)], P, smem, full, g, static_cast<int>(i));
+                }
             griddep_wait();
-            if (a.x) {
-                // the rows to quantize: every CTA reads them (the first copy unless weights went early)
-                const uint32_t xbytes = static_cast<uint32_t>(MT * K * 4);
+            if (B.quantize) {
+                // the rows to quantize, every linear's: every CTA reads them
+                uint32_t xbytes = 0;
+                for (int li = 0; li < B.count; ++li) xbytes += static_cast<uint32_t>(MT * B.lin[li].K * 4);
                 mbar_arrive_expect_tx(xbar, xbytes);
-                bulk_load(smem + P.x_off, a.x, xbytes, xbar);
+                for (int li = 0; li < B.count; ++li)
+                    bulk_load(smem + B.lin[li].x_off, B.lin[li].x, static_cast<uint32_t>(MT * B.lin[li].K * 4), xbar);
             }
             bool ok = true;
             for (; i < my_tiles; ++i) {
@@ -307,7 +386,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     ok = false;
                     break;
                 }
-                issue_tile(i, s);
+                const int64_t g = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
+                issue_tile(B.lin[lin_of(B, g)], P, smem, full, g, s);
             }
             if (!ok || *abort_flag) {
                 // let the copies already issued land before the CTA exits
@@ -322,90 +402,95 @@ __global__ void __launch_bounds__(kGThreads, 1)
     } else {
         // ------------------------------------------------------------ consumers
         griddep_wait();
-        // Stage the activations: token m, block b = 32 c + l -> four 16-byte planes at
-        // m * act_stride + 2048 c + 512 p + 16 l; the block row sums as floats; s_a.
-        float* rsf_sm = reinterpret_cast<float*>(smem + P.rs_off);
-        auto plane_addr = [&](int64_t m, int64_t b, int p) {
-            return smem + m * P.act_stride + (b >> 5) * kChunkAct + p * 512 + (b & 31) * 16;
-        };
-        if (a.x) {
-            // Quantize here, from the rows the producer copied in (nb <= 256).  The units are
-            // 16 codes (a block's plane): lane group 4b .. 4b+3 of a warp holds block b.
-            const bool got = __all_sync(0xffffffffu, mbar_wait(xbar, 0, ctl));
-            const uint32_t xs_base = smem_u32(smem + P.x_off);
-            for (int m = 0; m < MT; ++m) {
-                const uint32_t xr = xs_base + static_cast<uint32_t>(m * K * 4);
-                float amax = 0.0f;
-                for (int64_t f = threadIdx.x; got && f < K / 4; f += kCW * 32) {
-                    const uint4 v = lds128(xr + static_cast<uint32_t>(f * 16));
-                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(__uint_as_float(v.x)), fabsf(__uint_as_float(v.y))),
-                                             fmaxf(fabsf(__uint_as_float(v.z)), fabsf(__uint_as_float(v.w)))));
+        // Stage every linear's activations: token m, block b = 32 c + l -> four 16-byte planes at
+        // act_off + m * act_stride + 2048 c + 512 p + 16 l; the block row sums as floats; s_a.
+        const bool got = !B.quantize || __all_sync(0xffffffffu, mbar_wait(xbar, 0, ctl));
+        int par = 0;  // alternates the amax slots from row to row
+        for (int li = 0; li < B.count; ++li) {
+            const GemvLin& L = B.lin[li];
+            const int64_t K = L.K, nb = K / kBlock;
+            float* rsf_sm = reinterpret_cast<float*>(smem + L.rs_off);
+            auto plane_addr = [&](int64_t m, int64_t b, int p) {
+                return smem + L.act_off + m * L.act_stride + (b >> 5) * kChunkAct + p * 512 + (b & 31) * 16;
+            };
+            if (B.quantize) {
+                // Quantize here, from the rows the producer copied in (nb <= 256).  The units are
+                // 16 codes (a block's plane): lane group 4b .. 4b+3 of a warp holds block b.
+                const uint32_t xs_base = smem_u32(smem + L.x_off);
+                for (int m = 0; m < MT; ++m, par ^= 1) {
+                    const uint32_t xr = xs_base + static_cast<uint32_t>(m * K * 4);
+                    float amax = 0.0f;
+                    for (int64_t f = threadIdx.x; got && f < K / 4; f += kCW * 32) {
+                        const uint4 v = lds128(xr + static_cast<uint32_t>(f * 16));
+                        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(__uint_as_float(v.x)), fabsf(__uint_as_float(v.y))),
+                                                 fmaxf(fabsf(__uint_as_float(v.z)), fabsf(__uint_as_float(v.w)))));
+                    }
+#pragma unroll
+                    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                    if (lane == 0) amax_red[par][warp] = amax;
+                    named_bar_sync(kBarStage, kCW * 32);
+                    amax = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < kCW; ++w) amax = fmaxf(amax, amax_red[par][w]);
+                    const float s = __fdiv_rn(amax, 127.0f);
+                    const float r = __frcp_rn(s);
+                    if (threadIdx.x == 0) sa_sm[li][m] = s;
+                    const int units = static_cast<int>(4 * nb);
+                    for (int u0 = warp * 32; u0 < units; u0 += kCW * 32) {  // warp-uniform trip count
+                        const int u = u0 + lane, b = u >> 2, p = u & 3;
+                        const bool on = got && u < units;
+                        // slot j holds float4 (j + rot) % 4 of the unit: consecutive lanes sit 64 bytes
+                        // apart, and the rotation spreads each 8-lane phase of the loads over all banks
+                        const int rot = (lane >> 1) & 3;
+                        float4 xs[4], q[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int jj = (j + rot) & 3;
+                            const uint4 v = on ? lds128(xr + static_cast<uint32_t>((64 * b + 16 * p + 4 * jj) * 4))
+                                               : make_uint4(0, 0, 0, 0);
+                            xs[j] = make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                                                __uint_as_float(v.w));
+                        }
+                        if (s > 0.0f) {  // s = 0: every code 0
+                            quant_lane<4>(xs, q, s, r);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) q[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                        uint32_t nr[4];
+                        float part = 0.0f;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            part += (q[j].x + q[j].y) + (q[j].z + q[j].w);  // exact
+                            nr[j] = pack4(code_bits(q[j].x), code_bits(q[j].y), code_bits(q[j].z), code_bits(q[j].w));
+                        }
+                        // back to k order: n[k] = nr[(k - rot) % 4], a rotation by rot in two select steps
+                        uint32_t h[4], n[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) h[k] = (rot & 1) ? nr[(k + 3) & 3] : nr[k];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) n[k] = (rot & 2) ? h[(k + 2) & 3] : h[k];
+                        if (on) *reinterpret_cast<uint4*>(plane_addr(m, b, p)) = plane_of(n[0], n[1], n[2], n[3]);
+                        part += __shfl_xor_sync(0xffffffffu, part, 1);
+                        part += __shfl_xor_sync(0xffffffffu, part, 2);
+                        if (on && p == 0) rsf_sm[m * nb + b] = part;
+                    }
                 }
+            } else {
+                for (int64_t u = threadIdx.x; u < MT * nb; u += kCW * 32) {
+                    const int64_t m = u / nb, b = u - m * nb;
+                    const int4* src = reinterpret_cast<const int4*>(L.a_q + m * K + 64 * b);
 #pragma unroll
-                for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-                if (lane == 0) amax_red[m & 1][warp] = amax;
-                named_bar_sync(kBarStage, kCW * 32);
-                amax = 0.0f;
-#pragma unroll
-                for (int w = 0; w < kCW; ++w) amax = fmaxf(amax, amax_red[m & 1][w]);
-                const float s = __fdiv_rn(amax, 127.0f);
-                const float r = __frcp_rn(s);
-                if (threadIdx.x == 0) sa_sm[m] = s;
-                const int units = static_cast<int>(4 * nb);
-                for (int u0 = warp * 32; u0 < units; u0 += kCW * 32) {  // warp-uniform trip count
-                    const int u = u0 + lane, b = u >> 2, p = u & 3;
-                    const bool on = got && u < units;
-                    // slot j holds float4 (j + rot) % 4 of the unit: consecutive lanes sit 64 bytes
-                    // apart, and the rotation spreads each 8-lane phase of the loads over all banks
-                    const int rot = (lane >> 1) & 3;
-                    float4 xs[4], q[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int jj = (j + rot) & 3;
-                        const uint4 v = on ? lds128(xr + static_cast<uint32_t>((64 * b + 16 * p + 4 * jj) * 4))
-                                           : make_uint4(0, 0, 0, 0);
-                        xs[j] = make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
-                                            __uint_as_float(v.w));
+                    for (int p = 0; p < 4; ++p) {
+                        const int4 v = __ldg(src + p);
+                        *reinterpret_cast<uint4*>(plane_addr(m, b, p)) =
+                            plane_of(static_cast<uint32_t>(v.x), static_cast<uint32_t>(v.y), static_cast<uint32_t>(v.z),
+                                     static_cast<uint32_t>(v.w));
                     }
-                    if (s > 0.0f) {  // s = 0: every code 0
-                        quant_lane<4>(xs, q, s, r);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) q[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                    uint32_t nr[4];
-                    float part = 0.0f;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        part += (q[j].x + q[j].y) + (q[j].z + q[j].w);  // exact
-                        nr[j] = pack4(code_bits(q[j].x), code_bits(q[j].y), code_bits(q[j].z), code_bits(q[j].w));
-                    }
-                    // back to k order: n[k] = nr[(k - rot) % 4], a rotation by rot in two select steps
-                    uint32_t h[4], n[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) h[k] = (rot & 1) ? nr[(k + 3) & 3] : nr[k];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) n[k] = (rot & 2) ? h[(k + 2) & 3] : h[k];
-                    if (on) *reinterpret_cast<uint4*>(plane_addr(m, b, p)) = plane_of(n[0], n[1], n[2], n[3]);
-                    part += __shfl_xor_sync(0xffffffffu, part, 1);
-                    part += __shfl_xor_sync(0xffffffffu, part, 2);
-                    if (on && p == 0) rsf_sm[m * nb + b] = part;
+                    rsf_sm[u] = static_cast<float>(__ldg(L.rs + u));
                 }
+                if (threadIdx.x < MT) sa_sm[li][threadIdx.x] = __ldg(L.s_a + threadIdx.x);
             }
-        } else {
-            for (int64_t u = threadIdx.x; u < MT * nb; u += kCW * 32) {
-                const int64_t m = u / nb, b = u - m * nb;
-                const int4* src = reinterpret_cast<const int4*>(a.a_q + m * K + 64 * b);
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    const int4 v = __ldg(src + p);
-                    *reinterpret_cast<uint4*>(plane_addr(m, b, p)) =
-                        plane_of(static_cast<uint32_t>(v.x), static_cast<uint32_t>(v.y), static_cast<uint32_t>(v.z),
-                                 static_cast<uint32_t>(v.w));
-                }
-                rsf_sm[u] = static_cast<float>(__ldg(a.rs + u));
-            }
-            if (threadIdx.x < MT) sa_sm[threadIdx.x] = __ldg(a.s_a + threadIdx.x);
         }
         named_bar_sync(kBarStage, kCW * 32);
         // the next kernel in the stream may start its prologue as this CTA's SM frees up; it
@@ -414,11 +499,18 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
         const int wpr = P.wpr;
         const int rslot = warp / wpr, sidx = warp - rslot * wpr;
-        const uint32_t act_base = smem_u32(smem), rs_base = smem_u32(rsf_sm);
-        const uint32_t krow = static_cast<uint32_t>(K / 2), nbu = static_cast<uint32_t>(nb);
         for (uint32_t i = 0; i < my_tiles; ++i) {
             const int s = static_cast<int>(i % ns);
-            const int64_t n0 = (blockIdx.x + static_cast<int64_t>(i) * gridDim.x) * tr;
+            const int64_t g = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
+            const int li = lin_of(B, g);
+            const GemvLin& L = B.lin[li];
+            const int64_t N = L.N, nb = L.K / kBlock;
+            const int tr = L.tr;
+            const int64_t n0 = (g - L.tile0) * tr;
+            const uint32_t act_base = smem_u32(smem + L.act_off), rs_base = smem_u32(smem + L.rs_off);
+            const uint32_t krow = static_cast<uint32_t>(L.K / 2), nbu = static_cast<uint32_t>(nb);
+            const int chunks = L.chunks;
+            const uint32_t act_stride = L.act_stride;
             const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (i / ns) & 1, ctl));
             const uint32_t st = smem_u32(smem + P.stage_off + s * P.stage_bytes);
             const int64_t rows = N - n0 < tr ? N - n0 : tr;
@@ -427,10 +519,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
             // arrays that do not start on one) has its ragged ends filled in from global memory
             const int64_t e0 = n0 * nb, e1 = (n0 + rows) * nb;
             const uint32_t s_slot = st + P.w_bytes, z_slot = st + P.w_bytes + P.sz_bytes;
-            const uint32_t swb = s_slot + static_cast<uint32_t>(reinterpret_cast<uintptr_t>(a.s_w + e0) & 15);
-            const uint32_t zwb = z_slot + static_cast<uint32_t>(reinterpret_cast<uintptr_t>(a.z_w + e0) & 15);
-            if (!(span_whole(a.s_w, e0, e1) && span_whole(a.z_w, e0, e1))) {  // the same for every consumer
-                fill_ragged(s_slot, z_slot, a.s_w, a.z_w, e0, e1, static_cast<int>(threadIdx.x));
+            const uint32_t swb = s_slot + static_cast<uint32_t>(reinterpret_cast<uintptr_t>(L.s_w + e0) & 15);
+            const uint32_t zwb = z_slot + static_cast<uint32_t>(reinterpret_cast<uintptr_t>(L.z_w + e0) & 15);
+            if (!(span_whole(L.s_w, e0, e1) && span_whole(L.z_w, e0, e1))) {  // the same for every consumer
+                fill_ragged(s_slot, z_slot, L.s_w, L.z_w, e0, e1, static_cast<int>(threadIdx.x));
                 // the slot is reloaded by a bulk copy (async proxy) after the stage is released
                 fence_proxy_async_smem();
                 named_bar_sync(kBarStage, kCW * 32);
@@ -449,7 +541,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll
                 for (int m = 0; m < MT; ++m) sum[j][m] = 0.0f;
             if (ok) {
-                for (int c = sidx; c < P.chunks; c += wpr) {
+                for (int c = sidx; c < chunks; c += wpr) {
                     const uint32_t b = static_cast<uint32_t>(c * kChunkBlocks + lane);
                     const bool live = b < nbu;
                     uint4 W0[RW], W1[RW];
@@ -467,7 +559,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
                         uint4 Pl[4];
-                        const uint32_t ad = act_base + m * P.act_stride + c * kChunkAct + 16 * lane;
+                        const uint32_t ad = act_base + m * act_stride + c * kChunkAct + 16 * lane;
 #pragma unroll
                         for (int p = 0; p < 4; ++p) Pl[p] = lds128(ad + p * 512);
                         const float rsf = live ? lds_f32(rs_base + (m * nbu + b) * 4) : 0.0f;
@@ -501,7 +593,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     for (int m = 1; m < MT; ++m)
                         if (lane == m) v = sum[j][m];
                     if (rok[j] && lane < MT)
-                        store_y(a.out, static_cast<int64_t>(lane) * N + n, fmaf(sa_sm[lane], v, a.bias ? a.bias[n] : 0.0f));
+                        store_y(L.out, static_cast<int64_t>(lane) * N + n,
+                                fmaf(sa_sm[li][lane], v, L.bias ? L.bias[n] : 0.0f));
                 }
             } else {
                 // the row's warps meet (every warp meets once per tile, whatever its waits gave)
@@ -513,7 +606,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 if (sidx == 0 && rok[0] && lane < MT) {
                     float v = 0.0f;
                     for (int q = 0; q < wpr; ++q) v += red[i & 1][rslot * wpr + q][lane];
-                    store_y(a.out, static_cast<int64_t>(lane) * N + n, fmaf(sa_sm[lane], v, a.bias ? a.bias[n] : 0.0f));
+                    store_y(L.out, static_cast<int64_t>(lane) * N + n,
+                            fmaf(sa_sm[li][lane], v, L.bias ? L.bias[n] : 0.0f));
                 }
             }
         }
@@ -522,7 +616,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 }
 
 template <int MT, int RW>
-cudaError_t launch_one(const GemvArgs& a, const GemvPlan& P, uint32_t* status, cudaStream_t s) {
+cudaError_t launch_one(const GemvBatch& b, const GemvPlan& P, uint32_t* status, cudaStream_t s) {
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -542,45 +636,104 @@ cudaError_t launch_one(const GemvArgs& a, const GemvPlan& P, uint32_t* status, c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, RW>, a, P, status, uint64_t(1000000000ull));
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, RW>, b, P, status, uint64_t(1000000000ull));
 }
 
 template <int MT>
-cudaError_t launch_mt(const GemvArgs& a, const GemvPlan& P, uint32_t* status, cudaStream_t s) {
+cudaError_t launch_mt(const GemvBatch& b, const GemvPlan& P, uint32_t* status, cudaStream_t s) {
     if constexpr (MT <= 2) {
-        if (P.tr == 32) return launch_one<MT, 4>(a, P, status, s);
-        if (P.tr == 16) return launch_one<MT, 2>(a, P, status, s);
+        if (P.tr == 32) return launch_one<MT, 4>(b, P, status, s);
+        if (P.tr == 16) return launch_one<MT, 2>(b, P, status, s);
     }
-    return launch_one<MT, 1>(a, P, status, s);
+    return launch_one<MT, 1>(b, P, status, s);
+}
+
+GemvArgs shape_only(int64_t M, int64_t K) {
+    GemvArgs a;
+    a.M = M;
+    a.N = 1;
+    a.K = K;
+    return a;
+}
+
+// The checks of a batch launch, and its plan: one M (1 .. kGemvMaxM), every linear quantized in
+// the kernel or none, every row short enough for the kernel, the staging areas within one CTA.
+bool plan_batch(const GemvArgs* a, int count, int num_sms, GemvBatch* b, GemvPlan* P) {
+    if (count < 1 || count > kGemvMaxLinears) return false;
+    const int64_t M = a[0].M;
+    const bool quantize = a[0].x != nullptr;
+    if (M < 1 || M > kGemvMaxM) return false;
+    for (int i = 0; i < count; ++i) {
+        if (a[i].M != M || a[i].N < 1 || (a[i].x != nullptr) != quantize || !gemv_supported(M, a[i].K)) return false;
+        if (quantize && !gemv_quantizes(M, a[i].K)) return false;
+    }
+    *b = GemvBatch{};
+    return make_plan(a, count, quantize, num_sms, b, P, count > 1 ? 8 : 1);
 }
 
 }  // namespace
 
 bool gemv_supported(int64_t M, int64_t K) {
+    const GemvArgs a = shape_only(M, K);
+    GemvBatch b{};
     GemvPlan P;
-    return M >= 1 && M <= kGemvMaxM && K >= kBlock && make_plan(M, 1, K, false, 1, &P);
+    return M >= 1 && M <= kGemvMaxM && K >= kBlock && make_plan(&a, 1, false, 1, &b, &P);
 }
 
 bool gemv_quantizes(int64_t M, int64_t K) {
+    const GemvArgs a = shape_only(M, K);
+    GemvBatch b{};
     GemvPlan P;
-    return M * K <= kGemvFuseElems && gemv_supported(M, K) && make_plan(M, 1, K, true, 1, &P);
+    return M * K <= kGemvFuseElems && gemv_supported(M, K) && make_plan(&a, 1, true, 1, &b, &P);
+}
+
+bool gemv_batch_fits(const GemvArgs* a, int count) {
+    GemvBatch b{};
+    GemvPlan P;
+    return plan_batch(a, count, 1, &b, &P);
+}
+
+int gemv_tile_rows(const GemvArgs& a, int num_sms) {
+    GemvBatch b{};
+    GemvPlan P;
+    return plan_batch(&a, 1, num_sms, &b, &P) ? P.tr : 0;
+}
+
+cudaError_t launch_gemv_batch(const GemvArgs* a, int count, int num_sms, uint32_t* status, cudaStream_t s) {
+    GemvBatch b{};
+    GemvPlan P;
+    if (!plan_batch(a, count, num_sms, &b, &P)) return cudaErrorInvalidValue;
+    for (int i = 0; i < count; ++i) {
+        GemvLin& L = b.lin[i];
+        L.x = a[i].x;
+        L.a_q = a[i].a_q;
+        L.s_a = a[i].s_a;
+        L.rs = a[i].rs;
+        L.wq = a[i].wq;
+        L.s_w = a[i].s_w;
+        L.z_w = a[i].z_w;
+        L.bias = a[i].bias;
+        L.out = a[i].out;
+        L.N = a[i].N;
+        L.K = a[i].K;
+    }
+    b.count = count;
+    b.quantize = a[0].x != nullptr;
+    b.early = a[0].early;
+    switch (a[0].M) {
+        case 1: return launch_mt<1>(b, P, status, s);
+        case 2: return launch_mt<2>(b, P, status, s);
+        case 3: return launch_mt<3>(b, P, status, s);
+        case 4: return launch_mt<4>(b, P, status, s);
+        case 5: return launch_mt<5>(b, P, status, s);
+        case 6: return launch_mt<6>(b, P, status, s);
+        case 7: return launch_mt<7>(b, P, status, s);
+        default: return launch_mt<8>(b, P, status, s);
+    }
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, int num_sms, uint32_t* status, cudaStream_t s) {
-    GemvPlan P;
-    if (a.M < 1 || a.M > kGemvMaxM || a.N < 1 || (a.x && !gemv_quantizes(a.M, a.K)) ||
-        !make_plan(a.M, a.N, a.K, a.x != nullptr, num_sms, &P))
-        return cudaErrorInvalidValue;
-    switch (a.M) {
-        case 1: return launch_mt<1>(a, P, status, s);
-        case 2: return launch_mt<2>(a, P, status, s);
-        case 3: return launch_mt<3>(a, P, status, s);
-        case 4: return launch_mt<4>(a, P, status, s);
-        case 5: return launch_mt<5>(a, P, status, s);
-        case 6: return launch_mt<6>(a, P, status, s);
-        case 7: return launch_mt<7>(a, P, status, s);
-        default: return launch_mt<8>(a, P, status, s);
-    }
+    return launch_gemv_batch(&a, 1, num_sms, status, s);
 }
 
 }  // namespace w4a8

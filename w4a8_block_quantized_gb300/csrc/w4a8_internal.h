@@ -195,6 +195,14 @@ bool gemv_supported(int64_t M, int64_t K);
 bool gemv_quantizes(int64_t M, int64_t K);
 
 cudaError_t launch_gemv(const GemvArgs& a, int num_sms, uint32_t* status, cudaStream_t s);
+
+// Up to kGemvMaxLinears independent linears of one M in one launch of the weight-streaming
+// kernel: every CTA stages (or quantizes) all of their activations, then the CTAs walk the row
+// tiles of all of them as one stream.  `early` is taken from the first entry.
+constexpr int kGemvMaxLinears = 8;
+bool gemv_batch_fits(const GemvArgs* a, int count);
+int gemv_tile_rows(const GemvArgs& a, int num_sms);  // the tile height a launch of `a` alone uses (0: none)
+cudaError_t launch_gemv_batch(const GemvArgs* a, int count, int num_sms, uint32_t* status, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace w4a8
