@@ -213,6 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tile_at(first + static_cast<int64_t>(i) * gridDim.x, tiles_t, tiles_w, tt, tw);
                     const uint8_t* tsrc = args.trec + static_cast<int64_t>(tt) * nb * kTokRec;
                     const uint8_t* wsrc = args.wrec + static_cast<int64_t>(tw) * nb * kWRec;
+                    // the tile's weight scales into L2 ahead of the epilogue's loads
+                    if (!DEBUG) bulk_prefetch_l2(args.sc + static_cast<int64_t>(tw) * nb * kTileW, nb * kTileW * 4u);
                     for (uint32_t p = 0; p < spt; ++p, ++j) {
                         const int s = static_cast<int>(j % kStages);
                         const uint32_t k = j / kStages;
@@ -482,6 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
                     tile_at(first + static_cast<int64_t>(i) * gridDim.x, tiles_t, tiles_w, tt, tw);
                     const uint8_t* tsrc = args.trec + static_cast<int64_t>(tt) * nb * W::kTok;
                     const uint8_t* wsrc = args.wrec + static_cast<int64_t>(tw) * nb * kWRec;
+                    // the tile's weight scales (nb x 128 floats, contiguous) into L2 now, a few
+                    // blocks before the epilogue reads the first of them: a scale load that misses
+                    // L2 holds up the drain of its block's accumulator, and with it the MMAs that
+                    // wait for that TMEM buffer
+                    if (!DEBUG) bulk_prefetch_l2(args.sc + static_cast<int64_t>(tw) * nb * kTileW, nb * kTileW * 4u);
                     for (uint32_t b = 0; b < nb; ++b, ++g) {
                         const int s = static_cast<int>(g % W::kStages);
                         const uint32_t k = g / W::kStages;
