@@ -42,12 +42,15 @@
 //                a stage's two blocks per drain keep four TMEM loads in flight per wait
 //
 // The barrier of a stage gates its MMAs: it completes once the stage's copies have landed
-// (producer arrival + transaction bytes) and the epilogue has released the two TMEM
+// (producer arrival + transaction bytes) and every epilogue warp has released the two TMEM
 // buffers the stage overwrites (one arrival per epilogue warp), so an issuer waits once per
 // block.  The epilogue drains a stage's two blocks together (four TMEM loads in flight per
-// wait), releases their buffers as soon as the accumulators are in registers, then folds
-// them into y; it frees a stage once its accumulators are complete.  Every wait is bounded (WaitCtl); a CTA
-// that gives up records a timeout and unwinds.
+// wait), releases their buffers as soon as the accumulators are in its registers, then folds
+// them into y; it frees a stage once its accumulators are complete.  The epilogue warps wait
+// and release each on their own: a rendezvous of all sixteen per stage (a vote on the wait,
+// a named barrier before one release) cost the skew between the warps at every stage
+// (measured on the 7B-class contraction: 4-7% of its time).  Every wait is bounded (WaitCtl); a
+// thread that gives up raises the CTA's abort flag, so every role stops waiting and unwinds.
 #include <cuda_fp16.h>
 
 #include "epilogue.cuh"
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 2);  // the producer and one epilogue thread
+            mbar_init(&full[s], 1 + kEpiWarps);  // the producer and every epilogue warp
             mbar_init(&empty[s], 1);
         }
         for (int i = 0; i < 2; ++i) mbar_init(&tfull[i], 2);  // one commit per block slot
@@ -293,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = q * 32 + lane;                // this thread's weight row in the tile
         const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 32);
         // the TMEM buffers start free: release the first two stages
-        if (warp == 4 && lane == 0)
+        if (lane == 0)
             for (uint32_t q0 = 0; q0 < 2 && q0 < total; ++q0) mbar_arrive(&full[q0]);
         uint32_t j = 0;  // stage counter of this CTA
         bool ok = true;
@@ -327,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ns1 = 2 * p + 3 < nb ? __ldg(sct + (2 * p + 3) * kTileW) : 0.0f;
                 }
                 const uint32_t pair = j & 1u, b0 = 2 * pair, b1 = b0 + 1;
-                if (!epi_all(mbar_wait(&tfull[pair], (j >> 1) & 1, ctl))) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&tfull[pair], (j >> 1) & 1, ctl))) {
                     ok = false;
                     break;
                 }
@@ -342,12 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_32x32b_x16(tl + b1 * kTileT + 16, v + 48);
                 }
                 tmem_wait_ld();
-                // the accumulators are in registers: the buffers are free for the stage two later
-                // (the epilogue warps meet on a named barrier, then one thread arrives: sixteen
-                // arrivals on one mbarrier word would serialise)
+                // this warp's accumulators are in registers: its part of the buffers is free for the
+                // stage two later (the stage barrier completes once every epilogue warp has arrived)
                 tc_fence_before();
-                epi_bar_sync();
-                if (warp == 4 && lane == 0 && j + 2 < total) mbar_arrive(&full[(j + 2) % kStages]);
+                __syncwarp();
+                if (lane == 0 && j + 2 < total) mbar_arrive(&full[(j + 2) % kStages]);
                 if (DEBUG) {
                     if (n < args.N) {
 #pragma unroll
@@ -449,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < W::kStages; ++s) {
-            mbar_init(&full[s], 2);  // the producer and one epilogue thread
+            mbar_init(&full[s], 1 + kEpiWarps);  // the producer and every epilogue warp
             mbar_init(&empty[s], 1);
         }
         for (int i = 0; i < W::kNBuf; ++i) mbar_init(&tfull[i], 1);
@@ -546,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
         const int q = warp & 3, h = (warp - 4) >> 2;  // TMEM lane quarter, 64-column quarter
         const int row = q * 32 + lane;
         const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 64);
-        if (warp == 4 && lane == 0)
+        if (lane == 0)
             for (uint32_t q0 = 0; q0 < W::kNBuf && q0 < total; ++q0) mbar_arrive(&full[q0]);
         uint32_t g = 0;
         bool ok = true;
@@ -574,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
                 const float sb = ns;
                 if (!DEBUG && b + 1 < nb) ns = __ldg(sct + (b + 1) * kTileW);
                 const uint32_t buf = g & 1u;
-                if (!epi_all(mbar_wait(&tfull[buf], (g >> 1) & 1, ctl))) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], (g >> 1) & 1, ctl))) {
                     ok = false;
                     break;
                 }
@@ -594,10 +596,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
                 tmem_ld_32x32b_x16(tb + 32, v);
                 tmem_ld_32x32b_x16(tb + 48, v + 16);
                 tmem_wait_ld();
-                // the accumulator is in registers: the buffer is free for block g + 2
+                // this warp's accumulators are in registers: its part of the buffer is free for
+                // block g + 2 (the stage barrier completes once every epilogue warp has arrived)
                 tc_fence_before();
-                epi_bar_sync();
-                if (warp == 4 && lane == 0 && g + W::kNBuf < total) mbar_arrive(&full[(g + W::kNBuf) % W::kStages]);
+                __syncwarp();
+                if (lane == 0 && g + W::kNBuf < total) mbar_arrive(&full[(g + W::kNBuf) % W::kStages]);
                 if (DEBUG) {
                     store_acc(v, 32, b);
                 } else {
