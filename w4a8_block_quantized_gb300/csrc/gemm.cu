@@ -121,25 +121,6 @@ __device__ __forceinline__ void tile_at32(int64_t t, int64_t tiles_t, int64_t ti
     tw = q;
 }
 
-// Named barrier 1 over the 16 epilogue warps (barrier 0 is __syncthreads).  Every epilogue
-// warp reaches each of these at the same point of the same loop: a wait that fails is voted
-// on with epi_all() first, so either all epilogue warps go on or all unwind together.
-__device__ __forceinline__ void epi_bar_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
-}
-__device__ __forceinline__ bool epi_all(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.and.pred p, 1, %2, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(v)), "n"(kEpiWarps * 32)
-        : "memory");
-    return r != 0;
-}
-
 // Bounded wait that ignores the abort flag: used while unwinding to let copies and MMAs
 // already in flight land before the CTA's shared memory and TMEM are released.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -638,11 +619,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
 // the same bytes the weight job writes into a weight record, so the MMAs, and every output,
 // are those of gemm_kernel bit for bit.  The epilogue reads 512 s_w from s_w itself.  No
 // weight record is written to or read from device memory.
-// Measured on the pp512 linear (512 x 1024 -> 3072), a stage of two 64-blocks takes about
-// 1.7 us here against 0.63 us in gemm_kernel: while the expanding warps load and store shared
-// memory, the tensor cores' stages stretch (a variant without any expansion work runs at
-// 0.8 us).  So the one-call entry points keep the weight records; this kernel is the form that
-// needs neither a workspace nor expanded weights in memory.
+// Measured alone after an L2 flush, it takes 20.5 us on the pp512 linear (512 x 1024 -> 3072)
+// against 14.3 us for gemm_kernel, and 59 / 88 us against 33 / 41 us on the M = 512 linears
+// 2048 -> 6144 and 6144 -> 2048: while the expanding warps load and store shared memory, the
+// tensor cores' stages stretch.  So the one-call entry points keep the weight records; this
+// kernel is the form that needs neither a workspace nor expanded weights in memory.  Every
+// epilogue warp arrives on the stage barrier itself, for its part of the expanded operand and
+// for its part of the released TMEM buffers (a named barrier of all sixteen before one arrival
+// cost 10-24% of this kernel's time).
 //
 // The packed weights have a ring of kPkSlots slots of their own, so their loads run ahead of the
 // operand stages -- and, with `early` set (they do not depend on the previous kernel), start
@@ -748,7 +732,7 @@ __device__ __forceinline__ bool expand_stage(const GemmArgs& args, uint8_t* smem
     const bool live = b < nb;
     // the zero point first: its latency overlaps the wait
     const uint32_t zz = (!DEBUG && live && (xc & 1) == 0 && n < args.N) ? neg_zero_pair(__ldg(args.z_w + n * nb + b)) : 0u;
-    if (!epi_all(mbar_wait(&wfull[jj % P::kPkSlots], (jj / P::kPkSlots) & 1, ctl))) return false;
+    if (!__all_sync(0xffffffffu, mbar_wait(&wfull[jj % P::kPkSlots], (jj / P::kPkSlots) & 1, ctl))) return false;
     if (live) {
         const uint4 w =
             *reinterpret_cast<const uint4*>(smem + P::kOffPk + (jj % P::kPkSlots) * P::kPk + xr * 64 + ((xc ^ xsw) << 4));
@@ -763,10 +747,11 @@ __device__ __forceinline__ bool expand_stage(const GemmArgs& args, uint8_t* smem
         *reinterpret_cast<uint4*>(rec + xr * 64 + (((e0 + 1) ^ xsw) << 4)) = hi;
         if (!DEBUG && (xc & 1) == 0) *reinterpret_cast<uint4*>(rec + kWZx + xr * 16) = make_uint4(zz, 0u, 0u, 0u);
     }
-    // the operand is written (generic proxy) before the tensor cores (async proxy) read it
+    // the operand is written (generic proxy) before the tensor cores (async proxy) read it; the
+    // stage barrier completes once every epilogue warp has arrived
     fence_proxy_async_smem();
-    epi_bar_sync();
-    if (et == 0) mbar_arrive(&full[jj % P::kStages]);
+    __syncwarp();
+    if ((et & 31) == 0) mbar_arrive(&full[jj % P::kStages]);
     return true;
 }
 
@@ -798,7 +783,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P::kStages; ++s) {
-            mbar_init(&full[s], 3);  // producer, two epilogue arrivals (operand expanded, TMEM released)
+            // the producer, and two arrivals per epilogue warp (its part of the operand expanded,
+            // its part of the TMEM buffers released)
+            mbar_init(&full[s], 1 + 2 * kEpiWarps);
             mbar_init(&empty[s], 1);
         }
         for (int s = 0; s < P::kPkSlots; ++s) mbar_init(&wfull[s], 1);  // producer
@@ -920,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
             ok = expand_stage<DEBUG>(args, smem, wfull, full, jj, spt, nb, first, tiles_t, tiles_w, et, ctl);
         if (args.early) griddep_wait();
         // the TMEM buffers start free: release the first two stages
-        if (lead)
+        if (lane == 0)
             for (uint32_t q0 = 0; q0 < 2 && q0 < total; ++q0) mbar_arrive(&full[q0]);
         uint32_t j = 0;  // stage counter of this CTA
         for (uint32_t i = 0; ok && i < my_tiles; ++i) {
@@ -957,7 +944,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
                     ns1 = weight_scale(swr, 2 * p + 3, nb);
                 }
                 const uint32_t pair = j & 1u, b0 = 2 * pair;
-                if (!epi_all(mbar_wait(&tfull[pair], (j >> 1) & 1, ctl))) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&tfull[pair], (j >> 1) & 1, ctl))) {
                     ok = false;
                     break;
                 }
@@ -975,10 +962,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
                     tmem_ld_32x32b_x16(tb + 16, v + 16);
                     tmem_wait_ld();
                     if (e == 1 || !two) {
-                        // the accumulators are in registers: the buffers serve the stage two later
+                        // this warp's accumulators are in registers: its part of the buffers serves
+                        // the stage two later
                         tc_fence_before();
-                        epi_bar_sync();
-                        if (lead && j + 2 < total) mbar_arrive(&full[(j + 2) % P::kStages]);
+                        __syncwarp();
+                        if (lane == 0 && j + 2 < total) mbar_arrive(&full[(j + 2) % P::kStages]);
                     }
                     if (DEBUG) {
                         if (n < args.N) {
