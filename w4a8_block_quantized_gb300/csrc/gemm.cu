@@ -377,13 +377,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- 256-token tiles
-// The large-M variant.  One MMA covers 128 weights x 256 tokens (N = 256), so the SM issues
-// half as many tcgen05.mma instructions per unit of work as with 128-token tiles (the MMA
-// issue rate of an SM, one instruction per ~50-90 cycles, is what bounds the 128-token
-// kernel).  Two TMEM buffers of 256 columns; one block per shared-memory stage, filled by two
-// bulk copies (a 256-token record and a weight record).  Roles, barriers and bounded waits
-// follow gemm_kernel; an epilogue thread owns one weight row and 64 token columns, drained
-// 32 at a time.
+// The large-M variant.  One MMA covers 128 weights x 256 tokens (N = 256), so per unit of work
+// the SM issues half as many tcgen05.mma instructions, reads the weight operand from shared
+// memory half as often and waits on half as many accumulator hand-offs as with 128-token tiles
+// (measured at M = 8192: the 128-token kernel takes 25% longer).  Two TMEM buffers of 256
+// columns; one block per shared-memory stage, filled by two bulk copies (a 256-token record and
+// a weight record).  Roles, barriers and bounded waits follow gemm_kernel; an epilogue thread
+// owns one weight row and 64 token columns, drained 32 at a time.
 namespace wide {
 constexpr int kTN = 256;
 constexpr int kStages = 4;
