@@ -729,15 +729,16 @@ def _pinned(a):
 
 @pytest.mark.parametrize("M,K,N", [(1500, 1024, 2560), (2048, 2048, 4096), (8300, 512, 256), (9000, 512, 1536),
                                    (16384, 1024, 1024), (512, 1024, 640), (700, 256, 200), (255, 512, 96),
-                                   (4096, 128, 64), (3, 1024, 256)])
+                                   (4096, 128, 64), (3, 1024, 256), (255, 2048, 96), (512, 16384, 1024)])
 def test_host_call_equals_fused(M, K, N):
     """x and y in page-locked host memory, chunked copies overlapping the computation: the
     outputs equal the device-buffer fused call's bit for bit -- two chunks with a ragged
     last one; six chunks over four compute streams (streams and activation buffers reused);
     chunks of whole 256-row tiles below 4096 rows each through the 256-token kernel; eight
     chunks; the full sixteen; in place on the mapped buffers (128-token tiles, a ragged last
-    tile, fewer than two tiles, 256-token tiles); the few-token form -- and lie within
-    tolerance of the oracle."""
+    tile, fewer than two tiles, 256-token tiles); the few-token form; in place with K split
+    over CTA pairs; four chunks of a linear whose K is split over CTA pairs (each chunk told
+    the uncut call's split) -- and lie within tolerance of the oracle."""
     b = B()
     d = synth.random_small(M, K, N, seed=70 + M + N, bias=True)
     g = inputs_to_dev(d)

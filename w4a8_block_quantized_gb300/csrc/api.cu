@@ -89,10 +89,11 @@ CallLayout call_layout(int64_t M, int64_t N, int64_t K, bool with_sa) {
 }
 
 // GEMM + epilogue from prepared activations (token records `tw` tokens wide) and prepared
-// weights.  Each output depends only on its own row and the kernel the width selects, so
-// rows cut into whole tiles of one width give the uncut call's outputs.
+// weights.  Each output depends only on its own row, the kernel the width selects and the K
+// split (`ksplit`, by default the one of this shape: gemm_ksplit), so rows cut into whole tiles
+// of one width and run with the uncut call's split give the uncut call's outputs.
 int run_linear(const uint8_t* trec, const float* s_a, const uint8_t* pw, const float* bias, const OutSpec& out,
-               int64_t M, int64_t N, int64_t K, int tw, const DeviceInfo& d, cudaStream_t st) {
+               int64_t M, int64_t N, int64_t K, int tw, const DeviceInfo& d, cudaStream_t st, int ksplit = 0) {
     const WLayout W = w_layout(N, K);
     GemmArgs g;
     g.M = M;
@@ -106,6 +107,7 @@ int run_linear(const uint8_t* trec, const float* s_a, const uint8_t* pw, const f
     g.bias = bias;
     g.out = out;
     g.status = d.status;
+    g.ksplit = ksplit > 0 ? ksplit : gemm_ksplit(M, N, K, tw, d.num_sms);
     return launch_gemm(g, false, d.num_sms, st) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
 }
 
@@ -130,6 +132,7 @@ int run_linear_packed(const uint8_t* trec, const float* s_a, const uint8_t* wq, 
     g.bias = bias;
     g.out = out;
     g.status = d.status;
+    g.ksplit = gemm_ksplit(M, N, K, kTileT, d.num_sms);  // as the record form of this shape
     return launch_gemm_packed(g, false, d.num_sms, st) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
 }
 
@@ -920,7 +923,8 @@ int w4a8_prefill_linear_host(const float* x_host, const uint8_t* wq, const uint1
             p.trec = act + A.rec;
             p.tw = A.tw;
             ok = launch_quant(p, cs) == cudaSuccess &&
-                 run_linear(act + A.rec, p.s_a_out, pw, bias, f32_out(y_dev + yo), rows, N, K, h.tw, *d, cs) ==
+                 run_linear(act + A.rec, p.s_a_out, pw, bias, f32_out(y_dev + yo), rows, N, K, h.tw, *d, cs,
+                            gemm_ksplit(M, N, K, h.tw, d->num_sms)) ==
                      W4A8_OK &&
                  cudaEventRecord(r->out[c], cs) == cudaSuccess;
         }

@@ -131,7 +131,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
     }
 }
 
-template <bool DEBUG>
+// KS: CTAs (a cluster) per tile, each contracting 1/KS of K (1, or 2 for the K split).
+template <bool DEBUG, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const GemmArgs args) {
     extern __shared__ uint8_t smem_raw[];
@@ -149,11 +150,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t tiles_t = (args.M + kTileT - 1) / kTileT;
     const int64_t tiles_w = (args.N + kTileW - 1) / kTileW;
     const int64_t ntiles = tiles_t * tiles_w;
-    const int64_t first = blockIdx.x;
+    // With a K split, a cluster of ks CTAs shares each tile (the host launches exactly one tile
+    // per cluster): CTA kr of the cluster contracts blocks kb0 .. kb0 + nbl - 1 of K.
+    constexpr uint32_t ks = static_cast<uint32_t>(KS);
+    static_assert(KS == 1 || (KS == 2 && !DEBUG), "the K split is a two-CTA cluster, outside the debug form");
+    const uint32_t kr = ks > 1 ? cluster_ctarank() : 0u;
+    const int64_t first = blockIdx.x / ks;
+    const uint32_t stride = gridDim.x / ks;
     // the host keeps ntiles * K/64 below 2^31, so the stage counters below fit 32 bits
-    const uint32_t my_tiles = ntiles > first ? static_cast<uint32_t>((ntiles - 1 - first) / gridDim.x + 1) : 0u;
-    const uint32_t nb = static_cast<uint32_t>(args.K / kBlock);
-    const uint32_t spt = (nb + 1) / 2;         // stages per tile
+    const uint32_t my_tiles = ntiles > first ? static_cast<uint32_t>((ntiles - 1 - first) / stride + 1) : 0u;
+    const uint32_t nb = static_cast<uint32_t>(args.K / kBlock);  // blocks of a tile's records
+    const uint32_t nbl = nb / ks, kb0 = kr * nbl;
+    const uint32_t spt = (nbl + 1) / 2;        // stages per tile
     const uint32_t total = my_tiles * spt;     // stages of this CTA, counted across its tiles
     const WaitCtl ctl{abort_flag, args.status, args.wait_limit_ns};
 
@@ -194,11 +202,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = true;
                 for (uint32_t i = 0; ok && i < my_tiles; ++i) {
                     int64_t tt, tw;
-                    tile_at(first + static_cast<int64_t>(i) * gridDim.x, tiles_t, tiles_w, tt, tw);
-                    const uint8_t* tsrc = args.trec + static_cast<int64_t>(tt) * nb * kTokRec;
-                    const uint8_t* wsrc = args.wrec + static_cast<int64_t>(tw) * nb * kWRec;
+                    tile_at(first + static_cast<int64_t>(i) * stride, tiles_t, tiles_w, tt, tw);
+                    // this CTA's first block of the tile's records
+                    const uint8_t* tsrc = args.trec + (static_cast<int64_t>(tt) * nb + kb0) * kTokRec;
+                    const uint8_t* wsrc = args.wrec + (static_cast<int64_t>(tw) * nb + kb0) * kWRec;
                     // the tile's weight scales into L2 ahead of the epilogue's loads
-                    if (!DEBUG) bulk_prefetch_l2(args.sc + static_cast<int64_t>(tw) * nb * kTileW, nb * kTileW * 4u);
+                    if (!DEBUG)
+                        bulk_prefetch_l2(args.sc + (static_cast<int64_t>(tw) * nb + kb0) * kTileW, nbl * kTileW * 4u);
                     for (uint32_t p = 0; p < spt; ++p, ++j) {
                         const int s = static_cast<int>(j % kStages);
                         const uint32_t k = j / kStages;
@@ -206,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ok = false;
                             break;
                         }
-                        const uint32_t b0 = 2 * p, cnt = nb - b0 < 2 ? 1u : 2u;
+                        const uint32_t b0 = 2 * p, cnt = nbl - b0 < 2 ? 1u : 2u;
                         uint8_t* st = smem + s * kStageBytes;
                         mbar_arrive_expect_tx(&full[s], cnt * (kTokRec + kWRec));
                         bulk_load(st, tsrc + static_cast<int64_t>(b0) * kTokRec, cnt * kTokRec, &full[s]);
@@ -242,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t j = i >> 1, k = i & 1u;
                 const int s = static_cast<int>(j % kStages);
                 const uint32_t pair = j & 1u;
-                const uint32_t b0 = 2 * (j % spt), cnt = nb - b0 < 2 ? 1u : 2u;
+                const uint32_t b0 = 2 * (j % spt), cnt = nbl - b0 < 2 ? 1u : 2u;
                 if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (j / kStages) & 1, ctl))) break;
                 tc_fence_after();
                 if (elect_one()) {
@@ -270,6 +280,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             drain_wait(&drain[iw], 0, 100000000ull);
         }
+        if (ks > 1) {  // the epilogue's two cluster barriers of the K split
+            cluster_sync_all();
+            cluster_sync_all();
+        }
     } else {
         // ------------------------------------------------------------ epilogue
         regs_inc<kRegsHigh>();
@@ -281,13 +295,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (uint32_t q0 = 0; q0 < 2 && q0 < total; ++q0) mbar_arrive(&full[q0]);
         uint32_t j = 0;  // stage counter of this CTA
         bool ok = true;
+        // this thread's sums and output position, kept past the tile loop for the K split
+        float y[32];
+        int64_t mt0 = 0, n = 0;
         for (uint32_t i = 0; ok && i < my_tiles; ++i) {
             int64_t tt, tw;
-            tile_at(first + static_cast<int64_t>(i) * gridDim.x, tiles_t, tiles_w, tt, tw);
-            const int64_t mt0 = tt * kTileT + h * 32;  // first token column of this warp
-            const int64_t n = tw * kTileW + row;       // this thread's weight row
-            // this row's scales, block after block; each stage's pair is loaded one stage ahead
-            const float* sct = DEBUG ? nullptr : args.sc + static_cast<int64_t>(tw) * nb * kTileW + row;
+            tile_at(first + static_cast<int64_t>(i) * stride, tiles_t, tiles_w, tt, tw);
+            mt0 = tt * kTileT + h * 32;  // first token column of this warp
+            n = tw * kTileW + row;       // this thread's weight row
+            // this row's scales, block after block (from this CTA's first block of K); each
+            // stage's pair is loaded one stage ahead
+            const float* sct = DEBUG ? nullptr : args.sc + (static_cast<int64_t>(tw) * nb + kb0) * kTileW + row;
             if (!DEBUG) {
                 // this tile's s_a and bias, loaded now into the warp's own slots so the stores at
                 // the end of the tile neither wait on memory nor hold registers through the loop
@@ -297,18 +315,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             float ns0 = 0.0f, ns1 = 0.0f;
             if (!DEBUG) {
                 ns0 = __ldg(sct);
-                if (nb > 1) ns1 = __ldg(sct + kTileW);
+                if (nbl > 1) ns1 = __ldg(sct + kTileW);
             }
-            float y[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) y[c] = 0.0f;
             for (uint32_t p = 0; p < spt; ++p, ++j) {
                 const int s = static_cast<int>(j % kStages);
-                const bool two = 2 * p + 1 < nb;
+                const bool two = 2 * p + 1 < nbl;
                 const float s0 = ns0, s1 = ns1;
                 if (!DEBUG && p + 1 < spt) {
                     ns0 = __ldg(sct + (2 * p + 2) * kTileW);
-                    ns1 = 2 * p + 3 < nb ? __ldg(sct + (2 * p + 3) * kTileW) : 0.0f;
+                    ns1 = 2 * p + 3 < nbl ? __ldg(sct + (2 * p + 3) * kTileW) : 0.0f;
                 }
                 const uint32_t pair = j & 1u, b0 = 2 * pair, b1 = b0 + 1;
                 if (!__all_sync(0xffffffffu, mbar_wait(&tfull[pair], (j >> 1) & 1, ctl))) {
@@ -340,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int c = 0; c < 32; ++c) {
                                 const int64_t m = mt0 + c;
                                 if (m < args.M)
-                                    args.acc[(m * args.N + n) * nb + 2 * p + e] =
+                                    args.acc[(m * args.N + n) * nb + kb0 + 2 * p + e] =
                                         static_cast<int32_t>(__uint_as_float(v[32 * e + c]) * 512.0f);
                             }
                         }
@@ -356,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             if (!DEBUG) __syncwarp();  // every lane: the slots were written by other lanes of the warp
-            if (!DEBUG && n < args.N) {
+            if (!DEBUG && ks == 1 && n < args.N) {
                 const float bn = epi_bias[warp - 4][lane];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
@@ -364,6 +381,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (m < args.M) store_y(args.out, m * args.N + n, fmaf(epi_sa[warp - 4][c], y[c], bn));
                 }
             }
+        }
+        if (ks > 1) {
+            // K split (one tile per cluster): the second CTA leaves its partial sums in its own
+            // stage memory, idle now that its MMAs are complete; the first adds them to its own,
+            // in that order, and stores the tile.  Every thread of both CTAs takes part in both
+            // cluster barriers (the other warps at the end of their roles), also after a wait gave
+            // up (the outputs are then undefined; the status word says so): the second CTA's memory
+            // stays until the first has read it.
+            float* part = reinterpret_cast<float*>(smem) + (warp - 4) * 32 * 32 + lane;  // [warp][c][lane]
+            if (kr == 1) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) part[c * 32] = y[c];
+            }
+            cluster_sync_all();
+            if (kr == 0 && n < args.N) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) y[c] += ld_shared_cluster_f32(part + c * 32, 1);
+                const float bn = epi_bias[warp - 4][lane];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int64_t m = mt0 + c;
+                    if (m < args.M) store_y(args.out, m * args.N + n, fmaf(epi_sa[warp - 4][c], y[c], bn));
+                }
+            }
+            cluster_sync_all();
         }
     }
 
@@ -673,6 +715,12 @@ __device__ __forceinline__ void prefetch_l2_span(const void* p, int64_t bytes) {
     for (uintptr_t a = a0; a < a1; a += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
 }
 
+// This CTA's share of the work: its tiles are first, first + stride, ...; of each tile's K it
+// contracts blocks kb0 .. kb0 + nbl - 1 (all of them unless K is split over a cluster).
+struct KPart {
+    uint32_t stride, kb0, nbl;
+};
+
 // A walk over the (tile, stage of the tile) pairs of a CTA's stages.
 struct StageCursor {
     uint32_t i, p;
@@ -680,16 +728,16 @@ struct StageCursor {
 };
 
 __device__ __forceinline__ void cursor_tile(StageCursor& c, uint32_t my_tiles, int64_t first, int64_t tiles_t,
-                                            int64_t tiles_w) {
-    if (c.i < my_tiles) tile_at32(first + static_cast<int64_t>(c.i) * gridDim.x, tiles_t, tiles_w, c.tt, c.tw);
+                                            int64_t tiles_w, uint32_t stride) {
+    if (c.i < my_tiles) tile_at32(first + static_cast<int64_t>(c.i) * stride, tiles_t, tiles_w, c.tt, c.tw);
 }
 
 __device__ __forceinline__ void cursor_next(StageCursor& c, uint32_t spt, uint32_t my_tiles, int64_t first,
-                                            int64_t tiles_t, int64_t tiles_w) {
+                                            int64_t tiles_t, int64_t tiles_w, uint32_t stride) {
     if (++c.p == spt) {
         c.p = 0;
         ++c.i;
-        cursor_tile(c, my_tiles, first, tiles_t, tiles_w);
+        cursor_tile(c, my_tiles, first, tiles_t, tiles_w, stride);
     }
 }
 
@@ -697,14 +745,15 @@ __device__ __forceinline__ void cursor_next(StageCursor& c, uint32_t spt, uint32
 // ring slot; advances both.
 __device__ __forceinline__ void issue_weights(const GemmArgs& args, uint8_t* smem, uint64_t* wfull, StageCursor& cw,
                                               uint32_t& wnext, uint32_t spt, uint32_t my_tiles, int64_t first,
-                                              int64_t tiles_t, int64_t tiles_w) {
+                                              int64_t tiles_t, int64_t tiles_w, const KPart& kp) {
     namespace P = packed;
     uint64_t* bar = &wfull[wnext % P::kPkSlots];
     mbar_arrive_expect_tx(bar, P::kPk);
-    tma_load_2d(smem + P::kOffPk + (wnext % P::kPkSlots) * P::kPk, &args.wmap, static_cast<int>(64 * cw.p),
+    // x: the stage's first packed byte of a row (32 per block), a multiple of 64 bytes
+    tma_load_2d(smem + P::kOffPk + (wnext % P::kPkSlots) * P::kPk, &args.wmap, static_cast<int>(64 * cw.p + 32 * kp.kb0),
                 static_cast<int>(cw.tw * kTileW), bar);
     ++wnext;
-    cursor_next(cw, spt, my_tiles, first, tiles_t, tiles_w);
+    cursor_next(cw, spt, my_tiles, first, tiles_t, tiles_w, kp.stride);
 }
 
 // 512 s_w[n, b] from the caller's fp16 scales (row pointer swr, null past N), 0 past the last
@@ -721,17 +770,18 @@ __device__ __forceinline__ float weight_scale(const uint16_t* swr, uint32_t b, u
 template <bool DEBUG>
 __device__ __forceinline__ bool expand_stage(const GemmArgs& args, uint8_t* smem, uint64_t* wfull, uint64_t* full,
                                              uint32_t jj, uint32_t spt, uint32_t nb, int64_t first, int64_t tiles_t,
-                                             int64_t tiles_w, int et, const WaitCtl& ctl) {
+                                             int64_t tiles_w, int et, const WaitCtl& ctl, const KPart& kp) {
     namespace P = packed;
     const int xr = et >> 2, xc = et & 3, xsw = (xr >> 1) & 3;
     const uint32_t ti = jj / spt, p = jj - ti * spt;
     int64_t tt, tw;
-    tile_at32(first + static_cast<int64_t>(ti) * gridDim.x, tiles_t, tiles_w, tt, tw);
+    tile_at32(first + static_cast<int64_t>(ti) * kp.stride, tiles_t, tiles_w, tt, tw);
     const int64_t n = tw * kTileW + xr;
-    const uint32_t b = 2 * p + (xc >> 1);
-    const bool live = b < nb;
+    const uint32_t b = 2 * p + (xc >> 1);  // block of this CTA's part of K
+    const bool live = b < kp.nbl;
     // the zero point first: its latency overlaps the wait
-    const uint32_t zz = (!DEBUG && live && (xc & 1) == 0 && n < args.N) ? neg_zero_pair(__ldg(args.z_w + n * nb + b)) : 0u;
+    const uint32_t zz =
+        (!DEBUG && live && (xc & 1) == 0 && n < args.N) ? neg_zero_pair(__ldg(args.z_w + n * nb + kp.kb0 + b)) : 0u;
     if (!__all_sync(0xffffffffu, mbar_wait(&wfull[jj % P::kPkSlots], (jj / P::kPkSlots) & 1, ctl))) return false;
     if (live) {
         const uint4 w =
@@ -755,7 +805,8 @@ __device__ __forceinline__ bool expand_stage(const GemmArgs& args, uint8_t* smem
     return true;
 }
 
-template <bool DEBUG>
+// KS: CTAs (a cluster) per tile, each contracting 1/KS of K, as in gemm_kernel.
+template <bool DEBUG, int KS>
 __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_constant__ GemmArgs args) {
     namespace P = packed;
     extern __shared__ uint8_t smem_raw[];
@@ -774,10 +825,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
     const int64_t tiles_t = (args.M + kTileT - 1) / kTileT;
     const int64_t tiles_w = (args.N + kTileW - 1) / kTileW;
     const int64_t ntiles = tiles_t * tiles_w;
-    const int64_t first = blockIdx.x;
-    const uint32_t my_tiles = ntiles > first ? static_cast<uint32_t>((ntiles - 1 - first) / gridDim.x + 1) : 0u;
-    const uint32_t nb = static_cast<uint32_t>(args.K / kBlock);
-    const uint32_t spt = (nb + 1) / 2;         // stages per tile
+    static_assert(KS == 1 || (KS == 2 && !DEBUG), "the K split is a two-CTA cluster, outside the debug form");
+    const uint32_t kr = KS > 1 ? cluster_ctarank() : 0u;
+    const int64_t first = blockIdx.x / KS;
+    const uint32_t nb = static_cast<uint32_t>(args.K / kBlock);  // blocks of a row
+    const KPart kp{gridDim.x / KS, kr * (nb / KS), nb / KS};
+    const uint32_t my_tiles = ntiles > first ? static_cast<uint32_t>((ntiles - 1 - first) / kp.stride + 1) : 0u;
+    const uint32_t nbl = kp.nbl;
+    const uint32_t spt = (nbl + 1) / 2;        // stages per tile
     const uint32_t total = my_tiles * spt;
     const WaitCtl ctl{abort_flag, args.status, args.wait_limit_ns};
 
@@ -817,15 +872,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
                 // two walks over (tile, stage of the tile): W for the weights (ahead), T for the
                 // token records; each looks its tile up once
                 StageCursor cw{}, ct{};
-                cursor_tile(cw, my_tiles, first, tiles_t, tiles_w);
-                cursor_tile(ct, my_tiles, first, tiles_t, tiles_w);
+                cursor_tile(cw, my_tiles, first, tiles_t, tiles_w, kp.stride);
+                cursor_tile(ct, my_tiles, first, tiles_t, tiles_w, kp.stride);
                 uint32_t wnext = 0;  // stages whose weights were issued
                 const uint32_t ahead = P::kPkSlots - P::kStages;
                 const uint32_t pre = total < static_cast<uint32_t>(P::kPkSlots) ? total : static_cast<uint32_t>(P::kPkSlots);
                 if (args.early)
-                    while (wnext < pre) issue_weights(args, smem, wfull, cw, wnext, spt, my_tiles, first, tiles_t, tiles_w);
+                    while (wnext < pre) issue_weights(args, smem, wfull, cw, wnext, spt, my_tiles, first, tiles_t, tiles_w, kp);
                 griddep_wait();
-                while (wnext < pre) issue_weights(args, smem, wfull, cw, wnext, spt, my_tiles, first, tiles_t, tiles_w);
+                while (wnext < pre) issue_weights(args, smem, wfull, cw, wnext, spt, my_tiles, first, tiles_t, tiles_w, kp);
                 bool ok = true;
                 uint32_t issued = 0;
                 for (uint32_t j = 0; j < total; ++j) {
@@ -834,17 +889,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
                         ok = false;
                         break;
                     }
-                    const uint32_t b0 = 2 * ct.p, cnt = nb - b0 < 2 ? 1u : 2u;
+                    const uint32_t b0 = 2 * ct.p, cnt = nbl - b0 < 2 ? 1u : 2u;
                     uint64_t* bar = &full[j % P::kStages];
                     mbar_arrive_expect_tx(bar, cnt * kTokRec);
                     bulk_load(smem + (j % P::kStages) * P::kStageBytes,
-                              args.trec + (static_cast<int64_t>(ct.tt) * nb + b0) * kTokRec, cnt * kTokRec, bar);
-                    cursor_next(ct, spt, my_tiles, first, tiles_t, tiles_w);
+                              args.trec + (static_cast<int64_t>(ct.tt) * nb + kp.kb0 + b0) * kTokRec, cnt * kTokRec, bar);
+                    cursor_next(ct, spt, my_tiles, first, tiles_t, tiles_w, kp.stride);
                     issued = j + 1;
                     // stage j - kStages is complete, and so is every stage before it: W(j + ahead)
                     // may reuse the slot of stage j + ahead - kPkSlots = j - kStages
                     if (k > 0 && wnext == j + ahead && wnext < total)
-                        issue_weights(args, smem, wfull, cw, wnext, spt, my_tiles, first, tiles_t, tiles_w);
+                        issue_weights(args, smem, wfull, cw, wnext, spt, my_tiles, first, tiles_t, tiles_w, kp);
                 }
                 if (!ok || *abort_flag) {
                     // let every copy already issued land before the CTA exits
@@ -868,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
                 const uint32_t j = i >> 1, k = i & 1u;
                 const int s = static_cast<int>(j % P::kStages);
                 const uint32_t pair = j & 1u;
-                const uint32_t b0 = 2 * (j % spt), cnt = nb - b0 < 2 ? 1u : 2u;
+                const uint32_t b0 = 2 * (j % spt), cnt = nbl - b0 < 2 ? 1u : 2u;
                 if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (j / P::kStages) & 1, ctl))) break;
                 tc_fence_after();
                 if (elect_one()) {
@@ -891,6 +946,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
             __syncwarp();
             drain_wait(&drain[iw], 0, 100000000ull);
         }
+        if (KS > 1) {  // the epilogue's two cluster barriers of the K split
+            cluster_sync_all();
+            cluster_sync_all();
+        }
     } else {
         // ------------------------------------------------------------ epilogue + expansion
         regs_inc<kRegsHigh>();
@@ -904,22 +963,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
         // kernel has finished: nothing here reads what it writes
         if (!args.early) griddep_wait();
         for (uint32_t jj = 0; ok && jj < total && jj < static_cast<uint32_t>(P::kStages); ++jj)
-            ok = expand_stage<DEBUG>(args, smem, wfull, full, jj, spt, nb, first, tiles_t, tiles_w, et, ctl);
+            ok = expand_stage<DEBUG>(args, smem, wfull, full, jj, spt, nb, first, tiles_t, tiles_w, et, ctl, kp);
         if (args.early) griddep_wait();
         // the TMEM buffers start free: release the first two stages
         if (lane == 0)
             for (uint32_t q0 = 0; q0 < 2 && q0 < total; ++q0) mbar_arrive(&full[q0]);
         uint32_t j = 0;  // stage counter of this CTA
+        // this thread's sums and output position, kept past the tile loop for the K split
+        float y[32];
+        int64_t mt0 = 0, n = 0;
         for (uint32_t i = 0; ok && i < my_tiles; ++i) {
             int64_t tt, tw;
-            tile_at32(first + static_cast<int64_t>(i) * gridDim.x, tiles_t, tiles_w, tt, tw);
-            const int64_t mt0 = tt * kTileT + h * 32;  // first token column of this warp
-            const int64_t n = tw * kTileW + row;       // this thread's weight row
-            const uint16_t* swr = (!DEBUG && n < args.N) ? args.s_w + n * nb : nullptr;
+            tile_at32(first + static_cast<int64_t>(i) * kp.stride, tiles_t, tiles_w, tt, tw);
+            mt0 = tt * kTileT + h * 32;  // first token column of this warp
+            n = tw * kTileW + row;       // this thread's weight row
+            // this row's scales from this CTA's first block of K
+            const uint16_t* swr = (!DEBUG && n < args.N) ? args.s_w + n * nb + kp.kb0 : nullptr;
             if (!DEBUG && i + 1 < my_tiles && h == 0) {
                 // the next tile's scales and zero points into L2 while this tile runs
                 int64_t tt1, tw1;
-                tile_at32(first + static_cast<int64_t>(i + 1) * gridDim.x, tiles_t, tiles_w, tt1, tw1);
+                tile_at32(first + static_cast<int64_t>(i + 1) * kp.stride, tiles_t, tiles_w, tt1, tw1);
                 const int64_t n1 = tw1 * kTileW + row;
                 if (n1 < args.N) {
                     prefetch_l2_span(args.s_w + n1 * nb, nb * 2);
@@ -931,17 +994,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
                 epi_bias[warp - 4][lane] = (args.bias && n < args.N) ? __ldg(args.bias + n) : 0.0f;
             }
             // 512 s_w: the power of two undoes the 2^-9 of the e4m3 weight operand (exact)
-            float ns0 = weight_scale(swr, 0, nb), ns1 = weight_scale(swr, 1, nb);
-            float y[32];
+            float ns0 = weight_scale(swr, 0, nbl), ns1 = weight_scale(swr, 1, nbl);
 #pragma unroll
             for (int c = 0; c < 32; ++c) y[c] = 0.0f;
             for (uint32_t p = 0; p < spt; ++p, ++j) {
                 const int s = static_cast<int>(j % P::kStages);
-                const bool two = 2 * p + 1 < nb;
+                const bool two = 2 * p + 1 < nbl;
                 const float s0 = ns0, s1 = ns1;
                 if (!DEBUG && p + 1 < spt) {
-                    ns0 = weight_scale(swr, 2 * p + 2, nb);
-                    ns1 = weight_scale(swr, 2 * p + 3, nb);
+                    ns0 = weight_scale(swr, 2 * p + 2, nbl);
+                    ns1 = weight_scale(swr, 2 * p + 3, nbl);
                 }
                 const uint32_t pair = j & 1u, b0 = 2 * pair;
                 if (!__all_sync(0xffffffffu, mbar_wait(&tfull[pair], (j >> 1) & 1, ctl))) {
@@ -974,7 +1036,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
                             for (int c = 0; c < 32; ++c) {
                                 const int64_t m = mt0 + c;
                                 if (m < args.M)
-                                    args.acc[(m * args.N + n) * nb + 2 * p + e] =
+                                    args.acc[(m * args.N + n) * nb + kp.kb0 + 2 * p + e] =
                                         static_cast<int32_t>(__uint_as_float(v[c]) * 512.0f);
                             }
                         }
@@ -987,14 +1049,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
                 // operand stage s is free too (the stage's MMAs are done): the weights of stage
                 // j + kStages go in, with the accumulators already folded (their registers free)
                 if (j + P::kStages < total &&
-                    !expand_stage<DEBUG>(args, smem, wfull, full, j + P::kStages, spt, nb, first, tiles_t, tiles_w, et, ctl)) {
+                    !expand_stage<DEBUG>(args, smem, wfull, full, j + P::kStages, spt, nb, first, tiles_t, tiles_w, et, ctl,
+                                         kp)) {
                     ok = false;
                     break;
                 }
             }
             if (!ok) break;
             if (!DEBUG) __syncwarp();  // every lane: the slots were written by other lanes of the warp
-            if (!DEBUG && n < args.N) {
+            if (!DEBUG && KS == 1 && n < args.N) {
                 const float bn = epi_bias[warp - 4][lane];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
@@ -1002,6 +1065,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
                     if (m < args.M) store_y(args.out, m * args.N + n, fmaf(epi_sa[warp - 4][c], y[c], bn));
                 }
             }
+        }
+        if (KS > 1) {
+            // K split: the hand-off of gemm_kernel (the second CTA's partial sums through its own
+            // idle stage memory, added by the first in the same order), so every output equals
+            // the record form's bit for bit
+            float* part = reinterpret_cast<float*>(smem) + (warp - 4) * 32 * 32 + lane;  // [warp][c][lane]
+            if (kr == 1) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) part[c * 32] = y[c];
+            }
+            cluster_sync_all();
+            if (kr == 0 && n < args.N) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) y[c] += ld_shared_cluster_f32(part + c * 32, 1);
+                const float bn = epi_bias[warp - 4][lane];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int64_t m = mt0 + c;
+                    if (m < args.M) store_y(args.out, m * args.N + n, fmaf(epi_sa[warp - 4][c], y[c], bn));
+                }
+            }
+            cluster_sync_all();
         }
     }
 
@@ -1031,7 +1116,7 @@ __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
 
 template <typename Kernel>
 cudaError_t launch(Kernel kernel, int smem_bytes, bool* attr_done, int64_t tiles, const GemmArgs& a, int num_sms,
-                   cudaStream_t s, int threads = kThreads) {
+                   cudaStream_t s, int threads = kThreads, int cluster = 1) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_done[dev]) {
@@ -1039,24 +1124,30 @@ cudaError_t launch(Kernel kernel, int smem_bytes, bool* attr_done, int64_t tiles
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    const int64_t grid = tiles < num_sms ? tiles : num_sms;
+    // a K split runs exactly one tile per cluster of `cluster` CTAs (the host checked that they
+    // all fit on the SMs at once)
+    const int64_t grid = cluster > 1 ? tiles * cluster : (tiles < num_sms ? tiles : num_sms);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = cluster > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& a, bool debug, int num_sms, cudaStream_t s) {
-    static bool attr_done[4][64] = {};
+    static bool attr_done[5][64] = {};
     if (num_sms < 1) return cudaErrorInvalidValue;
     const int64_t tiles_w = (a.N + kTileW - 1) / kTileW;
     if (a.tw == wide::kTN) {
@@ -1066,8 +1157,20 @@ cudaError_t launch_gemm(const GemmArgs& a, bool debug, int num_sms, cudaStream_t
     }
     if (a.tw != kTileT) return cudaErrorInvalidValue;
     const int64_t tiles = ((a.M + kTileT - 1) / kTileT) * tiles_w;
-    return debug ? launch(gemm_kernel<true>, kSmemBytes, attr_done[3], tiles, a, num_sms, s)
-                 : launch(gemm_kernel<false>, kSmemBytes, attr_done[0], tiles, a, num_sms, s);
+    // the per-block accumulators of the debug form do not depend on how K is shared
+    if (debug) return launch(gemm_kernel<true, 1>, kSmemBytes, attr_done[3], tiles, a, num_sms, s);
+    if (a.ksplit == 1) return launch(gemm_kernel<false, 1>, kSmemBytes, attr_done[0], tiles, a, num_sms, s);
+    if (a.ksplit != 2 || tiles * 2 > num_sms || (a.K / kBlock) % 2 != 0) return cudaErrorInvalidValue;
+    return launch(gemm_kernel<false, 2>, kSmemBytes, attr_done[4], tiles, a, num_sms, s, kThreads, 2);
+}
+
+int gemm_ksplit(int64_t M, int64_t N, int64_t K, int tw, int num_sms) {
+    if (tw != kTileT || M <= 0 || N <= 0) return 1;
+    const int64_t tiles = ((M + kTileT - 1) / kTileT) * ((N + kTileW - 1) / kTileW);
+    const int64_t nb = K / kBlock;
+    // Measured: at K = 1024 (8 tiles) the split lost ~2 us to the cluster's hand-off, at K = 6144
+    // (64 tiles) it saved 12 us of 41; from K = 2048 on each CTA drops eight stages or more.
+    return (tiles * 2 <= num_sms && nb >= 32 && nb % 2 == 0) ? 2 : 1;
 }
 
 namespace {
@@ -1091,7 +1194,7 @@ EncodeTiledFn encode_tiled() {
 }  // namespace
 
 cudaError_t launch_gemm_packed(const GemmArgs& a0, bool debug, int num_sms, cudaStream_t s) {
-    static bool attr_done[2][64] = {};
+    static bool attr_done[3][64] = {};
     if (num_sms < 1 || a0.tw != kTileT || !a0.wq || (!debug && (!a0.s_w || !a0.z_w))) return cudaErrorInvalidValue;
     const EncodeTiledFn enc = encode_tiled();
     if (!enc) return cudaErrorNotSupported;
@@ -1107,8 +1210,10 @@ cudaError_t launch_gemm_packed(const GemmArgs& a0, bool debug, int num_sms, cuda
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const int64_t tiles = ((a.M + kTileT - 1) / kTileT) * ((a.N + kTileW - 1) / kTileW);
-    return debug ? launch(gemm_packed_kernel<true>, packed::kSmemBytes, attr_done[1], tiles, a, num_sms, s)
-                 : launch(gemm_packed_kernel<false>, packed::kSmemBytes, attr_done[0], tiles, a, num_sms, s);
+    if (debug) return launch(gemm_packed_kernel<true, 1>, packed::kSmemBytes, attr_done[1], tiles, a, num_sms, s);
+    if (a.ksplit == 1) return launch(gemm_packed_kernel<false, 1>, packed::kSmemBytes, attr_done[0], tiles, a, num_sms, s);
+    if (a.ksplit != 2 || tiles * 2 > num_sms || (a.K / kBlock) % 2 != 0) return cudaErrorInvalidValue;
+    return launch(gemm_packed_kernel<false, 2>, packed::kSmemBytes, attr_done[2], tiles, a, num_sms, s, kThreads, 2);
 }
 
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s) {

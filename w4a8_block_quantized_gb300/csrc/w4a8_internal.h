@@ -129,6 +129,7 @@ struct GemmArgs {
     int64_t M = 0, N = 0, K = 0;       // output rows / columns (row stride N) and depth
     const uint8_t* trec = nullptr;      // token records [ceil(M/tw)][K/64]
     int tw = 128;                       // token tile (record width): 128 or 256
+    int ksplit = 1;                     // 128-token tiles: CTAs (a cluster) sharing one tile's K range
     const uint8_t* wrec = nullptr;      // weight records [ceil(N/128)][K/64]
     const float* sc = nullptr;          // weight scales [ceil(N/128)][K/64][128]
     // packed-weight form (128-token tiles): the caller's wq [N][K/2], s_w and z_w [N][K/64],
@@ -147,8 +148,15 @@ struct GemmArgs {
 };
 
 // Persistent launch over ceil(M/tw) x ceil(N/128) output tiles on at most `num_sms` CTAs, from
-// weight records (wrec, sc).
+// weight records (wrec, sc).  With ksplit = 2 (128-token tiles) every tile is shared by a
+// cluster of two CTAs, each contracting half of K; the second hands its partial sums to the
+// first through distributed shared memory.
 cudaError_t launch_gemm(const GemmArgs& a, bool debug, int num_sms, cudaStream_t s);
+// The K split for a record contraction of this shape: 2 when its 128-token tiles would leave
+// more than half of the SMs idle and K is an even number of at least 32 64-blocks, else 1.
+// A function of the uncut call's shape, so every entry point (and every row chunk of the
+// host-buffer call, which is told the uncut call's split) sums each output the same way.
+int gemm_ksplit(int64_t M, int64_t N, int64_t K, int tw, int num_sms);
 // The same contraction with 128-token tiles straight from the packed weights (wq, s_w, z_w): the
 // u4 codes are staged by TMA and expanded to the tensor-core operand in shared memory.  With
 // `early` set the weights are staged before the previous kernel in the stream has finished.
