@@ -81,7 +81,12 @@ int w4a8_quant_pack(const float *x, int64_t M, int64_t K,
 
 /* Quantized linear from pre-quantized activations (section 3 eq. (2), section 4
  * steps 2-3): block-64 integer contraction on the tensor cores, then the scale /
- * zero-point / bias epilogue writing fp32 y [M][N] directly.
+ * zero-point / bias epilogue writing fp32 y [M][N] directly.  Each output sums its blocks'
+ * scaled products in an order that depends only on the shape (M, N, K) and the GPU's SM
+ * count: in block order, or,
+ * for linears with few 128-token output tiles and K of at least 2048, as the sum of the two
+ * halves of K (two CTAs share the tile).  Every tensor-core entry point takes the same order
+ * for the same shape.
  * workspace: at least w4a8_linear_workspace_bytes(M, N, K) bytes (the activation
  * operand re-encoded for the tensor cores).  In the few-token form that size is 0 and
  * `workspace` may be NULL. */
