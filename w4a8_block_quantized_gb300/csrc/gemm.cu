@@ -309,13 +309,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!DEBUG) {
                 // this tile's s_a and bias, loaded now into the warp's own slots so the stores at
                 // the end of the tile neither wait on memory nor hold registers through the loop
-                epi_sa[warp - 4][lane] = mt0 + lane < args.M ? __ldg(args.s_a + mt0 + lane) : 0.0f;
+                epi_sa[warp - 4][lane] = mt0 + lane < args.M ? __ldcg(args.s_a + mt0 + lane) : 0.0f;
                 epi_bias[warp - 4][lane] = (args.bias && n < args.N) ? __ldg(args.bias + n) : 0.0f;
             }
             float ns0 = 0.0f, ns1 = 0.0f;
             if (!DEBUG) {
-                ns0 = __ldg(sct);
-                if (nbl > 1) ns1 = __ldg(sct + kTileW);
+                ns0 = __ldcg(sct);
+                if (nbl > 1) ns1 = __ldcg(sct + kTileW);
             }
 #pragma unroll
             for (int c = 0; c < 32; ++c) y[c] = 0.0f;
@@ -324,8 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool two = 2 * p + 1 < nbl;
                 const float s0 = ns0, s1 = ns1;
                 if (!DEBUG && p + 1 < spt) {
-                    ns0 = __ldg(sct + (2 * p + 2) * kTileW);
-                    ns1 = 2 * p + 3 < nbl ? __ldg(sct + (2 * p + 3) * kTileW) : 0.0f;
+                    ns0 = __ldcg(sct + (2 * p + 2) * kTileW);
+                    ns1 = 2 * p + 3 < nbl ? __ldcg(sct + (2 * p + 3) * kTileW) : 0.0f;
                 }
                 const uint32_t pair = j & 1u, b0 = 2 * pair, b1 = b0 + 1;
                 if (!__all_sync(0xffffffffu, mbar_wait(&tfull[pair], (j >> 1) & 1, ctl))) {
@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
             const int64_t mt0 = tt * W::kTN + h * 64;
             const int64_t n = tw * kTileW + row;
             const float* sct = DEBUG ? nullptr : args.sc + static_cast<int64_t>(tw) * nb * kTileW + row;
-            float ns = DEBUG ? 0.0f : __ldg(sct);
+            float ns = DEBUG ? 0.0f : __ldcg(sct);
             float y[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) y[c] = 0.0f;
@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
             };
             for (uint32_t b = 0; b < nb; ++b, ++g) {
                 const float sb = ns;
-                if (!DEBUG && b + 1 < nb) ns = __ldg(sct + (b + 1) * kTileW);
+                if (!DEBUG && b + 1 < nb) ns = __ldcg(sct + (b + 1) * kTileW);
                 const uint32_t buf = g & 1u;
                 if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], (g >> 1) & 1, ctl))) {
                     ok = false;
@@ -990,7 +990,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
                 }
             }
             if (!DEBUG) {
-                epi_sa[warp - 4][lane] = mt0 + lane < args.M ? __ldg(args.s_a + mt0 + lane) : 0.0f;
+                epi_sa[warp - 4][lane] = mt0 + lane < args.M ? __ldcg(args.s_a + mt0 + lane) : 0.0f;
                 epi_bias[warp - 4][lane] = (args.bias && n < args.N) ? __ldg(args.bias + n) : 0.0f;
             }
             // 512 s_w: the power of two undoes the 2^-9 of the e4m3 weight operand (exact)

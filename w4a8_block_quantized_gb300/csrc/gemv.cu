@@ -486,14 +486,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     const int4* src = reinterpret_cast<const int4*>(L.a_q + m * K + 64 * b);
 #pragma unroll
                     for (int p = 0; p < 4; ++p) {
-                        const int4 v = __ldg(src + p);
+                        const int4 v = __ldcg(src + p);
                         *reinterpret_cast<uint4*>(plane_addr(m, b, p)) =
                             plane_of(static_cast<uint32_t>(v.x), static_cast<uint32_t>(v.y), static_cast<uint32_t>(v.z),
                                      static_cast<uint32_t>(v.w));
                     }
-                    rsf_sm[u] = static_cast<float>(__ldg(L.rs + u));
+                    rsf_sm[u] = static_cast<float>(__ldcg(L.rs + u));
                 }
-                if (threadIdx.x < MT) sa_sm[li][threadIdx.x] = __ldg(L.s_a + threadIdx.x);
+                if (threadIdx.x < MT) sa_sm[li][threadIdx.x] = __ldcg(L.s_a + threadIdx.x);
             }
         }
         named_bar_sync(kBarStage, kCW * 32);

@@ -95,7 +95,11 @@ __device__ __forceinline__ void regs_inc() {
 
 // ---------------------------------------------------------------- programmatic dependent launch
 // Blocks until the grids this one depends on have completed and their memory is visible
-// (returns at once for a grid launched without a programmatic dependency).
+// (returns at once for a grid launched without a programmatic dependency).  What those grids
+// write is read afterwards with coherent loads (__ldcg, or bulk copies), never through the
+// read-only path (__ldg): that data is not read-only for this grid's lifetime, and a
+// read-only load may be scheduled ahead of the wait.  Measured: a contraction variant whose
+// prologue ran alongside the pre-pass and loaded s_a with __ldg read zeros now and then.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Allows the next programmatic-dependent grid to be scheduled before this one completes.
 __device__ __forceinline__ void griddep_launch_dependents() {
