@@ -11,6 +11,8 @@
 // per weight + one fp16 s_w and one fp16 z_w per 64 weights = 4.5 bits per weight).
 //
 // Persistent CTAs, one per SM, each walking row tiles t = blockIdx.x, blockIdx.x + grid, ...
+// (a launch of several linears: a contiguous range of tiles per CTA instead, so that each CTA
+// stages the activations of only the one or two linears its range touches)
 //   warp 8       producer: per tile three bulk copies into a ring of shared-memory stages --
 //                the tile's packed rows (contiguous: rows are K/2 bytes apart) and the
 //                16-byte-aligned interiors of its s_w and z_w rows (the few elements before
@@ -41,6 +43,9 @@
 #include "w4a8_internal.h"
 
 #include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <mutex>
 
 namespace w4a8 {
 namespace {
@@ -84,10 +89,13 @@ struct GemvBatch {
     int early = 0;     // the previous kernel in the stream writes none of the weights
 };
 
-// Shared-memory plan of one launch (computed on the host; identical for every CTA).  One tile
-// height for all linears (chosen over all their tiles; the measured alternative, each linear's
-// own height, balanced a decoder layer's tiles worse over the CTAs); a stage slot holds the
-// largest linear's tile.
+// Shared-memory plan of one launch (computed on the host; identical for every CTA).  The tile
+// heights (GemvLin::tr) are one for all linears, or, for a launch of several, may be one per
+// linear chosen so that every tile holds about the same bytes (a stage slot holds the largest
+// tile, so a deep linear's tiles no longer size the slots of the shallow ones).  Measured on a
+// 2048-hidden decoder layer's seven linears in one launch: per-linear heights with contiguous
+// ranges cut the step from 23.8 to 20.5 us (every CTA had quantized all seven rows, and the
+// slots sized for the 6144-deep linear left two stages).  `tr` below is the largest height.
 struct GemvPlan {
     int tr = 8;               // rows per tile
     int wpr = 1;              // warps per row (tr < 8)
@@ -97,9 +105,55 @@ struct GemvPlan {
     uint32_t smem = 0;
     int64_t tiles = 0;
     int grid = 0;
+    int contig = 0;           // each CTA takes a contiguous range of tiles (else every grid-th tile)
 };
 
 constexpr uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+// One candidate of a plan: tile height trs[i] for linear i; a stage slot holds the largest tile.
+// Replaces *best when its cost is lower.
+void consider_plan(const GemvArgs* a, int count, const int* trs, uint32_t bar_off, uint32_t stage_off, int num_sms,
+                   GemvPlan* best, int64_t* best_cost, int* best_tr) {
+    uint32_t wb = 0, sz = 0;
+    int64_t tiles = 0;
+    int trmax = 0;
+    for (int i = 0; i < count; ++i) {
+        const int64_t K = a[i].K, nb = K / kBlock;
+        wb = std::max(wb, align_up(static_cast<uint32_t>(trs[i] * K / 2), 16));
+        sz = std::max(sz, align_up(static_cast<uint32_t>(trs[i] * nb * 2 + 32), 16));
+        tiles += (a[i].N + trs[i] - 1) / trs[i];
+        trmax = std::max(trmax, trs[i]);
+    }
+    const uint32_t stage = align_up(wb + 2 * sz, 128);
+    const int64_t room = kSmemCap - 1024 - static_cast<int64_t>(stage_off);
+    int64_t ns = room / stage;
+    if (ns > kMaxStages) ns = kMaxStages;
+    if (ns < 2) return;
+    const int64_t grid = tiles < num_sms ? tiles : num_sms;
+    const int64_t waves = (tiles + grid - 1) / grid;
+    // bytes streamed by the busiest CTA, plus a fixed cost per tile (barriers, sums), counted as
+    // 16 KiB of streaming.  Measured on the 7B-class decode pair: with a 4 KiB charge the planner
+    // split the 14336-deep rows over two warps (4-row tiles, seven waves); one warp per row (8-row
+    // tiles, four waves) made the pair's step 7% faster, and the decoder-layer and single-linear
+    // steps were unchanged.
+    const int64_t cost = waves * (static_cast<int64_t>(stage) + 16384);
+    if (*best_cost >= 0 && cost >= *best_cost) return;
+    *best_cost = cost;
+    best->tr = trmax;
+    best->wpr = trmax >= 8 ? 1 : 8 / trmax;
+    best->ns = static_cast<int>(ns);
+    best->bar_off = bar_off;
+    best->stage_off = stage_off;
+    best->stage_bytes = stage;
+    best->w_bytes = wb;
+    best->sz_bytes = sz;
+    best->smem = stage_off + static_cast<uint32_t>(ns) * stage + 1024;  // + base alignment slack
+    best->tiles = tiles;
+    best->grid = static_cast<int>(grid);
+    // a batch: contiguous tile ranges, so that a CTA stages only the linears of its range
+    best->contig = count > 1 ? 1 : 0;
+    for (int i = 0; i < count; ++i) best_tr[i] = trs[i];
+}
 
 // Lays out the linears' staging areas (into b) and picks the tile height; false if they do not
 // fit one CTA's shared memory next to two weight stages.
@@ -107,8 +161,8 @@ constexpr uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a
 // one warp, whose sum runs in the same order whatever the height; a launch of several linears
 // uses only those, so its outputs equal each linear's own launch bit for bit when that launch
 // also has one warp per row.
-bool make_plan(const GemvArgs* a, int count, bool quantize, int num_sms, GemvBatch* b, GemvPlan* out,
-               int min_tr = 1) {
+bool plan_uncached(const GemvArgs* a, int count, bool quantize, int num_sms, GemvBatch* b, GemvPlan* out,
+                  int min_tr) {
     if (count < 1 || count > kGemvMaxLinears) return false;
     const int64_t M = a[0].M;
     int64_t off = 0;
@@ -135,54 +189,106 @@ bool make_plan(const GemvArgs* a, int count, bool quantize, int num_sms, GemvBat
     const uint32_t stage_off = align_up(bar_off + (2 * kMaxStages + 1) * 8 + 16, 1024);
     GemvPlan best;
     int64_t best_cost = -1;
-    for (int tr : {32, 16, 8, 4, 2, 1}) {
+    int best_tr[kGemvMaxLinears];
+    int trs[kGemvMaxLinears];
+    for (int tr : {32, 16, 8, 4, 2, 1}) {  // one height for every linear
         if (tr > 8 && M > 2) continue;  // more rows per warp only for one or two tokens
         if (tr < min_tr) continue;
-        uint32_t wb = 0, sz = 0;
-        int64_t tiles = 0;
-        for (int i = 0; i < count; ++i) {
-            const int64_t K = a[i].K, nb = K / kBlock;
-            wb = std::max(wb, align_up(static_cast<uint32_t>(tr * K / 2), 16));
-            sz = std::max(sz, align_up(static_cast<uint32_t>(tr * nb * 2 + 32), 16));
-            tiles += (a[i].N + tr - 1) / tr;
-        }
-        const uint32_t stage = align_up(wb + 2 * sz, 128);
-        const int64_t room = kSmemCap - 1024 - static_cast<int64_t>(stage_off);
-        int64_t ns = room / stage;
-        if (ns > kMaxStages) ns = kMaxStages;
-        if (ns < 2) continue;
-        const int64_t grid = tiles < num_sms ? tiles : num_sms;
-        const int64_t waves = (tiles + grid - 1) / grid;
-        // bytes streamed by the busiest CTA, plus a fixed cost per tile (barriers, sums), counted
-        // as 16 KiB of streaming.  Measured on the 7B-class decode pair: with a 4 KiB charge the
-        // planner split the 14336-deep rows over two warps (4-row tiles, seven waves); one warp per
-        // row (8-row tiles, four waves) made the pair's step 7% faster, and the decoder-layer and
-        // single-linear steps were unchanged.
-        const int64_t cost = waves * (static_cast<int64_t>(stage) + 16384);
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best.tr = tr;
-            best.wpr = tr >= 8 ? 1 : 8 / tr;
-            best.ns = static_cast<int>(ns);
-            best.bar_off = bar_off;
-            best.stage_off = stage_off;
-            best.stage_bytes = stage;
-            best.w_bytes = wb;
-            best.sz_bytes = sz;
-            best.smem = stage_off + static_cast<uint32_t>(ns) * stage + 1024;  // + base alignment slack
-            best.tiles = tiles;
-            best.grid = static_cast<int>(grid);
+        for (int i = 0; i < count; ++i) trs[i] = tr;
+        consider_plan(a, count, trs, bar_off, stage_off, num_sms, &best, &best_cost, best_tr);
+    }
+    if (count > 1) {
+        // A height per linear (multiples of 8, so every row keeps one warp), for tiles of about
+        // `target` bytes in every linear: the stage slots then fit the tiles of a deep linear and
+        // of a shallow one alike, and more of them fit.
+        const int hmax = M > 2 ? 8 : 32;
+        for (int64_t target : {8192, 12288, 16384, 24576, 32768, 49152, 65536}) {
+            for (int i = 0; i < count; ++i) {
+                const int64_t row = a[i].K / 2;
+                const int64_t t = 8 * std::max<int64_t>(1, (target + 4 * row) / (8 * row));
+                trs[i] = static_cast<int>(std::max<int64_t>(std::min<int64_t>(t, hmax), std::max(min_tr, 8)));
+            }
+            consider_plan(a, count, trs, bar_off, stage_off, num_sms, &best, &best_cost, best_tr);
         }
     }
     if (best_cost < 0) return false;
     int64_t t0 = 0;
     for (int i = 0; i < count; ++i) {
         b->lin[i].tile0 = t0;
-        b->lin[i].tr = best.tr;
-        t0 += (a[i].N + best.tr - 1) / best.tr;
+        b->lin[i].tr = best_tr[i];
+        t0 += (a[i].N + best_tr[i] - 1) / best_tr[i];
     }
     *out = best;
     return true;
+}
+
+// make_plan remembers its answers: one call of the API plans the same shapes several times
+// (the support checks, the batch's own plan, its launch), and a decode step is short enough
+// that host time shows in it.  A small direct-mapped table keyed by everything the plan reads.
+struct PlanKey {
+    int32_t count, quantize, num_sms, min_tr;
+    int64_t M, K[kGemvMaxLinears], N[kGemvMaxLinears];
+};
+struct PlanMemo {
+    bool used = false, ok = false;
+    PlanKey key;
+    GemvPlan plan;
+    GemvLin lin[kGemvMaxLinears];  // the layout fields make_plan sets
+};
+constexpr int kPlanSlots = 64;
+PlanMemo g_plan_memo[kPlanSlots];
+std::mutex g_plan_mu;
+
+bool make_plan(const GemvArgs* a, int count, bool quantize, int num_sms, GemvBatch* b, GemvPlan* out,
+               int min_tr = 1) {
+    if (count < 1 || count > kGemvMaxLinears) return false;
+    if (count == 1) return plan_uncached(a, count, quantize, num_sms, b, out, min_tr);  // cheaper than a lookup
+    PlanKey k;
+    std::memset(&k, 0, sizeof(k));
+    k.count = count;
+    k.quantize = quantize ? 1 : 0;
+    k.num_sms = num_sms;
+    k.min_tr = min_tr;
+    k.M = a[0].M;
+    uint64_t h = 1469598103934665603ull;
+    auto mix = [&h](uint64_t v) { h = (h ^ v) * 1099511628211ull; };
+    mix(static_cast<uint64_t>(count) | static_cast<uint64_t>(k.quantize) << 8 | static_cast<uint64_t>(min_tr) << 16);
+    mix(static_cast<uint64_t>(num_sms));
+    mix(static_cast<uint64_t>(k.M));
+    for (int i = 0; i < count; ++i) {
+        k.K[i] = a[i].K;
+        k.N[i] = a[i].N;
+        mix(static_cast<uint64_t>(a[i].K));
+        mix(static_cast<uint64_t>(a[i].N));
+    }
+    PlanMemo& m = g_plan_memo[h % kPlanSlots];
+    {
+        std::lock_guard<std::mutex> lk(g_plan_mu);
+        if (m.used && std::memcmp(&m.key, &k, sizeof(k)) == 0) {
+            for (int i = 0; i < count; ++i) {
+                GemvLin& L = b->lin[i];
+                L.chunks = m.lin[i].chunks;
+                L.act_stride = m.lin[i].act_stride;
+                L.act_off = m.lin[i].act_off;
+                L.rs_off = m.lin[i].rs_off;
+                L.x_off = m.lin[i].x_off;
+                L.tile0 = m.lin[i].tile0;
+                L.tr = m.lin[i].tr;
+            }
+            if (m.ok) *out = m.plan;
+            return m.ok;
+        }
+    }
+    GemvPlan P;
+    const bool ok = plan_uncached(a, count, quantize, num_sms, b, &P, min_tr);
+    if (ok) *out = P;
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    m.used = true;
+    m.ok = ok;
+    m.key = k;
+    m.plan = P;
+    for (int i = 0; i < count; ++i) m.lin[i] = b->lin[i];
+    return ok;
 }
 
 // The linear that global tile g belongs to.
@@ -346,8 +452,20 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ns = P.ns;
-    const uint32_t my_tiles =
-        P.tiles > blockIdx.x ? static_cast<uint32_t>((P.tiles - 1 - blockIdx.x) / gridDim.x + 1) : 0u;
+    // this CTA's tiles g_lo, g_lo + g_step, ...: a contiguous range (a batch: the CTA then stages
+    // only the one or two linears its range touches) or every gridDim.x-th tile
+    int64_t g_lo = blockIdx.x, g_step = gridDim.x;
+    uint32_t my_tiles;
+    if (P.contig) {
+        g_lo = P.tiles * blockIdx.x / gridDim.x;
+        my_tiles = static_cast<uint32_t>(P.tiles * (blockIdx.x + 1) / gridDim.x - g_lo);
+        g_step = 1;
+    } else {
+        my_tiles = P.tiles > blockIdx.x ? static_cast<uint32_t>((P.tiles - 1 - blockIdx.x) / gridDim.x + 1) : 0u;
+    }
+    // the linears those tiles belong to (tiles are numbered linear after linear)
+    const int li_lo = my_tiles ? lin_of(B, g_lo) : 0;
+    const int li_hi = my_tiles ? lin_of(B, g_lo + static_cast<int64_t>(my_tiles - 1) * g_step) : -1;
     const WaitCtl ctl{abort_flag, status, wait_limit_ns};
 
     if (threadIdx.x == 0) {
@@ -370,16 +488,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
             uint32_t i = 0;
             if (B.early)
                 for (; i < my_tiles && i < static_cast<uint32_t>(ns); ++i) {
-                    const int64_t g = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
+                    const int64_t g = g_lo + static_cast<int64_t>(i) * g_step;
                     issue_tile(B.lin[lin_of(B, g)], P, smem, full, g, static_cast<int>(i));
                 }
             griddep_wait();
             if (B.quantize) {
                 // the rows to quantize, every linear's: every CTA reads them
                 uint32_t xbytes = 0;
-                for (int li = 0; li < B.count; ++li) xbytes += static_cast<uint32_t>(MT * B.lin[li].K * 4);
+                for (int li = li_lo; li <= li_hi; ++li) xbytes += static_cast<uint32_t>(MT * B.lin[li].K * 4);
                 mbar_arrive_expect_tx(xbar, xbytes);
-                for (int li = 0; li < B.count; ++li)
+                for (int li = li_lo; li <= li_hi; ++li)
                     bulk_load(smem + B.lin[li].x_off, B.lin[li].x, static_cast<uint32_t>(MT * B.lin[li].K * 4), xbar);
             }
             bool ok = true;
@@ -390,7 +508,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     ok = false;
                     break;
                 }
-                const int64_t g = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
+                const int64_t g = g_lo + static_cast<int64_t>(i) * g_step;
                 issue_tile(B.lin[lin_of(B, g)], P, smem, full, g, s);
             }
             if (!ok || *abort_flag) {
@@ -410,7 +528,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         // act_off + m * act_stride + 2048 c + 512 p + 16 l; the block row sums as floats; s_a.
         const bool got = !B.quantize || __all_sync(0xffffffffu, mbar_wait(xbar, 0, ctl));
         int par = 0;  // alternates the amax slots from row to row
-        for (int li = 0; li < B.count; ++li) {
+        for (int li = li_lo; li <= li_hi; ++li) {
             const GemvLin& L = B.lin[li];
             const int64_t K = L.K, nb = K / kBlock;
             float* rsf_sm = reinterpret_cast<float*>(smem + L.rs_off);
@@ -505,7 +623,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int rslot = warp / wpr, sidx = warp - rslot * wpr;
         for (uint32_t i = 0; i < my_tiles; ++i) {
             const int s = static_cast<int>(i % ns);
-            const int64_t g = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
+            const int64_t g = g_lo + static_cast<int64_t>(i) * g_step;
             const int li = lin_of(B, g);
             const GemvLin& L = B.lin[li];
             const int64_t N = L.N, nb = L.K / kBlock;
@@ -647,6 +765,7 @@ template <int MT>
 cudaError_t launch_mt(const GemvBatch& b, const GemvPlan& P, uint32_t* status, cudaStream_t s) {
     if constexpr (MT <= 2) {
         if (P.tr == 32) return launch_one<MT, 4>(b, P, status, s);
+        if (P.tr == 24) return launch_one<MT, 3>(b, P, status, s);
         if (P.tr == 16) return launch_one<MT, 2>(b, P, status, s);
     }
     return launch_one<MT, 1>(b, P, status, s);
@@ -677,19 +796,38 @@ bool plan_batch(const GemvArgs* a, int count, int num_sms, GemvBatch* b, GemvPla
 
 }  // namespace
 
-bool gemv_supported(int64_t M, int64_t K) {
+namespace {
+// Both answers for one (M, K), remembered: the API asks them for every entry of every call.
+// One word per slot -- valid bit, M, K / 64, the two answers -- so readers need no lock.
+constexpr int kFitSlots = 256;
+std::atomic<uint64_t> g_fit[kFitSlots];
+
+uint64_t fits_uncached(int64_t M, int64_t K) {
     const GemvArgs a = shape_only(M, K);
     GemvBatch b{};
     GemvPlan P;
-    return M >= 1 && M <= kGemvMaxM && K >= kBlock && make_plan(&a, 1, false, 1, &b, &P);
+    const bool sup = M >= 1 && M <= kGemvMaxM && K >= kBlock && make_plan(&a, 1, false, 1, &b, &P);
+    const bool quant = sup && M * K <= kGemvFuseElems && make_plan(&a, 1, true, 1, &b, &P);
+    return (sup ? 1u : 0u) | (quant ? 2u : 0u);
 }
 
-bool gemv_quantizes(int64_t M, int64_t K) {
-    const GemvArgs a = shape_only(M, K);
-    GemvBatch b{};
-    GemvPlan P;
-    return M * K <= kGemvFuseElems && gemv_supported(M, K) && make_plan(&a, 1, true, 1, &b, &P);
+// bit 0: the few-token kernel takes (M, K); bit 1: it also quantizes such rows itself
+uint64_t fits(int64_t M, int64_t K) {
+    if (M < 1 || M > kGemvMaxM || K < kBlock || K % kBlock != 0 || K / kBlock >= (int64_t(1) << 40))
+        return fits_uncached(M, K);
+    const uint64_t tag = (uint64_t(1) << 63) | static_cast<uint64_t>(M) << 48 | static_cast<uint64_t>(K / kBlock) << 2;
+    std::atomic<uint64_t>& slot = g_fit[(static_cast<uint64_t>(K / kBlock) * 8 + static_cast<uint64_t>(M)) % kFitSlots];
+    const uint64_t v = slot.load(std::memory_order_relaxed);
+    if ((v & ~uint64_t(3)) == tag) return v & 3;
+    const uint64_t r = fits_uncached(M, K);
+    slot.store(tag | r, std::memory_order_relaxed);
+    return r;
 }
+}  // namespace
+
+bool gemv_supported(int64_t M, int64_t K) { return (fits(M, K) & 1) != 0; }
+
+bool gemv_quantizes(int64_t M, int64_t K) { return (fits(M, K) & 2) != 0; }
 
 bool gemv_batch_fits(const GemvArgs* a, int count) {
     GemvBatch b{};
