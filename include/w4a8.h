@@ -86,7 +86,9 @@ int w4a8_quant_pack(const float *x, int64_t M, int64_t K,
  * count: in block order, or,
  * for linears with few 128-token output tiles and K of at least 2048, as the sum of the two
  * halves of K (two CTAs share the tile).  Every tensor-core entry point takes the same order
- * for the same shape.
+ * for the same shape.  The contraction runs tiles of 256 tokens from M = 4096 on, and below
+ * that where tiles of 128 would take more waves of the SMs and no K split; both kernels sum
+ * in block order, so the tile width changes no output.
  * workspace: at least w4a8_linear_workspace_bytes(M, N, K) bytes (the activation
  * operand re-encoded for the tensor cores).  In the few-token form that size is 0 and
  * `workspace` may be NULL. */
@@ -262,9 +264,9 @@ size_t w4a8_debug_workspace_bytes(int64_t m_cnt, int64_t n_cnt, int64_t K);
 
 /* Debug: the exact per-block int32 accumulators acc[m][n][b] (section 3 eq. (2), first
  * sum) for the window m0 <= m < m0 + m_cnt, n0 <= n < n0 + n_cnt, computed by the
- * tensor-core contraction that w4a8_linear runs for a problem of M tokens: the 256-token
- * kernel (token records 256 wide, N = 256 MMAs) when M >= 4096, the 128-token kernel
- * otherwise.  For M <= W4A8_DECODE_MAX_M w4a8_linear forms its block products on the CUDA
+ * tensor-core contraction that w4a8_linear runs for this problem (M, N, K) on the current
+ * device: the 256-token kernel (token records 256 wide, N = 256 MMAs) where w4a8_linear takes
+ * it (always from M = 4096 on), the 128-token kernel otherwise.  For M <= W4A8_DECODE_MAX_M w4a8_linear forms its block products on the CUDA
  * cores instead; this call still runs the 128-token tensor-core contraction there.
  * acc: int32 [m_cnt][n_cnt][K/64], indexed by the position inside the window.  The window
  * must lie inside [0, M) x [0, N) and be non-empty.  workspace: at least

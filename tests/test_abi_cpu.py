@@ -199,9 +199,10 @@ def test_host_call_workspace_and_chunking(lib):
     call's scratch (one chunk) or the prepared weights and one prepared-activation buffer per
     compute stream (at most four), sized for the largest chunk.  A call is cut into at most
     sixteen chunks of whole token tiles, each moving at least 8 MiB of x and y; the tiles are
-    spread evenly, so the first (tiles mod chunks) chunks take one tile more than the rest."""
-    def plan(M, N, K):
-        tw = 256 if M >= 4096 else 128
+    spread evenly, so the first (tiles mod chunks) chunks take one tile more than the rest.
+    Below 4096 rows the call may take tiles of 128 or 256 tokens (by the device's SM count), so
+    the size covers the larger of the two plans."""
+    def plan(M, N, K, tw):
         chunks = 1 if M <= 8 else max(1, min(16, M // tw, M * (K + N) * 4 // (8 << 20)))
         tiles = -(-M // tw)
         largest = min((tiles // chunks + (tiles % chunks > 0)) * tw, M)
@@ -210,7 +211,16 @@ def test_host_call_workspace_and_chunking(lib):
     def base(M, N, K):
         return _align(_align(M * K * 4) + M * N * 4)
 
-    cases = [  # (M, N, K, chunks, rows of the largest chunk)
+    def act_bytes(rows, K, tw):  # token records of width tw, then the row scales
+        return _align(-(-rows // tw) * (K // 64) * 144 * tw) + _align(rows * 4)
+
+    def want(M, N, K, tw):
+        chunks, last = plan(M, N, K, tw)
+        if chunks == 1:
+            return base(M, N, K) + lib.w4a8_prefill_workspace_bytes(M, N, K)
+        return base(M, N, K) + lib.w4a8_prepared_weights_bytes(N, K) + min(chunks, 4) * act_bytes(last, K, tw)
+
+    cases = [  # (M, N, K, chunks, rows of the largest chunk) with 128-token tiles
         (512, 3072, 1024, 1, 512),        # the pp512 linear: 8 MiB in all, one chunk
         (700, 200, 256, 1, 700),
         (3, 256, 1024, 1, 3),
@@ -220,21 +230,17 @@ def test_host_call_workspace_and_chunking(lib):
         (2048, 4096, 2048, 6, 384),       # 16 tiles: 3 3 3 3 2 2
     ]
     for M, N, K, chunks, last in cases:
-        assert plan(M, N, K) == (chunks, last), (M, N, K)
+        assert plan(M, N, K, 128) == (chunks, last), (M, N, K)
+        assert act_bytes(last, K, 128) == lib.w4a8_prepared_activations_bytes(last, K)
         got = lib.w4a8_prefill_host_workspace_bytes(M, N, K)
-        if chunks == 1:
-            want = base(M, N, K) + lib.w4a8_prefill_workspace_bytes(M, N, K)
-        else:
-            want = base(M, N, K) + lib.w4a8_prepared_weights_bytes(N, K) + \
-                min(chunks, 4) * lib.w4a8_prepared_activations_bytes(last, K)
-        assert got == want, (M, N, K)
+        assert got == max(want(M, N, K, 128), want(M, N, K, 256)), (M, N, K)
     # 256-token records: chunks of whole 256-row tiles, below 4096 rows each
-    assert plan(8192, 14336, 4096)[0] == 16 and plan(16384, 1024, 1024) == (16, 1024)
+    assert plan(8192, 14336, 4096, 256)[0] == 16 and plan(16384, 1024, 1024, 256) == (16, 1024)
     for M, N, K in ((8192, 14336, 4096), (8300, 512, 256), (9000, 1536, 512), (16384, 1024, 1024)):
-        chunks, last = plan(M, N, K)
+        chunks, last = plan(M, N, K, 256)
         assert chunks > 1 and last < 4096
         got = lib.w4a8_prefill_host_workspace_bytes(M, N, K)
-        assert got >= base(M, N, K) + lib.w4a8_prepared_weights_bytes(N, K) + min(chunks, 4) * (last * K * 2)
+        assert got >= want(M, N, K, 256)
     assert lib.w4a8_prefill_host_workspace_bytes(0, 64, 128) == 0
     assert lib.w4a8_prefill_host_workspace_bytes(4, 64, 100) == ctypes.c_size_t(-1).value
 

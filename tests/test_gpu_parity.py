@@ -359,6 +359,36 @@ def test_split_calls_equal_fused():
         check_y(y_split, y_ref, bound, f"split N={N}")
 
 
+@pytest.mark.parametrize("M,K,N", [(512, 2048, 6144), (640, 1024, 4096), (1000, 256, 20480)])
+def test_wide_tiles_below_4096_tokens(M, K, N):
+    """Shapes whose 128-token tiles would take more waves of the 152 SMs (192, 160 and 1280
+    tiles) run the one-call entry points on 256-token tiles (96, 96 and 640 tiles; 640 and 1000
+    rows leave a half and a ragged last tile).  The prepared-operand calls keep 128-token records:
+    without the K split both kernels sum every output in block order, so all of them agree bit
+    for bit, and the per-block accumulators (the 256-token kernel's) are exact."""
+    b = B()
+    d = synth.random_small(M, K, N, seed=M + N, bias=True)
+    g = inputs_to_dev(d)
+    y_fused = b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"])
+    act = b.prepare_activations(g["x"])
+    pw = b.prepare_weights(g["wq"], g["s_w"], g["z_w"])
+    assert torch.equal(b.linear_prepared(act, pw, M, N, K, bias=g["bias"]), y_fused)
+    a_q, s_a, rs = b.quant_pack(g["x"])
+    assert torch.equal(b.linear(a_q, s_a, rs, g["wq"], g["s_w"], g["z_w"], g["bias"]), y_fused)
+    yh = b.prefill_linear_host(_pinned(d["x"]), g["wq"], g["s_w"], g["z_w"], g["bias"])
+    torch.cuda.synchronize()
+    assert torch.equal(yh, y_fused.cpu())
+    rows = np.unique(np.linspace(0, M - 1, 48).astype(np.int64))
+    y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"], rows=rows)
+    check_y(y_fused[torch.from_numpy(rows).to(dev())], y_ref, bound, f"wide tiles {M}x{K}->{N}")
+    a_np = a_q.cpu().numpy()
+    for m0, mc, n0, nc in ((0, 300, 0, 200), (M - 140, 140, N - 130, 130)):
+        got = b.debug_block_acc(a_q, g["wq"], N, m0, mc, n0, nc).cpu().numpy()
+        ref = oracle.block_acc(a_np, d["wq"], N, m0, mc, n0, nc)
+        assert np.array_equal(got, ref), f"{int((got != ref).sum())} accumulators differ"
+    assert b.sync_status() == 0
+
+
 @pytest.mark.parametrize("M,K,N", [(9, 64, 1), (300, 1024, 513), (512, 1088, 3072), (129, 6144, 130),
                                    (4100, 512, 300)])
 def test_linear_act_equals_fused(M, K, N):

@@ -79,13 +79,31 @@ struct CallLayout {
     size_t w_off = 0, total = 0;
 };
 
-CallLayout call_layout(int64_t M, int64_t N, int64_t K, bool with_sa) {
+CallLayout call_layout(int64_t M, int64_t N, int64_t K, bool with_sa, int tw) {
     CallLayout c;
-    c.act = act_layout(M, K, with_sa, token_tile(M));
+    c.act = act_layout(M, K, with_sa, tw);
     c.w = w_layout(N, K);
     c.w_off = c.act.total;
     c.total = c.w_off + c.w.total;
     return c;
+}
+
+// The token-record width (and so the contraction kernel) of the one-call entry points
+// (w4a8_prefill_linear, w4a8_linear, the host-buffer call, the debug call) for a problem of this
+// shape: 256 from 4096 tokens on; below that, 256 where 128-token tiles would take more waves of
+// the SMs and run without the K split.  Per token the 256-token kernel takes about 4/5 of the
+// 128-token kernel's time (measured at 8192 tokens), so a wave of it counts as 1.6 of a
+// 128-token wave.  Measured on 512 tokens, K 2048 -> N 6144 (192 tiles of 128 tokens, 96 of
+// 256): the contraction alone 34.1 -> 26.6 us.  Without the K split both kernels sum every
+// output in the same order, so the width changes no output: the prepared-operand entry points,
+// which keep token_tile(M), give the same results bit for bit.
+int call_tile(int64_t M, int64_t N, int64_t K, int num_sms) {
+    if (token_tile(M) != kTileT) return token_tile(M);
+    if (num_sms < 1 || gemm_ksplit(M, N, K, kTileT, num_sms) > 1) return kTileT;
+    const int64_t tn = (N + kTileW - 1) / kTileW;
+    const int64_t w128 = ((M + 127) / 128 * tn + num_sms - 1) / num_sms;
+    const int64_t w256 = ((M + 255) / 256 * tn + num_sms - 1) / num_sms;
+    return w256 * 256 * 4 < w128 * 128 * 5 ? 256 : kTileT;
 }
 
 // GEMM + epilogue from prepared activations (token records `tw` tokens wide) and prepared
@@ -154,12 +172,15 @@ void set_weight_job(PrepArgs* p, const uint8_t* wq, const uint16_t* w_scale, con
 // else the pre-pass outputs; the tensor-core form needs the re-encoded activations and the
 // prepared weights.
 bool few_tokens(int64_t M, int64_t K) { return M <= kGemvMaxM && gemv_supported(M, K); }
-size_t linear_ws(int64_t M, int64_t N, int64_t K) {
-    return few_tokens(M, K) ? 0 : call_layout(M, N, K, false).total;
+// (The tensor-core form's size covers either token-record width, so it does not depend on the
+// device.)
+size_t call_ws(int64_t M, int64_t N, int64_t K, bool with_sa) {
+    return std::max(call_layout(M, N, K, with_sa, kTileT).total, call_layout(M, N, K, with_sa, 256).total);
 }
+size_t linear_ws(int64_t M, int64_t N, int64_t K) { return few_tokens(M, K) ? 0 : call_ws(M, N, K, false); }
 size_t prefill_ws(int64_t M, int64_t N, int64_t K) {
     if (few_tokens(M, K)) return gemv_quantizes(M, K) ? 0 : decode_layout(M, K).total;
-    return call_layout(M, N, K, true).total;
+    return call_ws(M, N, K, true);
 }
 
 // The few-token kernel from x (it quantizes) or from the pre-pass outputs.
@@ -326,10 +347,10 @@ int linear_impl(const int8_t* a_q, const float* a_scale, const int32_t* rowsum, 
         if ((rc = current_device(&d)) != W4A8_OK) return rc;
         return run_gemv(nullptr, a_q, a_scale, rowsum, wq, w_scale, w_zero, bias, out, M, N, K, *d, st);
     }
-    const CallLayout L = call_layout(M, N, K, false);
-    if (!workspace || workspace_bytes < L.total) return W4A8_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < linear_ws(M, N, K)) return W4A8_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return W4A8_ERR_ALIGN;
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
+    const CallLayout L = call_layout(M, N, K, false, call_tile(M, N, K, d->num_sms));
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     PrepArgs p;
     p.a_q_in = a_q;
@@ -390,7 +411,7 @@ int prefill_impl(const float* x, const uint8_t* wq, const uint16_t* w_scale, con
         return run_gemv(nullptr, p.a_q_out, p.s_a_out, p.rs_out, wq, w_scale, w_zero, bias, out, M, N, K, *d, st,
                         true);
     }
-    const CallLayout L = call_layout(M, N, K, true);
+    const CallLayout L = call_layout(M, N, K, true, call_tile(M, N, K, d->num_sms));
     float* s_a = reinterpret_cast<float*>(ws + L.act.s_a);
     PrepArgs p;
     p.x = x;
@@ -610,13 +631,13 @@ int w4a8_debug_block_acc(const int8_t* a_q, const uint8_t* wq, int64_t M, int64_
     if (!a_q || !wq || !acc) return W4A8_ERR_ARG;
     if (m0 < 0 || n0 < 0 || m_cnt <= 0 || n_cnt <= 0 || m0 + m_cnt > M || n0 + n_cnt > N) return W4A8_ERR_SHAPE;
     if (!aligned(a_q, 16) || !aligned(wq, 16) || !aligned(acc, 4)) return W4A8_ERR_ALIGN;
-    // the token-record width (and so the contraction kernel) that a linear of M tokens runs
-    const ActLayout L = act_layout(m_cnt, K, false, token_tile(M));
+    DeviceInfo* d = nullptr;
+    if ((rc = current_device(&d)) != W4A8_OK) return rc;
+    // the token-record width (and so the contraction kernel) that w4a8_linear runs for this problem
+    const ActLayout L = act_layout(m_cnt, K, false, call_tile(M, N, K, d->num_sms));
     const WLayout W = w_layout(n_cnt, K);
     if (!workspace || workspace_bytes < w4a8_debug_workspace_bytes(m_cnt, n_cnt, K)) return W4A8_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return W4A8_ERR_ALIGN;
-    DeviceInfo* d = nullptr;
-    if ((rc = current_device(&d)) != W4A8_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     uint8_t* wrec = ws + L.total;
@@ -753,9 +774,9 @@ struct HostPlan {
     }
 };
 
-HostPlan host_plan(int64_t M, int64_t N, int64_t K) {
+HostPlan host_plan(int64_t M, int64_t N, int64_t K, int tw) {
     HostPlan h;
-    h.tw = token_tile(M);
+    h.tw = tw;
     h.M = M;
     if (!few_tokens(M, K)) {
         const int64_t by_rows = M / h.tw;
@@ -843,7 +864,8 @@ extern "C" {
 size_t w4a8_prefill_host_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (check_shape(M, N, K) != W4A8_OK) return static_cast<size_t>(-1);
     if (M == 0 || N == 0) return 0;
-    return host_plan(M, N, K).total;
+    // either token-record width (the call picks one by the device's SM count)
+    return std::max(host_plan(M, N, K, kTileT).total, host_plan(M, N, K, 256).total);
 }
 
 int w4a8_prefill_linear_host(const float* x_host, const uint8_t* wq, const uint16_t* w_scale,
@@ -856,10 +878,10 @@ int w4a8_prefill_linear_host(const float* x_host, const uint8_t* wq, const uint1
     if (!aligned(wq, 16) || !aligned(w_scale, 2) || !aligned(w_zero, 2) || (bias && !aligned(bias, 4)) ||
         !aligned(workspace, 16))
         return W4A8_ERR_ALIGN;
-    const HostPlan h = host_plan(M, N, K);
-    if (workspace_bytes < h.total) return W4A8_ERR_WORKSPACE;
+    if (workspace_bytes < w4a8_prefill_host_workspace_bytes(M, N, K)) return W4A8_ERR_WORKSPACE;
     DeviceInfo* d = nullptr;
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
+    const HostPlan h = host_plan(M, N, K, call_tile(M, N, K, d->num_sms));
     const HostBuf xb = host_buffer(x_host), yb = host_buffer(y_host);
     if (!xb.locked || !yb.locked) return W4A8_ERR_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
