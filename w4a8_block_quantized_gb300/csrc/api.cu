@@ -89,8 +89,8 @@ CallLayout call_layout(int64_t M, int64_t N, int64_t K, bool with_sa, int tw) {
 }
 
 // The token-record width (and so the contraction kernel) of the one-call entry points
-// (w4a8_prefill_linear, w4a8_linear, the host-buffer call, the debug call) for a problem of this
-// shape: 256 from 4096 tokens on; below that, 256 where 128-token tiles would take more waves of
+// (w4a8_prefill_linear, also as a one-chunk host-buffer call; w4a8_linear; the debug call) for
+// a problem of this shape: 256 from 4096 tokens on; below that, 256 where 128-token tiles would take more waves of
 // the SMs and run without the K split.  Per token the 256-token kernel takes about 4/5 of the
 // 128-token kernel's time (measured at 8192 tokens), so a wave of it counts as 1.6 of a
 // 128-token wave.  Measured on 512 tokens, K 2048 -> N 6144 (192 tiles of 128 tokens, 96 of
@@ -864,8 +864,7 @@ extern "C" {
 size_t w4a8_prefill_host_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (check_shape(M, N, K) != W4A8_OK) return static_cast<size_t>(-1);
     if (M == 0 || N == 0) return 0;
-    // either token-record width (the call picks one by the device's SM count)
-    return std::max(host_plan(M, N, K, kTileT).total, host_plan(M, N, K, 256).total);
+    return host_plan(M, N, K, token_tile(M)).total;
 }
 
 int w4a8_prefill_linear_host(const float* x_host, const uint8_t* wq, const uint16_t* w_scale,
@@ -878,10 +877,14 @@ int w4a8_prefill_linear_host(const float* x_host, const uint8_t* wq, const uint1
     if (!aligned(wq, 16) || !aligned(w_scale, 2) || !aligned(w_zero, 2) || (bias && !aligned(bias, 4)) ||
         !aligned(workspace, 16))
         return W4A8_ERR_ALIGN;
-    if (workspace_bytes < w4a8_prefill_host_workspace_bytes(M, N, K)) return W4A8_ERR_WORKSPACE;
+    // Row chunks keep the 128-token width below 4096 rows: a chunk has a fraction of the call's
+    // tiles, so it would not fill the SMs with 256-token ones (measured: two chunks of 256 rows,
+    // K 2048 -> N 6144, lost 8% end to end).  A one-chunk call is the fused call, which picks
+    // its own width; either way the outputs are the same (call_tile).
+    const HostPlan h = host_plan(M, N, K, token_tile(M));
+    if (workspace_bytes < h.total) return W4A8_ERR_WORKSPACE;
     DeviceInfo* d = nullptr;
     if ((rc = current_device(&d)) != W4A8_OK) return rc;
-    const HostPlan h = host_plan(M, N, K, call_tile(M, N, K, d->num_sms));
     const HostBuf xb = host_buffer(x_host), yb = host_buffer(y_host);
     if (!xb.locked || !yb.locked) return W4A8_ERR_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
