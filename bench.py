@@ -272,13 +272,27 @@ def run_bench(args):
     batch = binding.Batch([dict(x=t["x"], wq=t["wq"], s_w=t["s_w"], z_w=t["z_w"], bias=t["bias"], y=t["y"],
                                 ws=t["ws"]) for t in lin], stream) if decode else None
 
-    def step():
+    def step_on(s):
         if batch is not None:
-            batch.run(stream)
+            batch.run(s)
             return
         for t in lin:
             binding.prefill_linear(t["x"], t["wq"], t["s_w"], t["z_w"], t["bias"], y=t["y"], ws=t["ws"],
-                                   stream=stream)
+                                   stream=s)
+
+    def step():
+        step_on(stream)
+
+    # the kernels one step launches, counted from a command tape of one step (its kernel nodes)
+    side = torch.cuda.Stream(device=device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step_on(side)                    # one ordinary step before recording
+        with binding.Tape(side) as tape:
+            step_on(side)
+    side.synchronize()
+    kernels_per_step = tape.kernels()
+    tape.free()
 
     # The clock sampler starts before the warm-up so that nvidia-smi's own start-up (which
     # can stall a fresh box for seconds) never falls inside the timed region.
@@ -549,7 +563,8 @@ def run_bench(args):
                 "bound": e2e_bound,
                 "copies_then_call": {"value": round(e2e_value * e2e_s / e2e_serial_s, 3 if not decode else 1),
                                      "ms_per_step": round(e2e_serial_s * 1e3 / e2e_steps, 4)}},
-        "gpu_launches": args.steps * (1 if one_launch else 2) * len(lin),
+        "gpu_launches": args.steps * kernels_per_step,
+        "gpu_launches_per_step": kernels_per_step,
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
@@ -699,6 +714,7 @@ def layer_step(lin, specs, stream, flush, reps, decode):
             for c in calls:
                 c(side)
     side.synchronize()
+    launches = tape.kernels()
 
     def timed(run):
         ms = []
@@ -722,10 +738,10 @@ def layer_step(lin, specs, stream, flush, reps, decode):
     tape.free()
     ops = sum(s.ops for s in specs)
     return {"mode": ("q/k/v and gate/up as row-concatenated groups on shared inputs (4 linears); " +
-                     ("one batch call: a few-token launch per group, each after the first streaming its "
-                      "weights while the previous one runs" if decode else
+                     ("one batch call (the four groups in one few-token launch where they fit one, "
+                      "else a launch each)" if decode else
                       "weights prepared at load, per group one pre-pass + one contraction")),
-            "launches_per_step": len(group_entries) if decode else len(calls),
+            "launches_per_step": launches,
             "ms_per_step_eager": round(t_eager, 5), "ms_per_step_tape": round(t_tape, 5),
             "tok_s_tape": round(M / (t_tape * 1e-3), 1), "tops_tape": round(ops / (t_tape * 1e-3) / 1e12, 3),
             "l2": "flushed before every step (outside the events)"}

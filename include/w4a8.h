@@ -292,6 +292,9 @@ int w4a8_tape_begin(void *stream);
 int w4a8_tape_end(void *stream, w4a8_tape **tape);
 int w4a8_tape_replay(const w4a8_tape *tape, void *stream);
 void w4a8_tape_free(w4a8_tape *tape);
+/* The number of kernel launches one replay of the tape makes (the kernel nodes of its graph;
+ * copies, event records and waits are not counted); -1 for a NULL tape. */
+int64_t w4a8_tape_kernels(const w4a8_tape *tape);
 
 /* Synchronizes `stream`, then returns and clears the current device's status word:
  * W4A8_OK, W4A8_ERR_TIMEOUT if a kernel gave up on a wait since the last call, or

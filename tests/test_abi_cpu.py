@@ -131,6 +131,7 @@ def test_tape_arguments_rejected(lib):
     assert lib.w4a8_tape_end(ctypes.c_void_p(1 << 20), None) == b.W4A8_ERR_ARG
     assert lib.w4a8_tape_replay(None, None) == b.W4A8_ERR_ARG
     lib.w4a8_tape_free(None)                                      # a no-op
+    assert lib.w4a8_tape_kernels(None) == -1
 
 
 def test_deep_few_token_rows_take_the_tensor_core_form(lib):

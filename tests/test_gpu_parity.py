@@ -806,6 +806,41 @@ def test_host_call_reuses_a_workspace_in_stream_order():
     assert b.sync_status() == 0
 
 
+def test_tape_counts_its_kernels():
+    """w4a8_tape_kernels: the kernel launches one replay makes -- a fused call (pre-pass and
+    contraction), a quantizing few-token call (one kernel), a decoder layer's four few-token
+    groups in one batch call (one launch), and the 7B-class pair as a batch (a launch each)."""
+    b = B()
+    s = torch.cuda.Stream()
+
+    def count(fn):
+        with torch.cuda.stream(s):
+            fn()                      # one ordinary call before recording
+            with b.Tape(s) as t:
+                fn()
+        s.synchronize()
+        n = t.kernels()
+        t.free()
+        return n
+
+    def ents(M, shapes, seed):
+        out = []
+        for i, (K, N) in enumerate(shapes):
+            g = inputs_to_dev(synth.random_small(M, K, N, seed=seed + i, bias=True))
+            out.append(dict(x=g["x"], wq=g["wq"], s_w=g["s_w"], z_w=g["z_w"], bias=g["bias"]))
+        return out
+
+    g = ents(300, [(1024, 640)], 80)[0]
+    assert count(lambda: b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"], stream=s)) == 2
+    g = ents(1, [(1024, 640)], 81)[0]
+    assert count(lambda: b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"], stream=s)) == 1
+    layer = b.Batch(ents(1, [(2048, 4096), (2048, 2048), (2048, 12288), (6144, 2048)], 82), s)
+    assert count(lambda: layer.run(s)) == 1
+    pair = b.Batch(ents(1, [(4096, 14336), (14336, 4096)], 86), s)
+    assert count(lambda: pair.run(s)) == 2
+    assert b.sync_status() == 0
+
+
 def test_tape_records_the_host_call():
     """Host-buffer calls recorded into a tape -- one cut into chunks (its side streams joined
     back into the capture), one small enough to work on the mapped host buffers in place --

@@ -62,6 +62,7 @@ SIGNATURES = {
     "w4a8_tape_end": (ctypes.c_int, [_P, ctypes.POINTER(_P)]),
     "w4a8_tape_replay": (ctypes.c_int, [_P, _P]),
     "w4a8_tape_free": (None, [_P]),
+    "w4a8_tape_kernels": (ctypes.c_int64, [_P]),
     "w4a8_sync_status": (ctypes.c_int, [_P]),
     "w4a8_selftest_wait_timeout": (ctypes.c_int, [_I64, _P]),
     "w4a8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -548,6 +549,12 @@ class Tape:
         if self.handle is None:
             raise RuntimeError("tape not recorded")
         _check(load().w4a8_tape_replay(self.handle, _stream(stream)), "w4a8_tape_replay")
+
+    def kernels(self) -> int:
+        """Kernel launches per replay (w4a8_tape_kernels)."""
+        if self.handle is None:
+            raise RuntimeError("tape not recorded")
+        return int(load().w4a8_tape_kernels(self.handle))
 
     def free(self):
         if self.handle is not None:

@@ -15,6 +15,7 @@
 
 struct w4a8_tape {
     cudaGraphExec_t exec = nullptr;
+    int64_t kernels = 0;  // kernel nodes of the recorded graph: launches per replay
 };
 
 extern "C" {
@@ -36,6 +37,31 @@ int w4a8_tape_end(void* stream, w4a8_tape** out) {
     cudaGraph_t graph = nullptr;
     if (cudaStreamEndCapture(static_cast<cudaStream_t>(stream), &graph) != cudaSuccess || !graph)
         return W4A8_ERR_CUDA;
+    // count the kernel nodes (the other nodes are event records and waits of the side streams)
+    int64_t kernels = 0;
+    size_t n = 0;
+    if (cudaGraphGetNodes(graph, nullptr, &n) != cudaSuccess) {
+        cudaGraphDestroy(graph);
+        return W4A8_ERR_CUDA;
+    }
+    if (n > 0) {
+        cudaGraphNode_t* nodes = new (std::nothrow) cudaGraphNode_t[n];
+        if (!nodes) {
+            cudaGraphDestroy(graph);
+            return W4A8_ERR_ARG;
+        }
+        bool ok = cudaGraphGetNodes(graph, nodes, &n) == cudaSuccess;
+        for (size_t i = 0; ok && i < n; ++i) {
+            cudaGraphNodeType t;
+            ok = cudaGraphNodeGetType(nodes[i], &t) == cudaSuccess;
+            if (ok && t == cudaGraphNodeTypeKernel) ++kernels;
+        }
+        delete[] nodes;
+        if (!ok) {
+            cudaGraphDestroy(graph);
+            return W4A8_ERR_CUDA;
+        }
+    }
     cudaGraphExec_t exec = nullptr;
     const cudaError_t e = cudaGraphInstantiate(&exec, graph, 0);
     cudaGraphDestroy(graph);
@@ -46,6 +72,7 @@ int w4a8_tape_end(void* stream, w4a8_tape** out) {
         return W4A8_ERR_ARG;
     }
     t->exec = exec;
+    t->kernels = kernels;
     *out = t;
     return W4A8_OK;
 }
@@ -54,6 +81,8 @@ int w4a8_tape_replay(const w4a8_tape* tape, void* stream) {
     if (!tape || !tape->exec) return W4A8_ERR_ARG;
     return cudaGraphLaunch(tape->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
 }
+
+int64_t w4a8_tape_kernels(const w4a8_tape* tape) { return tape ? tape->kernels : -1; }
 
 void w4a8_tape_free(w4a8_tape* tape) {
     if (!tape) return;
