@@ -190,8 +190,11 @@ def _run_both(d):
 @pytest.mark.parametrize("M,K,N,bias", [(1, 64, 1, False), (1, 64, 16, True), (7, 128, 33, True),
                                         (128, 1024, 256, False), (129, 192, 257, True), (255, 1024, 130, True),
                                         (300, 2048, 513, False), (64, 64, 4000, True), (513, 4096, 64, False),
-                                        (17, 16384, 100, True), (9, 20480, 70, False)])
+                                        (17, 16384, 100, True), (9, 20480, 70, False), (256, 1024, 3000, True)])
 def test_linear_small_shapes(M, K, N, bias):
+    """The fused call against the oracle and against w4a8_quant_pack + w4a8_linear.  Rows of
+    1024 or less take four, two or one warps per row in the pre-pass, whichever keeps its launch
+    in one wave: (128, 1024) four, (256, 1024, 3000) two (its weight job takes 192 CTAs)."""
     d = synth.random_small(M, K, N, seed=M + K + N, bias=bias)
     y_fused, y_sep = _run_both(d)
     y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])

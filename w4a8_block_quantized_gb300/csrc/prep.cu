@@ -408,9 +408,23 @@ cudaError_t run_quant(const PrepArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// The row CTAs run_quant launches for G warps per row (8-warp CTAs).
+int64_t quant_row_ctas(int64_t M, int G) {
+    const int64_t rpc = 8 / G, need = (M + rpc - 1) / rpc, cap = 152 * 2;
+    const int64_t iters = (need + cap - 1) / cap;
+    return iters > 0 ? (need + iters - 1) / iters : 1;
+}
+
 template <bool PLANES>
 cudaError_t dispatch_quant(const PrepArgs& a, cudaStream_t s) {
     const int64_t n4 = a.K / 4;
+    // Short rows: more warps per row (shorter chains per lane, more SMs) while the whole launch,
+    // the weight job's CTAs included, still fits one wave of two 256-thread CTAs per SM.
+    // Measured at 128 and 512 rows of 1024: the pre-pass alone 8.2 -> 6.1 us with four warps per
+    // row; the fused call's launch (with its weight job) keeps one warp per row at 512 rows,
+    // where four would have spilled into a second wave and cost 0.8 us.
+    if (n4 <= 128 * 2 && quant_row_ctas(a.M, 4) + weight_ctas(a) <= 152 * 2) return run_quant<4, 2, PLANES>(a, s);
+    if (n4 <= 64 * 4 && quant_row_ctas(a.M, 2) + weight_ctas(a) <= 152 * 2) return run_quant<2, 4, PLANES>(a, s);
     // smallest warp group G whose lanes hold the row in at most 8 float4 each (so the next
     // row can be prefetched): 1-8 warps of a 256-thread CTA, then the 16 warps of a 512-thread
     // CTA; past that, the two-pass kernel
