@@ -121,6 +121,22 @@ __device__ __forceinline__ void tile_at32(int64_t t, int64_t tiles_t, int64_t ti
     tw = q;
 }
 
+// y[c] = fma(s, v[c], y[c]) for c < C, two columns per instruction (fma.rn.f32x2: the same
+// single-rounding fp32 fma per element as fmaf, so the sums are unchanged bit for bit).
+template <int C>
+__device__ __forceinline__ void fma_cols(float* y, float s, const uint32_t* v) {
+    uint64_t ss;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(s));
+#pragma unroll
+    for (int c = 0; c < C; c += 2) {
+        uint64_t yy, vv;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(yy) : "f"(y[c]), "f"(y[c + 1]));
+        asm("mov.b64 %0, {%1, %2};" : "=l"(vv) : "r"(v[c]), "r"(v[c + 1]));
+        asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(yy) : "l"(ss), "l"(vv));
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(y[c]), "=f"(y[c + 1]) : "l"(yy));
+    }
+}
+
 // Bounded wait that ignores the abort flag: used while unwinding to let copies and MMAs
 // already in flight land before the CTA's shared memory and TMEM are released.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -363,11 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 } else {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) y[c] = fmaf(s0, __uint_as_float(v[c]), y[c]);
+                    fma_cols<32>(y, s0, v);
                     if (two) {
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) y[c] = fmaf(s1, __uint_as_float(v[32 + c]), y[c]);
+                        fma_cols<32>(y, s1, v + 32);
                     }
                 }
             }
@@ -613,8 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
                 if (DEBUG) {
                     store_acc(v, 0, b);
                 } else {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) y[c] = fmaf(sb, __uint_as_float(v[c]), y[c]);
+                    fma_cols<32>(y, sb, v);
                 }
                 tmem_ld_32x32b_x16(tb + 32, v);
                 tmem_ld_32x32b_x16(tb + 48, v + 16);
@@ -627,8 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_wide_kernel(const GemmArgs a
                 if (DEBUG) {
                     store_acc(v, 32, b);
                 } else {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) y[32 + c] = fmaf(sb, __uint_as_float(v[c]), y[32 + c]);
+                    fma_cols<32>(y + 32, sb, v);
                 }
             }
             if (!ok) break;
@@ -1042,8 +1054,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_packed_kernel(const __grid_c
                         }
                     } else {
                         const float sb = e == 0 ? s0 : s1;
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) y[c] = fmaf(sb, __uint_as_float(v[c]), y[c]);
+                        fma_cols<32>(y, sb, v);
                     }
                 }
                 // operand stage s is free too (the stage's MMAs are done): the weights of stage
