@@ -63,12 +63,21 @@ __device__ __forceinline__ int plane_off(int r, int j, int p) {
 
 // Section 3 eq. (3) planes of four float codes (exact integers in [-127, 127]): hi word holds
 // e4m3(16 * floor(q / 16)) (the signed high nibble times 16), lo word e4m3(q - that) (the
-// unsigned low nibble), element j in byte j.
+// unsigned low nibble), element j in byte j.  Two elements per mul / sub .rn.f32x2; every
+// product and difference here is exact (q is an integer in [-127, 127]).
 __device__ __forceinline__ void planes4f(float4 q, uint32_t& hi, uint32_t& lo) {
-    const float h0 = 16.0f * floorf(q.x * 0.0625f), h1 = 16.0f * floorf(q.y * 0.0625f);
-    const float h2 = 16.0f * floorf(q.z * 0.0625f), h3 = 16.0f * floorf(q.w * 0.0625f);
+    const uint64_t k16 = pk2(0.0625f, 0.0625f), k1 = pk2(16.0f, 16.0f);
+    float a0, a1, a2, a3;
+    upk2(mul2(pk2(q.x, q.y), k16), a0, a1);
+    upk2(mul2(pk2(q.z, q.w), k16), a2, a3);
+    const uint64_t h01 = mul2(pk2(floorf(a0), floorf(a1)), k1), h23 = mul2(pk2(floorf(a2), floorf(a3)), k1);
+    float h0, h1, h2, h3, l0, l1, l2, l3;
+    upk2(h01, h0, h1);
+    upk2(h23, h2, h3);
+    upk2(sub2(pk2(q.x, q.y), h01), l0, l1);
+    upk2(sub2(pk2(q.z, q.w), h23), l2, l3);
     hi = e4m3x2(h0, h1) | (e4m3x2(h2, h3) << 16);
-    lo = e4m3x2(q.x - h0, q.y - h1) | (e4m3x2(q.z - h2, q.w - h3) << 16);
+    lo = e4m3x2(l0, l1) | (e4m3x2(l2, l3) << 16);
 }
 
 // Four float codes as int8 bytes: adding 1.5 * 2^23 puts the integer, in two's complement,

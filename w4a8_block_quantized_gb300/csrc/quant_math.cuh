@@ -58,16 +58,53 @@ static __device__ __noinline__ float requant(float x, float s) {
 // about 127 * 2^-128) has no finite reciprocal, and deep in the subnormal range so few
 // significant bits that |x/s| can pass 127; such a row (uniform across the warp) takes the
 // recompute for every element: IEEE division, round half away, clamp.
+// Two fp32 lanes per instruction (mul / add / sub .rn.f32x2): each element is rounded exactly
+// as the scalar operation rounds it.
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// rint_flag on two elements at once: t = x * r, q = (t + 1.5 * 2^23) - 1.5 * 2^23, and the
+// near-tie flag from |t - q| (the same roundings, element by element, as rint_flag).
+__device__ __forceinline__ void rint_flag2(float x0, float x1, uint64_t rr, float& q0, float& q1, bool& tie) {
+    const uint64_t kc = pk2(12582912.0f, 12582912.0f);
+    const uint64_t t = mul2(pk2(x0, x1), rr);
+    const uint64_t q = sub2(add2(t, kc), kc);
+    float d0, d1;
+    upk2(sub2(t, q), d0, d1);
+    upk2(q, q0, q1);
+    tie |= fmaxf(fabsf(d0), fabsf(d1)) >= 0.5f - 0x1p-15f;
+}
+
 template <int V>
 __device__ __forceinline__ void quant_lane(const float4 (&x)[V], float4 (&q)[V], float s, float r) {
     const bool tiny = !(r < __int_as_float(0x7f800000));
     bool tie = tiny;
+    const uint64_t rr = pk2(r, r);
 #pragma unroll
     for (int i = 0; i < V; ++i) {
-        q[i].x = rint_flag(x[i].x * r, tie);
-        q[i].y = rint_flag(x[i].y * r, tie);
-        q[i].z = rint_flag(x[i].z * r, tie);
-        q[i].w = rint_flag(x[i].w * r, tie);
+        rint_flag2(x[i].x, x[i].y, rr, q[i].x, q[i].y, tie);
+        rint_flag2(x[i].z, x[i].w, rr, q[i].z, q[i].w, tie);
     }
     if (__any_sync(0xffffffffu, tie)) {
 #pragma unroll
