@@ -181,24 +181,32 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ ncu traffic record
+def sources_sha256(paths):
+    """sha256 over the listed source files' bytes, concatenated in order (the kernel's .cu
+    file and every in-tree header it includes)."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def recorded_traffic(workload: str):
     """DRAM bytes (read + write) per launch of the workload's dominant kernel from the
-    committed ncu launch list, or None when there is none or that kernel's source changed
-    since it was taken."""
-    import hashlib
+    committed ncu capture, or None when there is none or any source file of that kernel (its
+    .cu file or an in-tree header it includes) changed since it was taken."""
     rec = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(rec):
         return None
     with open(rec) as f:
         e = json.load(f).get(workload)
-    if not e:
+    if not e or not e.get("sources"):
         return None
-    src = os.path.join(ROOT, e.get("source", ""))
-    if not os.path.isfile(src):
+    if not all(os.path.isfile(os.path.join(ROOT, p)) for p in e["sources"]):
         return None
-    with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != e.get("sha256"):
-            return None
+    if sources_sha256(e["sources"]) != e.get("sha256"):
+        return None
     return e.get("dram_bytes_per_launch")
 
 

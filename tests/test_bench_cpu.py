@@ -58,3 +58,45 @@ def test_cpu_baseline_object():
     assert one["unit"] == "TOPS" and 0 < one["value"] and "rows" in one["sample"]
     # one thread cannot outrun the whole pool by much (timing noise aside)
     assert one["value"] <= 2 * c["value"]
+
+
+def test_traffic_record_follows_every_source_of_its_kernel(tmp_path, monkeypatch):
+    """The recorded DRAM bytes are reported only while every listed source file (the kernel's
+    .cu file and the headers it includes) is byte-identical to the one captured."""
+    sys.path.insert(0, ROOT)
+    import bench
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "k.cu").write_text("kernel\n")
+    (tmp_path / "h.cuh").write_text("header\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    entry = {"kernel": "k", "sources": ["k.cu", "h.cuh"], "dram_bytes_per_launch": 1234}
+    entry["sha256"] = bench.sources_sha256(entry["sources"])
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"c1": entry}))
+    assert bench.recorded_traffic("c1") == 1234
+    assert bench.recorded_traffic("c2") is None
+    (tmp_path / "h.cuh").write_text("header changed\n")
+    assert bench.recorded_traffic("c1") is None
+    (tmp_path / "h.cuh").write_text("header\n")
+    assert bench.recorded_traffic("c1") == 1234
+    (tmp_path / "h.cuh").unlink()
+    assert bench.recorded_traffic("c1") is None
+
+
+def test_committed_traffic_record_lists_the_included_headers():
+    """Each entry of the committed record lists its kernel's .cu file and every in-tree header
+    that file includes, directly or through another header."""
+    import re
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    for e in rec.values():
+        srcs = e["sources"]
+        todo, seen = [srcs[0]], set()
+        while todo:
+            p = todo.pop()
+            if p in seen:
+                continue
+            seen.add(p)
+            with open(os.path.join(ROOT, p)) as f:
+                for inc in re.findall(r'#include "([^"]+)"', f.read()):
+                    todo.append(os.path.join(os.path.dirname(p), inc))
+        assert seen == set(srcs), (e["kernel"], sorted(seen ^ set(srcs)))
