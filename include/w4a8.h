@@ -113,8 +113,9 @@ int w4a8_prefill_linear(const float *x, const uint8_t *wq, const uint16_t *w_sca
 /* A sequence of fused calls (section 4: a decoder layer's linears) in one library call: the
  * same as w4a8_prefill_linear on each entry in order, on `stream`, bit for bit, with one M
  * for all.  Two ways the library uses what it then knows:
- *   - Few tokens (M <= W4A8_DECODE_MAX_M), 3 to 8 entries whose rows the weight-streaming
- *     kernel quantizes itself (M * K <= 16384) and whose activations fit one CTA together,
+ *   - Few tokens (M <= W4A8_DECODE_MAX_M), 3 to 8 entries (or 2 whose packed weights total at
+ *     most 24 MiB) whose rows the weight-streaming kernel quantizes itself (M * K <= 16384)
+ *     and whose activations fit one CTA together,
  *     with no entry's y overlapping any x or another y: ONE launch walks the row tiles of all
  *     entries as a single weight stream, so the kernel's start-up cost is paid once.  (Used
  *     when each entry's own launch would give every output row one warp, so the sums run in

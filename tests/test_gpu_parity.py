@@ -541,14 +541,16 @@ def test_decode_offset_scale_views(M, K, N):
 
 @pytest.mark.parametrize("M,K_N", [(1, ((2048, 4096), (2048, 2048), (2048, 12288), (6144, 2048))),
                                    (1, ((4096, 14336), (14336, 4096))),
+                                   (1, ((1024, 3072), (3072, 1024))),
+                                   (4, ((2048, 2048), (2048, 2048))),
                                    (2, ((1024, 3072), (2048, 1000), (1088, 257))),
                                    (1, tuple((64 * (i + 1), 100 + 37 * i) for i in range(8))),
                                    (1, tuple((1024, 512) for _ in range(9)))])
 def test_batch_of_independent_linears(M, K_N):
     """Independent entries, which the few-token batch runs in one launch where they fit (a
-    decoder layer's four groups, the 7B-class pair, ragged K / odd N at two tokens, the most
-    entries one launch takes, and one entry more): every output equals the separate call's bit
-    for bit."""
+    decoder layer's four groups, the 7B-class pair, two small pairs, ragged K / odd N at two
+    tokens, the most entries one launch takes, and one entry more): every output equals the
+    separate call's bit for bit."""
     b = B()
     ds = [synth.random_small(M, K, N, seed=300 + 7 * i + K + N, bias=i % 2 == 0) for i, (K, N) in enumerate(K_N)]
     gs = [inputs_to_dev(d) for d in ds]
@@ -588,6 +590,30 @@ def test_batch_equals_separate_calls(M):
     for i, (d, y) in enumerate(zip(ds, ys)):
         y_ref, bound, _, _, _ = oracle.prefill_linear(d["x"], d["wq"], d["s_w"], d["z_w"], d["bias"])
         check_y(y, y_ref, bound, f"batch entry {i} M={M}")
+    assert b.sync_status() == 0
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_batch_pair_reading_its_own_output(M):
+    """Two few-token entries where the second reads the first's y: the pair may not share a
+    launch, and both outputs equal the separate calls in order, bit for bit, and the oracle's
+    within tolerance (the second against the first's device output as its input)."""
+    b = B()
+    d1 = synth.random_small(M, 1024, 3072, seed=410, bias=True)
+    d2 = synth.random_small(M, 3072, 1024, seed=411, bias=False)
+    g1, g2 = inputs_to_dev(d1), inputs_to_dev(d2)
+    y1 = torch.empty((M, 3072), device=dev())
+    ents = [dict(x=g1["x"], wq=g1["wq"], s_w=g1["s_w"], z_w=g1["z_w"], bias=g1["bias"], y=y1),
+            dict(x=y1, wq=g2["wq"], s_w=g2["s_w"], z_w=g2["z_w"], bias=None)]
+    ys = b.prefill_linear_batch(ents)
+    torch.cuda.synchronize()
+    r1 = b.prefill_linear(g1["x"], g1["wq"], g1["s_w"], g1["z_w"], g1["bias"])
+    r2 = b.prefill_linear(r1, g2["wq"], g2["s_w"], g2["z_w"], None)
+    assert torch.equal(ys[0], r1) and torch.equal(ys[1], r2)
+    y_ref, bound, _, _, _ = oracle.prefill_linear(d1["x"], d1["wq"], d1["s_w"], d1["z_w"], d1["bias"])
+    check_y(ys[0], y_ref, bound, f"first of the pair M={M}")
+    y_ref, bound, _, _, _ = oracle.prefill_linear(r1.cpu().numpy(), d2["wq"], d2["s_w"], d2["z_w"], None)
+    check_y(ys[1], y_ref, bound, f"second of the pair M={M}")
     assert b.sync_status() == 0
 
 
@@ -812,7 +838,8 @@ def test_host_call_reuses_a_workspace_in_stream_order():
 def test_tape_counts_its_kernels():
     """w4a8_tape_kernels: the kernel launches one replay makes -- a fused call (pre-pass and
     contraction), a quantizing few-token call (one kernel), a decoder layer's four few-token
-    groups in one batch call (one launch), and the 7B-class pair as a batch (a launch each)."""
+    groups in one batch call (one launch), a pair of 3 MB of weights as a batch (one launch),
+    and the 7B-class pair as a batch (a launch each: 58.7 MB of weights)."""
     b = B()
     s = torch.cuda.Stream()
 
@@ -839,6 +866,8 @@ def test_tape_counts_its_kernels():
     assert count(lambda: b.prefill_linear(g["x"], g["wq"], g["s_w"], g["z_w"], g["bias"], stream=s)) == 1
     layer = b.Batch(ents(1, [(2048, 4096), (2048, 2048), (2048, 12288), (6144, 2048)], 82), s)
     assert count(lambda: layer.run(s)) == 1
+    small = b.Batch(ents(1, [(1024, 3072), (3072, 1024)], 84), s)
+    assert count(lambda: small.run(s)) == 1
     pair = b.Batch(ents(1, [(4096, 14336), (14336, 4096)], 86), s)
     assert count(lambda: pair.run(s)) == 2
     assert b.sync_status() == 0

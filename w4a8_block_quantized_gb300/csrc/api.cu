@@ -496,6 +496,7 @@ int w4a8_prefill_linear_batch(const w4a8_linear_ref* linears, int64_t count, int
         GemvArgs g[kGemvMaxLinears];
         int n = 0;
         bool one = true;
+        int64_t wbytes = 0;  // packed weights of all entries
         DeviceInfo* d = nullptr;
         int rc = current_device(&d);
         if (rc != W4A8_OK) return rc;
@@ -513,12 +514,16 @@ int w4a8_prefill_linear_batch(const w4a8_linear_ref* linears, int64_t count, int
             a.M = M;
             a.N = l.N;
             a.K = l.K;
+            wbytes += l.N * (l.K / 2);
             one = one && gemv_tile_rows(a, d->num_sms) >= 8;
         }
-        // Measured: a decoder layer's four groups (and its seven linears) run faster in one
-        // launch, the 7B-class pair slower (staging both long rows leaves two weight stages), so
-        // one launch from three entries on.
-        if (one && n >= 3 && gemv_batch_fits(g, n))
+        // Measured (one token unless noted), a launch per entry -> one launch: a decoder layer's
+        // seven linears 35 -> 21 us; pairs of 3 MB of weights (1024-deep) 14.3 -> 10.2, of
+        // 12.6 MB (2048/6144-deep) 18.4 -> 14.3, two 2048-deep linears at four tokens
+        // 20.5 -> 14.3; but the 7B-class pair (58.7 MB) 27.2 -> 28.8 on one box, where each of
+        // two launches has every SM and the second streams its weights during the first's tail.
+        // So one launch from three entries on, or for a pair of at most 24 MiB of weights.
+        if (one && (n >= 3 || (n == 2 && wbytes <= (int64_t(24) << 20))) && gemv_batch_fits(g, n))
             return launch_gemv_batch(g, n, d->num_sms, d->status, static_cast<cudaStream_t>(stream)) == cudaSuccess
                        ? W4A8_OK
                        : W4A8_ERR_CUDA;
