@@ -696,8 +696,8 @@ LAYER_GROUPS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
 def layer_step(lin, specs, stream, flush, reps, decode):
     """The 7-linear set run the way a decoder layer runs it: q/k/v and gate/up as
     row-concatenated groups on their shared inputs (4 linears).  Prefill: weights prepared
-    once at load time, per step one pre-pass and one contraction per group; decode: one
-    few-token call per group (one launch each).  Timed per step (L2 flushed before each,
+    once at load time, per step one pre-pass and one contraction per group; decode: the four
+    groups in one batch call (one few-token launch where they fit one).  Timed per step (L2 flushed before each,
     outside the events) as eager calls and replayed from a command tape."""
     from w4a8_block_quantized_gb300 import binding
     by = {t["spec"].name: t for t in lin}
