@@ -55,6 +55,26 @@ def record_prepass_bytes(M: int, K: int) -> int:
     return M * K * 4 + M * K * 2 + M * (K // 64) * 16 + 4 * M
 
 
+def fused_step_bytes(M: int, K: int, N: int, bias: bool):
+    """Bytes of one fused prefill call (w4a8_prefill_linear) two ways.
+    algorithmic: x read, the packed u4 weights and their fp16 scales and zeros read, bias read,
+    y written, each once.
+    as designed: what the call moves through its tensor-core records, each written once and read
+    back once (re-reads served by L2 not counted): the pre-pass reads x and writes the token
+    records (two e4m3 planes, 16-byte zero-point entries, s_a); its weight job reads the packed
+    weights, scales and zeros and writes the weight records (1 B per weight, 16-byte zero-point
+    entries per 64, rows padded to 128) and the fp32 scales; the contraction reads all of those
+    records and the bias and writes y."""
+    nb = K // 64
+    n_pad = (N + 127) // 128 * 128
+    packed = N * K // 2 + 2 * 2 * N * nb
+    algorithmic = 4 * M * K + packed + (4 * N if bias else 0) + 4 * M * N
+    tok_rec = M * K * 2 + M * nb * 16 + 4 * M
+    w_rec = n_pad * K + n_pad * nb * 16 + n_pad * nb * 4
+    designed = (4 * M * K + tok_rec) + (packed + w_rec) + (tok_rec + w_rec + (4 * N if bias else 0) + 4 * M * N)
+    return algorithmic, designed
+
+
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -594,6 +614,18 @@ def run_bench(args):
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
+    if not decode:
+        # the whole fused step's data movement over the step time: the bytes the method needs,
+        # and the bytes this design moves through its records (the weight expansion included)
+        alg, des = (sum(v) for v in zip(*(fused_step_bytes(s.M, s.K, s.N, s.bias) for s in specs)))
+        step_s = ms_per_step * 1e-3
+        out["step_bytes"] = {"algorithmic": alg, "as_designed": des, "ratio": round(des / alg, 3),
+                             "algorithmic_GBs": round(alg / step_s / 1e9, 1),
+                             "as_designed_GBs": round(des / step_s / 1e9, 1), "peak": hbm_gbs,
+                             "rule": "algorithmic: x, packed u4 weights, fp16 scales and zeros, bias read, y "
+                                     "written, once each; as designed: plus the token and weight records "
+                                     "written by the pre-pass and read by the contraction (weight rows padded "
+                                     "to 128; L2 re-reads not counted)"}
     if layer is not None:
         out["layer"] = layer
     if targets is not None:

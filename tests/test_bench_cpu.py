@@ -100,3 +100,23 @@ def test_committed_traffic_record_lists_the_included_headers():
                 for inc in re.findall(r'#include "([^"]+)"', f.read()):
                     todo.append(os.path.join(os.path.dirname(p), inc))
         assert seen == set(srcs), (e["kernel"], sorted(seen ^ set(srcs)))
+
+
+def test_fused_step_bytes_by_hand():
+    """The fused step's byte counts for the pp512 linear (M 512, K 1024, N 3072, bias), term by
+    term: x 2 MiB, packed weights 1.5 MiB, fp16 scales and zeros 192 KiB, bias 12 KiB, y 6 MiB;
+    token records 2 B per element + 16 B per 64 elements + 4 B per row, weight records 1 B per
+    weight + 16 B and a 4-byte scale per 64 (3072 rows, already a multiple of 128)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    M, K, N = 512, 1024, 3072
+    x, wq, sz, bias, y = 4 * M * K, N * K // 2, 2 * 2 * N * (K // 64), 4 * N, 4 * M * N
+    tok = 2 * M * K + 16 * M * (K // 64) + 4 * M
+    wrec = N * K + 16 * N * (K // 64) + 4 * N * (K // 64)
+    alg, des = bench.fused_step_bytes(M, K, N, True)
+    assert alg == x + wq + sz + bias + y == 10170368
+    assert des == (x + tok) + (wq + sz + wrec) + (tok + wrec + bias + y)
+    # rows padded to 128 in the weight records; no bias
+    alg2, des2 = bench.fused_step_bytes(1, 128, 130, False)
+    assert alg2 == 4 * 128 + 130 * 64 + 2 * 2 * 130 * 2 + 4 * 130
+    assert des2 - alg2 == 2 * (2 * 128 + 16 * 2 + 4) + 2 * (256 * 128 + 256 * 2 * 16 + 256 * 2 * 4)
