@@ -93,6 +93,12 @@ __device__ __forceinline__ void regs_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Named barrier `id` (1..15; 0 is __syncthreads) over `threads` threads (a multiple of 32):
+// a group of warps meets without waiting for the rest of the block.
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // Blocks until the grids this one depends on have completed and their memory is visible
 // (returns at once for a grid launched without a programmatic dependency).  What those grids
