@@ -19,6 +19,7 @@
 #include "sm103_ptx.cuh"
 #include "w4a8_internal.h"
 
+#include <atomic>
 #include <cuda_fp16.h>
 
 namespace w4a8 {
@@ -423,6 +424,21 @@ cudaError_t run_quant(const PrepArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// 256-thread CTAs of quant_kernel<G, V, PLANES> resident on one SM (its register use decides),
+// asked once per instantiation.
+template <int G, int V, bool PLANES>
+int ctas_per_sm() {
+    static std::atomic<int> n{0};
+    int v = n.load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, quant_kernel<G, V, PLANES, 8>, 256, 0) != cudaSuccess ||
+            v < 1)
+            v = 2;
+        n.store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
 // The row CTAs run_quant launches for G warps per row (8-warp CTAs).
 int64_t quant_row_ctas(int64_t M, int G) {
     const int64_t rpc = 8 / G, need = (M + rpc - 1) / rpc, cap = 152 * 2;
@@ -434,12 +450,14 @@ template <bool PLANES>
 cudaError_t dispatch_quant(const PrepArgs& a, cudaStream_t s) {
     const int64_t n4 = a.K / 4;
     // Short rows: more warps per row (shorter chains per lane, more SMs) while the whole launch,
-    // the weight job's CTAs included, still fits one wave of two 256-thread CTAs per SM.
-    // Measured at 128 and 512 rows of 1024: the pre-pass alone 8.2 -> 6.1 us with four warps per
-    // row; the fused call's launch (with its weight job) keeps one warp per row at 512 rows,
-    // where four would have spilled into a second wave and cost 0.8 us.
-    if (n4 <= 128 * 2 && quant_row_ctas(a.M, 4) + weight_ctas(a) <= 152 * 2) return run_quant<4, 2, PLANES>(a, s);
-    if (n4 <= 64 * 4 && quant_row_ctas(a.M, 2) + weight_ctas(a) <= 152 * 2) return run_quant<2, 4, PLANES>(a, s);
+    // the weight job's CTAs included, still fits one wave (as many 256-thread CTAs per SM as the
+    // instantiation's registers allow: three for four warps per row).  Measured at 128 and 512
+    // rows of 1024: the pre-pass alone 8.2 -> 6.1 us with four warps per row; the fused pp512
+    // call (512 rows, 192 weight-job CTAs: 448 CTAs in all) 18.1 -> 17.0 us per step.
+    if (n4 <= 128 * 2 && quant_row_ctas(a.M, 4) + weight_ctas(a) <= 152 * ctas_per_sm<4, 2, PLANES>())
+        return run_quant<4, 2, PLANES>(a, s);
+    if (n4 <= 64 * 4 && quant_row_ctas(a.M, 2) + weight_ctas(a) <= 152 * ctas_per_sm<2, 4, PLANES>())
+        return run_quant<2, 4, PLANES>(a, s);
     // smallest warp group G whose lanes hold the row in at most 8 float4 each (so the next
     // row can be prefetched): 1-8 warps of a 256-thread CTA, then the 16 warps of a 512-thread
     // CTA; past that, the two-pass kernel
