@@ -89,6 +89,8 @@ __device__ __forceinline__ uint32_t bytes4f(float4 q) {
     return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
 }
 
+constexpr int kWeightItems = 2;  // weight-job items a thread loads before it expands any
+
 __device__ __forceinline__ float h2f(uint16_t bits) { return __half2float(__ushort_as_half(bits)); }
 
 // The sums of H values (H in {1, 2, 4}) over each 16-lane half of the warp, reduced together:
@@ -132,43 +134,61 @@ __device__ __forceinline__ float half_warp_sums(const float (&p)[H], int lane, i
 // exact) with 12 zero bytes, and 512 s_w[n,b] (fp32, into the scale array; the power of two
 // undoes the 2^-9 scale of the e4m3 weight operand); zeros for rows past N.
 __device__ void weights_job(const PrepArgs& a, int64_t cta, int64_t ctas) {
+    constexpr int U = kWeightItems;
     const int64_t nb = a.K / kBlock;
     const int64_t tiles = (a.N + kTileW - 1) / kTileW;
     const int64_t total = tiles * nb * kTileW;
     const int64_t stride = ctas * blockDim.x;
-    for (int64_t i = cta * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const int64_t rb = i >> 7;  // record index: tile * nb + b
-        const int r = static_cast<int>(i & 127);
-        const int64_t n = (rb / nb) * kTileW + r;
-        const int64_t b = rb - (rb / nb) * nb;
-        uint8_t* rec = a.wrec + rb * kWRec;
-        uint4 o[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
-                      make_uint4(0u, 0u, 0u, 0u)};
-        if (n < a.N) {
-            const uint4* src = reinterpret_cast<const uint4*>(a.wq + (a.n_first + n) * (a.K / 2) + b * 32);
-            const uint4 w0 = __ldcs(src), w1 = __ldcs(src + 1);
-            expand8(w0.x, o[0].x, o[0].y);
-            expand8(w0.y, o[0].z, o[0].w);
-            expand8(w0.z, o[1].x, o[1].y);
-            expand8(w0.w, o[1].z, o[1].w);
-            expand8(w1.x, o[2].x, o[2].y);
-            expand8(w1.y, o[2].z, o[2].w);
-            expand8(w1.z, o[3].x, o[3].y);
-            expand8(w1.w, o[3].z, o[3].w);
-        }
-        const int sw = (r >> 1) & 3;
+    // U items per thread, i0 + u * stride: every load of the U items goes out before the first
+    // expansion, so their latencies overlap
+    for (int64_t i0 = cta * blockDim.x + threadIdx.x; i0 < total; i0 += stride * U) {
+        uint4 w0[U], w1[U];
+        uint16_t sh[U], zh[U];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(rec + r * 64 + ((c ^ sw) << 4)) = o[c];
-        if (a.s_w) {
-            float sv = 0.0f;
-            uint32_t zz = 0u;
-            if (n < a.N) {
-                const int64_t src = (a.n_first + n) * nb + b;
-                sv = 512.0f * h2f(a.s_w[src]);
-                zz = neg_zero_pair(a.z_w[src]);
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = i0 + u * stride;
+            const int64_t rb = i >> 7;
+            const int64_t n = (rb / nb) * kTileW + (i & 127);
+            const int64_t b = rb - (rb / nb) * nb;
+            w0[u] = w1[u] = make_uint4(0u, 0u, 0u, 0u);
+            sh[u] = zh[u] = 0;
+            if (i < total && n < a.N) {
+                const uint4* src = reinterpret_cast<const uint4*>(a.wq + (a.n_first + n) * (a.K / 2) + b * 32);
+                w0[u] = __ldcs(src);
+                w1[u] = __ldcs(src + 1);
+                if (a.s_w) {
+                    const int64_t sidx = (a.n_first + n) * nb + b;
+                    sh[u] = a.s_w[sidx];
+                    zh[u] = a.z_w[sidx];
+                }
             }
-            *reinterpret_cast<uint4*>(rec + kWZx + r * 16) = make_uint4(zz, 0u, 0u, 0u);
-            a.sc[i] = sv;  // [tile][b][r]: the same linear index as the thread's item
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i >= total) break;
+            const int64_t rb = i >> 7;
+            const int r = static_cast<int>(i & 127);
+            const int64_t n = (rb / nb) * kTileW + r;
+            uint8_t* rec = a.wrec + rb * kWRec;
+            uint4 o[4];
+            expand8(w0[u].x, o[0].x, o[0].y);
+            expand8(w0[u].y, o[0].z, o[0].w);
+            expand8(w0[u].z, o[1].x, o[1].y);
+            expand8(w0[u].w, o[1].z, o[1].w);
+            expand8(w1[u].x, o[2].x, o[2].y);
+            expand8(w1[u].y, o[2].z, o[2].w);
+            expand8(w1[u].z, o[3].x, o[3].y);
+            expand8(w1[u].w, o[3].z, o[3].w);
+            const int sw = (r >> 1) & 3;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(rec + r * 64 + ((c ^ sw) << 4)) = o[c];
+            if (a.s_w) {
+                const bool live = n < a.N;
+                *reinterpret_cast<uint4*>(rec + kWZx + r * 16) =
+                    make_uint4(live ? neg_zero_pair(zh[u]) : 0u, 0u, 0u, 0u);
+                a.sc[i] = live ? 512.0f * h2f(sh[u]) : 0.0f;  // [tile][b][r]: the item's linear index
+            }
         }
     }
 }
@@ -410,6 +430,35 @@ int weight_ctas(const PrepArgs& a) {
     return static_cast<int>(c < 152 * 8 ? c : 152 * 8);
 }
 
+// CTAs of quant_kernel<G, V, PLANES, NW> resident on one SM (its register use decides), asked
+// once per instantiation.
+template <int G, int V, bool PLANES, int NW = 8>
+int ctas_per_sm() {
+    static std::atomic<int> n{0};
+    int v = n.load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, quant_kernel<G, V, PLANES, NW>, NW * 32, 0) !=
+                cudaSuccess ||
+            v < 1)
+            v = 1;
+        n.store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// The weight job's CTAs beside `row_ctas` row CTAs when the SMs hold `slots` CTAs at once: one
+// item per thread while the whole launch fits one wave, else two (loaded together), which
+// halves the CTAs that queue behind the row CTAs.  Measured on the fused call: the 7B-class
+// pair 814 -> 802 and 939 -> 911 us, the 512-row linears unchanged; two items per thread on
+// the pp512 linear, which fits one wave, had cost 17.0 -> 19.1 us, so it keeps one.
+int weight_ctas_fit(const PrepArgs& a, int64_t row_ctas, int64_t slots) {
+    const int64_t one = weight_ctas(a);
+    if (row_ctas + one <= slots) return static_cast<int>(one);
+    const int64_t items = ((a.N + kTileW - 1) / kTileW) * (a.K / kBlock) * kTileW;
+    const int64_t c = (items + 256 * kWeightItems - 1) / (256 * kWeightItems);
+    return static_cast<int>(c < 152 * 8 ? c : 152 * 8);
+}
+
 template <int G, int V, bool PLANES, int NW = 8>
 cudaError_t run_quant(const PrepArgs& a, cudaStream_t s) {
     constexpr int RPC = NW / G;
@@ -419,24 +468,9 @@ cudaError_t run_quant(const PrepArgs& a, cudaStream_t s) {
     constexpr int64_t cap = NW == 8 ? 152 * 2 : 152;
     const int64_t iters = (need + cap - 1) / cap;
     const int row_ctas = static_cast<int>(iters > 0 ? (need + iters - 1) / iters : 1);
-    const int grid = row_ctas + weight_ctas(a);
+    const int grid = row_ctas + weight_ctas_fit(a, row_ctas, 152 * ctas_per_sm<G, V, PLANES, NW>());
     quant_kernel<G, V, PLANES, NW><<<grid, NW * 32, 0, s>>>(a, row_ctas);
     return cudaGetLastError();
-}
-
-// 256-thread CTAs of quant_kernel<G, V, PLANES> resident on one SM (its register use decides),
-// asked once per instantiation.
-template <int G, int V, bool PLANES>
-int ctas_per_sm() {
-    static std::atomic<int> n{0};
-    int v = n.load(std::memory_order_relaxed);
-    if (v == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, quant_kernel<G, V, PLANES, 8>, 256, 0) != cudaSuccess ||
-            v < 1)
-            v = 2;
-        n.store(v, std::memory_order_relaxed);
-    }
-    return v;
 }
 
 // The row CTAs run_quant launches for G warps per row (8-warp CTAs).
