@@ -89,7 +89,12 @@ __device__ __forceinline__ uint32_t bytes4f(float4 q) {
     return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
 }
 
-constexpr int kWeightItems = 2;  // weight-job items a thread loads before it expands any
+// Weight-job items a thread loads before it expands any.  The job has one item per thread up
+// to 152 * 8 CTAs; past that cap each thread loops over several, and loading two at a time
+// overlaps their latencies.  Measured on the 7B-class pair's fused calls (2.9 items per thread):
+// 814 -> 802 and 939 -> 911 us.  (Halving the CTAs to give every thread two items had cost the
+// 512-row linears of a decoder layer 0.6 us each.)
+constexpr int kWeightItems = 2;
 
 __device__ __forceinline__ float h2f(uint16_t bits) { return __half2float(__ushort_as_half(bits)); }
 
@@ -446,19 +451,6 @@ int ctas_per_sm() {
     return v;
 }
 
-// The weight job's CTAs beside `row_ctas` row CTAs when the SMs hold `slots` CTAs at once: one
-// item per thread while the whole launch fits one wave, else two (loaded together), which
-// halves the CTAs that queue behind the row CTAs.  Measured on the fused call: the 7B-class
-// pair 814 -> 802 and 939 -> 911 us, the 512-row linears unchanged; two items per thread on
-// the pp512 linear, which fits one wave, had cost 17.0 -> 19.1 us, so it keeps one.
-int weight_ctas_fit(const PrepArgs& a, int64_t row_ctas, int64_t slots) {
-    const int64_t one = weight_ctas(a);
-    if (row_ctas + one <= slots) return static_cast<int>(one);
-    const int64_t items = ((a.N + kTileW - 1) / kTileW) * (a.K / kBlock) * kTileW;
-    const int64_t c = (items + 256 * kWeightItems - 1) / (256 * kWeightItems);
-    return static_cast<int>(c < 152 * 8 ? c : 152 * 8);
-}
-
 template <int G, int V, bool PLANES, int NW = 8>
 cudaError_t run_quant(const PrepArgs& a, cudaStream_t s) {
     constexpr int RPC = NW / G;
@@ -468,7 +460,7 @@ cudaError_t run_quant(const PrepArgs& a, cudaStream_t s) {
     constexpr int64_t cap = NW == 8 ? 152 * 2 : 152;
     const int64_t iters = (need + cap - 1) / cap;
     const int row_ctas = static_cast<int>(iters > 0 ? (need + iters - 1) / iters : 1);
-    const int grid = row_ctas + weight_ctas_fit(a, row_ctas, 152 * ctas_per_sm<G, V, PLANES, NW>());
+    const int grid = row_ctas + weight_ctas(a);
     quant_kernel<G, V, PLANES, NW><<<grid, NW * 32, 0, s>>>(a, row_ctas);
     return cudaGetLastError();
 }
