@@ -444,8 +444,12 @@ int ctas_per_sm() {
     if (v == 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, quant_kernel<G, V, PLANES, NW>, NW * 32, 0) !=
                 cudaSuccess ||
-            v < 1)
-            v = 1;
+            v < 1) {
+            // not remembered, and cleared, so that the launch that follows reports only its own
+            // status: two per SM, what these kernels' launch bounds guarantee for 256 threads
+            (void)cudaGetLastError();
+            return NW == 8 ? 2 : 1;
+        }
         n.store(v, std::memory_order_relaxed);
     }
     return v;
